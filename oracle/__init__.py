@@ -1,0 +1,118 @@
+"""CPU oracle of the mHC site program -- TEST INFRASTRUCTURE.
+
+Only tests/, __graft_entry__.smoke() and bench.py's CPU-baseline leg may import
+this package.  The CUDA library and its Python binding never do, and this
+package imports nothing from them.  It wraps oracle/hc_oracle.c (float64 plain
+loops, one token at a time; see that file's header for the formulas and the
+pages they follow).  Inputs may be float32 or float64 arrays; they are widened
+to float64 before the call, so float32 inputs are used bit-for-bit.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+from . import build as _build
+
+_lib = None
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        path = _build.build()
+        lib = ctypes.CDLL(path)
+        dp = ctypes.POINTER(ctypes.c_double)
+        lib.hco_pre.argtypes = [dp, dp, dp, dp, ctypes.c_long, ctypes.c_int, ctypes.c_long,
+                                ctypes.c_int, ctypes.c_double, dp, dp, dp, dp, dp, dp, ctypes.c_int]
+        lib.hco_post.argtypes = [dp, dp, dp, dp, dp, ctypes.c_long, ctypes.c_int, ctypes.c_long,
+                                 ctypes.c_int]
+        lib.hco_expand.argtypes = [dp, dp, ctypes.c_long, ctypes.c_int, ctypes.c_long]
+        lib.hco_mean.argtypes = [dp, dp, ctypes.c_long, ctypes.c_int, ctypes.c_long]
+        for fn in (lib.hco_pre, lib.hco_post, lib.hco_expand, lib.hco_mean):
+            fn.restype = ctypes.c_int
+        lib.hco_max_threads.restype = ctypes.c_int
+        _lib = lib
+    return _lib
+
+
+def _f64(a) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(a), dtype=np.float64)
+
+
+def _p(a: np.ndarray | None):
+    if a is None:
+        return None
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+
+
+def max_threads() -> int:
+    return int(_load().hco_max_threads())
+
+
+def default_threads() -> int:
+    return max(1, min(max_threads(), os.cpu_count() or 1))
+
+
+def pre(x, fn_w, scale, base, iters: int, eps: float, want_mixes: bool = False,
+        threads: int | None = None):
+    """Pre-chain of one site.  x [T, s, d] -> dict(pre [T,s], post [T,s], comb [T,s,s],
+    y [T,d], and with want_mixes also mixes [T,R] (rescaled) and logits [T,R])."""
+    x = _f64(x)
+    T, s, d = x.shape
+    R = (2 + s) * s
+    fn_w = _f64(fn_w).reshape(R, s * d)
+    scale, base = _f64(scale).reshape(3), _f64(base).reshape(R)
+    out = dict(pre=np.empty((T, s)), post=np.empty((T, s)), comb=np.empty((T, s, s)),
+               y=np.empty((T, d)))
+    mixes = np.empty((T, R)) if want_mixes else None
+    logits = np.empty((T, R)) if want_mixes else None
+    rc = _load().hco_pre(_p(x), _p(fn_w), _p(scale), _p(base), T, s, d, int(iters), float(eps),
+                         _p(out["pre"]), _p(out["post"]), _p(out["comb"]), _p(out["y"]),
+                         _p(mixes), _p(logits), threads or default_threads())
+    if rc != 0:
+        raise ValueError(f"hco_pre failed with code {rc}")
+    if want_mixes:
+        out["mixes"], out["logits"] = mixes, logits
+    return out
+
+
+def post(x, f, post_gates, comb, threads: int | None = None) -> np.ndarray:
+    """hc_post: x [T,s,d], f [T,d], post [T,s], comb [T,s,s] -> x' [T,s,d]."""
+    x = _f64(x)
+    T, s, d = x.shape
+    f, pg, cb = _f64(f).reshape(T, d), _f64(post_gates).reshape(T, s), _f64(comb).reshape(T, s, s)
+    out = np.empty((T, s, d))
+    rc = _load().hco_post(_p(x), _p(f), _p(pg), _p(cb), _p(out), T, s, d,
+                          threads or default_threads())
+    if rc != 0:
+        raise ValueError(f"hco_post failed with code {rc}")
+    return out
+
+
+def expand(emb, s: int) -> np.ndarray:
+    emb = _f64(emb)
+    T, d = emb.shape
+    out = np.empty((T, s, d))
+    if _load().hco_expand(_p(emb), _p(out), T, s, d) != 0:
+        raise ValueError("hco_expand failed")
+    return out
+
+
+def mean(x) -> np.ndarray:
+    x = _f64(x)
+    T, s, d = x.shape
+    out = np.empty((T, d))
+    if _load().hco_mean(_p(x), _p(out), T, s, d) != 0:
+        raise ValueError("hco_mean failed")
+    return out
+
+
+def site(x, fn_w, scale, base, f, iters: int, eps: float, threads: int | None = None):
+    """One whole site: pre-chain, then hc_post with the given branch output f."""
+    r = pre(x, fn_w, scale, base, iters, eps, threads=threads)
+    r["x_out"] = post(x, f, r["post"], r["comb"], threads=threads)
+    return r
