@@ -1,0 +1,469 @@
+#!/usr/bin/env python3
+"""Benchmark of the mHC site program on GB300.
+
+A step is one pass of the whole site program -- hc_pre_fused (RMS-rescaled
+mixes contraction, gates, Sinkhorn, collapse) then hc_post -- over one batch of
+synthetic tokens already resident in HBM.  The default workload is the prefill
+chunk (T = 4096 tokens, s = 4 streams, hidden 4096, 20 Sinkhorn iterations,
+eps 1e-6): its 256 MiB stream state is larger than L2, so every step streams
+from HBM without a flush.  The JSON line also carries the T = 1 decode latency
+per site (CUDA-graph replay of back-to-back sites).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
+
+With --gpus N > 1 the script expects torchrun: each rank runs its own batch on
+its own GPU (weak scaling, no collective on the data path); value is the tokens
+of all ranks over the slowest rank's time.  --impl reference times the float64
+CPU oracle on the host cores instead (rank 0 only).
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from mhc_hyper_connection_hc_gb300 import synth  # noqa: E402
+
+METRIC = "mHC site tokens/s + achieved HBM GB/s (fraction of roofline); T=1 µs/site"
+FALLBACK_HBM_GBS = 6800.0        # used only when MEASURED_PEAKS.json is absent
+FALLBACK_NOTE = "of fallback (6.8 TB/s, one earlier GB300 measurement)"
+GB300_SMS, GB300_MAX_MHZ, FP32_LANES = 152, 2070, 128
+WORKLOAD_IDS = {"decode": 1, "verify": 2, "prefill": 3, "sweep": 4, "wide": 5}
+
+
+# ----------------------------------------------------------------------------- host helpers
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    return int(os.environ.get("RANK", "0")), ws, int(os.environ.get("LOCAL_RANK", "0"))
+
+
+def aggregate(elapsed_s: float, units: float, group=None):
+    """Max elapsed and summed units over ranks (identity without torch.distributed)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return elapsed_s, units
+    t = torch.tensor([elapsed_s], dtype=torch.float64)
+    u = torch.tensor([units], dtype=torch.float64)
+    if dist.get_backend(group) == "nccl":
+        t, u = t.cuda(), u.cuda()
+    dist.all_reduce(t, op=dist.ReduceOp.MAX, group=group)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM, group=group)
+    return float(t.item()), float(u.item())
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if not os.path.exists(p):
+        return None
+    try:
+        return json.load(open(p))
+    except (OSError, ValueError):
+        return None
+
+
+def hbm_peak(kind: str):
+    """(GB/s, note): the measured copy bandwidth, else the fallback."""
+    mp = measured_peaks()
+    if mp:
+        for key in (f"hbm_gbs_{kind}", "hbm_gbs"):
+            if isinstance(mp.get(key), (int, float)):
+                return float(mp[key]), f"of measured ({key})"
+    return FALLBACK_HBM_GBS, FALLBACK_NOTE
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "mhc_hyper_connection_hc_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as fh:
+            h.update(name.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from a committed ncu summary, only if taken on the
+    current kernel sources (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(path):
+        return None
+    want = kernel_source_hash()
+    for line in open(path):
+        parts = line.split()
+        if len(parts) == 4 and parts[0] == kernel and parts[1] == workload and parts[3] == want:
+            return float(parts[2])
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms in the background."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, ValueError):
+            self.proc = None
+        time.sleep(0.25)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or not self.path or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        os.unlink(self.path)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- CPU oracle timing
+
+def time_oracle(w: synth.Workload, max_tokens: int, budget_s: float, max_reps: int):
+    """Time the float64 oracle (pre + post) on a bounded sample of the workload."""
+    import oracle
+    n = min(w.T, max_tokens)
+    inp = synth.workload_inputs(w, T=n)
+    x = inp["x"].astype(np.float64)
+    f = inp["f"].astype(np.float64)
+    threads = oracle.default_threads()
+    eps = float(np.float32(w.eps))
+    times = []
+    t_start = time.perf_counter()
+    while len(times) < max_reps and (not times or time.perf_counter() - t_start < budget_s):
+        t0 = time.perf_counter()
+        oracle.site(x, inp["fn_w"], inp["scale"], inp["base"], f, w.iters, eps, threads=threads)
+        times.append(time.perf_counter() - t0)
+    best = min(times)
+    return {"value": n / best, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "sample": f"{n} of {w.T} tokens of the {w.name} workload (s={w.s}, d={w.d}, "
+                      f"iters={w.iters}), pre-chain + hc_post in float64, best of {len(times)} "
+                      f"runs, inputs pre-widened to float64 outside the timed call",
+            "seconds_per_run": best}
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    w = synth.WORKLOADS[WORKLOAD_IDS[args.workload]]
+    sample = min(w.T, args.ref_tokens)
+    for _ in range(args.warmup):
+        time_oracle(w, max_tokens=min(sample, 64), budget_s=0.0, max_reps=1)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        cb = time_oracle(w, max_tokens=sample, budget_s=0.0, max_reps=1)
+    elapsed = time.perf_counter() - t0
+    value = sample * args.steps / elapsed
+    cb["value"] = value
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * elapsed / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": workload_config(w, sample_tokens=sample),
+            "cpu_baseline": cb,
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(w: synth.Workload, sample_tokens=None):
+    cfg = {"workload": f"{w.name}: T={w.T} tokens, streams={w.s}, hidden={w.d}, "
+                       f"{w.iters} Sinkhorn iters, eps={w.eps:g}",
+           "T": w.T, "streams": w.s, "hidden": w.d, "rows": w.R, "iters": w.iters, "eps": w.eps,
+           "x_dist": "U[-1,1)" if w.x_dist == "uniform" else "N(0,1)",
+           "l2": f"inputs larger than L2: x is {w.T * w.K * 4 / 2**20:.0f} MiB per step, no flush"
+                 if w.T * w.K * 4 > 129e6 else "inputs fit in L2 (latency workload)"}
+    if sample_tokens is not None:
+        cfg["tokens_per_step_sampled"] = sample_tokens
+    return cfg
+
+
+# ----------------------------------------------------------------------------- GPU arm
+
+def run_gpu(args):
+    import torch
+    from mhc_hyper_connection_hc_gb300 import hc
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    w = synth.WORKLOADS[WORKLOAD_IDS[args.workload]]
+    T, s, d, iters = w.T, w.s, w.d, w.iters
+    stream = torch.cuda.Stream(device=dev)
+
+    inp = synth.workload_inputs(w)
+    with torch.cuda.stream(stream):
+        dv = {k: torch.from_numpy(v).to(dev) for k, v in inp.items()}
+        ws = hc.new_workspace(T, s, d, dev, stream)
+        out = hc.new_pre_outputs(T, s, d, dev)
+        x_out = torch.empty(T, s, d, dtype=torch.float32, device=dev)
+    stream.synchronize()
+    path = hc.hc_pre_auto_path(T, s, d)
+    pre_launches = 1 if path == hc.HC_PATH_CLUSTER else 2
+
+    def pre():
+        hc.hc_pre_fused(dv["x"], dv["fn_w"], dv["scale"], dv["base"], iters, w.eps, out["pre"],
+                        out["post"], out["comb"], out["y"], ws, stream)
+
+    def post():
+        hc.hc_post(dv["x"], dv["f"], out["post"], out["comb"], x_out, stream)
+
+    for _ in range(args.warmup):
+        pre()
+        post()
+    stream.synchronize()
+    if hc.hc_workspace_status(ws, stream) != 0:
+        raise RuntimeError("a kernel flagged an error during warm-up")
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(dev.index if dev.index is not None else 0) as clk:
+        for k in range(K):
+            ev[k][0].record(stream)
+            pre()
+            ev[k][1].record(stream)
+            post()
+            ev[k][2].record(stream)
+        stream.synchronize()
+    torch.cuda.synchronize(dev)
+    barrier()
+    clocks = clk.summary()
+    total_s = ev[0][0].elapsed_time(ev[-1][2]) / 1e3
+    pre_ms = [ev[k][0].elapsed_time(ev[k][1]) for k in range(K)]
+    post_ms = [ev[k][1].elapsed_time(ev[k][2]) for k in range(K)]
+    if hc.hc_workspace_status(ws, stream) != 0:
+        raise RuntimeError("a kernel flagged an error in the timed region")
+    max_s, all_tokens = aggregate(total_s, float(T * K))
+
+    # Roofline of the dominant kernel (algorithmic bytes per launch / mean launch time).
+    pre_bytes = T * s * d * 4 + T * d * 4                 # x read once, y written
+    post_bytes = T * s * d * 4 * 2 + T * d * 4            # x and f read, x' written
+    pre_flops = 2 * w.R * w.K * T + 2 * w.K * T + 2 * w.K * T
+    pre_avg, post_avg = statistics.mean(pre_ms) / 1e3, statistics.mean(post_ms) / 1e3
+    peak, note = hbm_peak("burst")
+    fp32_peak = GB300_SMS * FP32_LANES * 2 * (clocks.get("sm_mhz") or GB300_MAX_MHZ) * 1e6 / 1e12
+    src_hash = kernel_source_hash()
+    wl_tag = f"T{T}_s{s}_d{d}"
+    kernels = {
+        "hc_pre_fused": {"us": pre_avg * 1e6, "algorithmic_bytes": pre_bytes,
+                         "GB/s": pre_bytes / pre_avg / 1e9, "frac_hbm": pre_bytes / pre_avg / 1e9 / peak,
+                         "TFLOP/s": pre_flops / pre_avg / 1e12,
+                         "frac_fp32": pre_flops / pre_avg / 1e12 / fp32_peak,
+                         "launches_per_step": pre_launches,
+                         "path": "cluster" if path == hc.HC_PATH_CLUSTER else "generic"},
+        "hc_post": {"us": post_avg * 1e6, "algorithmic_bytes": post_bytes,
+                    "GB/s": post_bytes / post_avg / 1e9, "frac_hbm": post_bytes / post_avg / 1e9 / peak,
+                    "launches_per_step": 1},
+    }
+    dom = max(kernels, key=lambda k: kernels[k]["us"])
+    kd = kernels[dom]
+    roofline = {"bound": "hbm", "kernel": dom, "achieved": kd["GB/s"], "peak": peak, "unit": "GB/s",
+                "frac": kd["GB/s"] / peak, "peak_note": note,
+                "traffic": profiled_traffic(dom, wl_tag),
+                "algorithmic_bytes_per_launch": kd["algorithmic_bytes"]}
+
+    line = {"metric": METRIC, "value": all_tokens / max_s, "unit": "tokens/s", "n_gpus": world,
+            "steps": K, "warmup": args.warmup, "ms_per_step": 1e3 * max_s / K,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic", "config": workload_config(w), "roofline": roofline,
+            "kernels": kernels, "gpu_launches": (pre_launches + 1) * K, "clocks": clocks,
+            "kernel_sources": src_hash}
+
+    if not args.no_e2e:
+        line["e2e"] = measure_e2e(w, dv, ws, out, x_out, stream, K, pre, post)
+    if not args.no_decode:
+        line["decode_t1"] = measure_decode(dev)
+    if rank == 0 and world == 1 and not args.no_cpu:
+        line["cpu_baseline"] = time_oracle(w, max_tokens=args.cpu_tokens, budget_s=10.0, max_reps=3)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def measure_e2e(w, dv, ws, out, x_out, stream, K, pre, post):
+    """The same step through the C ABI with HOST buffers: pinned host -> device
+    copies of x and f, the site, and the device -> host read of every output."""
+    import torch
+    host_in = {k: dv[k].cpu().pin_memory() for k in ("x", "f")}
+    host_out = {"x_out": torch.empty_like(x_out, device="cpu").pin_memory()}
+    for k, v in out.items():
+        host_out[k] = torch.empty_like(v, device="cpu").pin_memory()
+    h2d = sum(t.numel() * 4 for t in host_in.values())
+    d2h = sum(t.numel() * 4 for t in host_out.values())
+
+    def step():
+        dv["x"].copy_(host_in["x"], non_blocking=True)
+        dv["f"].copy_(host_in["f"], non_blocking=True)
+        pre()
+        post()
+        host_out["x_out"].copy_(x_out, non_blocking=True)
+        for k, v in out.items():
+            host_out[k].copy_(v, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            step()
+        stream.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(K):
+            step()
+        e1.record(stream)
+        stream.synchronize()
+    sec = e0.elapsed_time(e1) / 1e3
+    return {"value": w.T * K / sec, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": 1e3 * sec / K}
+
+
+def measure_decode(dev, n_sites: int = 300):
+    """T = 1 site latency: 300 back-to-back sites (pre + post) replayed as one CUDA
+    graph, and the same launches issued eagerly on a stream."""
+    import torch
+    from mhc_hyper_connection_hc_gb300 import hc
+    w = synth.WORKLOADS[1]
+    inp = synth.workload_inputs(w)
+    stream = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(stream):
+        dv = {k: torch.from_numpy(v).to(dev) for k, v in inp.items()}
+        ws = hc.new_workspace(1, w.s, w.d, dev, stream)
+        out = hc.new_pre_outputs(1, w.s, w.d, dev)
+        xo = torch.empty(1, w.s, w.d, device=dev)
+    stream.synchronize()
+
+    def site():
+        hc.hc_pre_fused(dv["x"], dv["fn_w"], dv["scale"], dv["base"], w.iters, w.eps, out["pre"],
+                        out["post"], out["comb"], out["y"], ws, stream)
+        hc.hc_post(dv["x"], dv["f"], out["post"], out["comb"], xo, stream)
+
+    def pre_only():
+        hc.hc_pre_fused(dv["x"], dv["fn_w"], dv["scale"], dv["base"], w.iters, w.eps, out["pre"],
+                        out["post"], out["comb"], out["y"], ws, stream)
+
+    res = {}
+    for name, fn in (("site", site), ("pre", pre_only)):
+        with torch.cuda.stream(stream):
+            for _ in range(20):
+                fn()
+            stream.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(n_sites):
+                fn()
+            e1.record(stream)
+            stream.synchronize()
+            res[f"us_per_{name}_stream"] = e0.elapsed_time(e1) * 1e3 / n_sites
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for _ in range(n_sites):
+                    fn()
+            g.replay()
+            stream.synchronize()
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+            stream.synchronize()
+            res[f"us_per_{name}_graph"] = e0.elapsed_time(e1) * 1e3 / n_sites
+    # single launch + synchronize wall (the pages' gate measured this way, with allocations)
+    walls = []
+    for _ in range(20):
+        torch.cuda.synchronize(dev)
+        t0 = time.perf_counter()
+        site()
+        stream.synchronize()
+        walls.append((time.perf_counter() - t0) * 1e6)
+    res["us_per_site_wall_sync"] = statistics.median(walls)
+    if hc.hc_workspace_status(ws, stream) != 0:
+        raise RuntimeError("a kernel flagged an error in the decode measurement")
+    res["path"] = "cluster" if hc.hc_pre_auto_path(1, w.s, w.d) == hc.HC_PATH_CLUSTER else "generic"
+    return res
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("gb300", "reference"), default="gb300")
+    ap.add_argument("--workload", choices=tuple(WORKLOAD_IDS), default="prefill")
+    ap.add_argument("--cpu-tokens", type=int, default=4096, help="tokens of the CPU-oracle sample")
+    ap.add_argument("--ref-tokens", type=int, default=256, help="tokens per reference-arm step")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    rank, world, _ = dist_env()
+    if args.gpus != world and world > 1:
+        ap.error(f"--gpus {args.gpus} but WORLD_SIZE={world}")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,162 @@
+/*
+ * hc.h -- C ABI of the GB300 (sm_103a) mHC site-program library.
+ *
+ * mHC (manifold-constrained hyper-connections) carries a residual stream state
+ * x[T, s, d] of s parallel streams per token.  Each site (attention, then MLP,
+ * of every layer) runs, per token, the program given in the module header of
+ * the memra-engine "hyper.rs" page ("ARITHMETIC CONTRACT"):
+ *
+ *   mixes[t, :]   = fn_w . x[t, :, :]                  rows R = (2+s)*s
+ *   mixes[t, :]  *= rsqrt(mean(x[t]^2) + eps)          over the whole s*d slab
+ *   pre/post/comb = sinkhorn(mixes[t, :], scale, base)
+ *   y[t, :]       = sum_c pre[t, c] * x[t, c, :]
+ *   f             = branch(rms_norm(y))                (not part of this library)
+ *   x'[t, k, :]   = post[t, k] * f[t, :] + sum_j comb[t, j, k] * x[t, j, :]
+ *
+ * The split, which the pages never print, is read as:
+ *   logit[r] = mixes[r] * scale[g(r)] + base[r], g = 0 for the s pre rows,
+ *              1 for the s post rows, 2 for the s*s comb rows (that row order);
+ *   pre  = sigmoid(logit) + eps,  post = 2 * sigmoid(logit),
+ *   comb = exp(logit[2s + j*s + k]) then `iters` rounds of (divide each row by
+ *          its sum + eps; divide each column by its sum + eps).
+ *
+ * Conventions (all entry points):
+ *   - Layout is token-major: element (t, k, i) of a [T, s, d] state is at
+ *     (t*s + k)*d + i, so one token's s*d slab is contiguous (hyper.rs module
+ *     header, "MEMORY LAYOUT").  fn_w is row-major [R, s*d].
+ *   - Every tensor pointer is a DEVICE pointer to float32 owned by the caller.
+ *     The library never allocates, never frees and never synchronises; all
+ *     work is enqueued on `stream` (a cudaStream_t; NULL = legacy default).
+ *   - Outputs are fully overwritten; inputs are never written.
+ *   - Arguments are validated on the host before anything is launched; a
+ *     non-zero return means nothing was enqueued, except HC_ERR_CUDA, which
+ *     reports the error of the launch itself.
+ *   - T == 0 is a valid empty batch: nothing is launched and HC_OK returned.
+ *   - Limits: 1 <= s <= 8 (the pages' fused kernels size their shared arrays
+ *     for hc <= 8), d >= 4 and d % 4 == 0, iters >= 1, eps > 0 and finite
+ *     (HyperTopology::from_plan refuses streams == 0, epsilon <= 0 and zero
+ *     iterations), T*s*d < 2^31.
+ *   - Pointers to x, fn_w, y, f, x_out, emb and out must be 16-byte aligned
+ *     (vector and bulk-copy access); pre, post, comb, scale and base 4-byte.
+ */
+#ifndef MHC_GB300_HC_H
+#define MHC_GB300_HC_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum hc_status {
+    HC_OK = 0,
+    HC_ERR_NULL = 1,        /* a required pointer is NULL                            */
+    HC_ERR_DIM = 2,         /* T, s, d, iters or eps outside the limits above        */
+    HC_ERR_ALIGN = 3,       /* pointer misaligned, or d % 4 != 0                     */
+    HC_ERR_ALIAS = 4,       /* an output overlaps an input or another output         */
+    HC_ERR_WORKSPACE = 5,   /* workspace NULL or smaller than hc_pre_workspace_bytes */
+    HC_ERR_CUDA = 6,        /* the CUDA runtime reported an error                    */
+    HC_ERR_DEVICE = 7,      /* a kernel flagged an error in the workspace status word */
+    HC_ERR_UNSUPPORTED = 8  /* the requested kernel path cannot run this shape here  */
+};
+
+/* Kernel paths of hc_pre_fused_path. */
+enum hc_pre_path {
+    HC_PATH_AUTO = 0,     /* what hc_pre_fused runs                                   */
+    HC_PATH_GENERIC = 1,  /* any supported shape: split-K mixes kernel + finish kernel */
+    HC_PATH_CLUSTER = 2   /* one fused launch, x read once: thread-block clusters split
+                             the hidden dimension; needs s <= 4 and s*d <= 16384 with
+                             d % 64 == 0                                               */
+};
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char *hc_status_string(int rc);
+
+/*
+ * hc_expand -- model entry: [T, d] embeddings -> [T, s, d] stream state, every
+ * stream a copy of the token's embedding (hyper.rs `expand`; the pages give
+ * only the shapes, replication is the reading used).
+ *   emb [T, d] (in), x [T, s, d] (out, must not overlap emb).
+ */
+int hc_expand(const float *emb, float *x, int T, int s, int d, void *stream);
+
+/*
+ * Bytes of device workspace hc_pre_fused needs for this shape.  The workspace
+ * holds a status word (first 256 bytes) and, on the generic path, split-K
+ * partial sums.  It must be zeroed once before first use (hc_workspace_init);
+ * every call leaves it valid for the next.  Calls that share a workspace must
+ * not run concurrently.
+ */
+size_t hc_pre_workspace_bytes(int T, int s, int d);
+
+/* Zero `ws_bytes` of workspace on `stream` (a cudaMemsetAsync). */
+int hc_workspace_init(void *workspace, size_t ws_bytes, void *stream);
+
+/*
+ * Read the workspace status word (synchronises `stream`): HC_OK, or
+ * HC_ERR_DEVICE if a kernel gave up on a bounded wait.  The word is sticky
+ * until hc_workspace_init clears it.
+ */
+int hc_workspace_status(const void *workspace, void *stream);
+
+/*
+ * hc_pre_fused -- the pre-chain of one site (hyper.rs `pre` + `pre_finish_into`,
+ * module header lines "mixes", "mixes *= rsqrt", "pre/post/comb = sinkhorn",
+ * "y = sum_c pre . x").  Unlike the pages' fused kernels, which take the mixes
+ * precomputed by a separate GEMM, this call computes the mixes contraction
+ * itself, so each token's slab is read from memory inside the same program.
+ *
+ *   x     [T, s, d]  stream state (in)
+ *   fn_w  [R, s*d]   row-major mixing weights, R = (2+s)*s (in)
+ *   scale [3]        gate scales: pre, post, comb (in)
+ *   base  [R]        per-row bias (in)
+ *   pre   [T, s]     sigmoid gates + eps (out)
+ *   post  [T, s]     2 * sigmoid gates (out)
+ *   comb  [T, s, s]  Sinkhorn-normalised combination, comb[t, j, k] (out)
+ *   y     [T, d]     collapsed branch input (out)
+ *   workspace, ws_bytes: device scratch of >= hc_pre_workspace_bytes(T, s, d).
+ *   Outputs must not overlap x, fn_w, scale, base or each other.
+ * Results are float32; per-token values do not depend on what other tokens
+ * are in the batch within one path (each path reduces in a fixed order), and
+ * repeated calls are bit-identical.
+ */
+int hc_pre_fused(const float *x, const float *fn_w, const float *scale, const float *base,
+                 int T, int s, int d, int iters, float eps,
+                 float *pre, float *post, float *comb, float *y,
+                 void *workspace, size_t ws_bytes, void *stream);
+
+/*
+ * hc_pre_fused with an explicit kernel path (enum hc_pre_path).  Returns
+ * HC_ERR_UNSUPPORTED if that path cannot run the shape on this device.
+ */
+int hc_pre_fused_path(const float *x, const float *fn_w, const float *scale, const float *base,
+                      int T, int s, int d, int iters, float eps,
+                      float *pre, float *post, float *comb, float *y,
+                      void *workspace, size_t ws_bytes, void *stream, int path);
+
+/* The path HC_PATH_AUTO picks for this shape on the current device. */
+int hc_pre_auto_path(int T, int s, int d);
+
+/*
+ * hc_post -- the post-branch half of a site (hyper.rs `post`):
+ *   x_out[t, k, :] = post[t, k] * f[t, :] + sum_j comb[t, j, k] * x[t, j, :]
+ * where x is the site's INPUT stream state (the residual), not the layer's.
+ *   x [T, s, d] (in), f [T, d] branch output (in), post [T, s] (in),
+ *   comb [T, s, s] (in), x_out [T, s, d] (out; must not overlap x, f, post or
+ *   comb -- the pages ping-pong two state buffers and never update in place).
+ */
+int hc_post(const float *x, const float *f, const float *post, const float *comb,
+            float *x_out, int T, int s, int d, void *stream);
+
+/*
+ * hc_mean -- unweighted stream mean [T, s, d] -> [T, d] (hyper.rs
+ * `contract_mean`, the glm5_next trunk exit `HcCollapse::Mean`).
+ *   x [T, s, d] (in), out [T, d] (out, must not overlap x).
+ */
+int hc_mean(const float *x, float *out, int T, int s, int d, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MHC_GB300_HC_H */

@@ -1,0 +1,238 @@
+// hc_api.cu -- the extern "C" entry points declared in include/hc.h.
+//
+// Every entry validates its arguments on the host before enqueuing anything
+// (the pages refuse bad shapes loudly by name -- hyper.rs HyperTopology::from_plan
+// and load_site -- and here a status code plays that role), then calls the
+// launcher of the chosen kernel path and reports the launch's cudaError.
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "hc_internal.cuh"
+
+namespace hc {
+
+bool device_info(DeviceInfo &out)
+{
+    static std::mutex mu;
+    static DeviceInfo cache[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+        return false;
+    std::lock_guard<std::mutex> lock(mu);
+    DeviceInfo &c = cache[dev];
+    if (c.device != dev) {
+        DeviceInfo n;
+        n.device = dev;
+        if (cudaDeviceGetAttribute(&n.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&n.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
+                cudaSuccess ||
+            cudaDeviceGetAttribute(&n.cc_major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&n.cc_minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+            return false;
+        c = n;
+    }
+    out = c;
+    return true;
+}
+
+}  // namespace hc
+
+namespace {
+
+using hc::kStatusBytes;
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+// Byte ranges [a, a+na) and [b, b+nb) overlap (empty ranges never do).
+bool overlap(const void *a, size_t na, const void *b, size_t nb)
+{
+    if (na == 0 || nb == 0)
+        return false;
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + nb && y < x + na;
+}
+
+bool dims_ok(int T, int s, int d)
+{
+    if (T < 0 || s < 1 || s > 8 || d < 4)
+        return false;
+    const int64_t n = (int64_t)T * s * d;
+    return n < ((int64_t)1 << 31);
+}
+
+int cuda_rc(cudaError_t e) { return e == cudaSuccess ? HC_OK : HC_ERR_CUDA; }
+
+cudaStream_t as_stream(void *s) { return static_cast<cudaStream_t>(s); }
+
+}  // namespace
+
+extern "C" {
+
+const char *hc_status_string(int rc)
+{
+    switch (rc) {
+    case HC_OK: return "ok";
+    case HC_ERR_NULL: return "a required pointer is NULL";
+    case HC_ERR_DIM: return "dimension or parameter out of range (need T >= 0, 1 <= s <= 8, d >= 4, T*s*d < 2^31, iters >= 1, finite eps > 0)";
+    case HC_ERR_ALIGN: return "misaligned pointer or d not a multiple of 4 (tensors 16-byte aligned, gates 4-byte)";
+    case HC_ERR_ALIAS: return "an output buffer overlaps an input or another output";
+    case HC_ERR_WORKSPACE: return "workspace is NULL, misaligned or smaller than hc_pre_workspace_bytes";
+    case HC_ERR_CUDA: return "the CUDA runtime reported an error";
+    case HC_ERR_DEVICE: return "a kernel flagged an error in the workspace status word (bounded wait gave up)";
+    case HC_ERR_UNSUPPORTED: return "the requested kernel path cannot run this shape on this device";
+    default: return "unknown status";
+    }
+}
+
+int hc_expand(const float *emb, float *x, int T, int s, int d, void *stream)
+{
+    if (!dims_ok(T, s, d))
+        return HC_ERR_DIM;
+    if (T == 0)
+        return HC_OK;
+    if (!emb || !x)
+        return HC_ERR_NULL;
+    if (d % 4 || !aligned(emb, 16) || !aligned(x, 16))
+        return HC_ERR_ALIGN;
+    const size_t in_b = (size_t)T * d * 4, out_b = in_b * s;
+    if (overlap(emb, in_b, x, out_b))
+        return HC_ERR_ALIAS;
+    return cuda_rc(hc::launch_expand(emb, x, T, s, d, as_stream(stream)));
+}
+
+int hc_mean(const float *x, float *out, int T, int s, int d, void *stream)
+{
+    if (!dims_ok(T, s, d))
+        return HC_ERR_DIM;
+    if (T == 0)
+        return HC_OK;
+    if (!x || !out)
+        return HC_ERR_NULL;
+    if (d % 4 || !aligned(x, 16) || !aligned(out, 16))
+        return HC_ERR_ALIGN;
+    const size_t out_b = (size_t)T * d * 4, in_b = out_b * s;
+    if (overlap(x, in_b, out, out_b))
+        return HC_ERR_ALIAS;
+    return cuda_rc(hc::launch_mean(x, out, T, s, d, as_stream(stream)));
+}
+
+int hc_post(const float *x, const float *f, const float *post, const float *comb, float *x_out,
+            int T, int s, int d, void *stream)
+{
+    if (!dims_ok(T, s, d))
+        return HC_ERR_DIM;
+    if (T == 0)
+        return HC_OK;
+    if (!x || !f || !post || !comb || !x_out)
+        return HC_ERR_NULL;
+    if (d % 4 || !aligned(x, 16) || !aligned(f, 16) || !aligned(x_out, 16) || !aligned(post, 4) ||
+        !aligned(comb, 4))
+        return HC_ERR_ALIGN;
+    const size_t xb = (size_t)T * s * d * 4, fb = (size_t)T * d * 4;
+    const size_t pb = (size_t)T * s * 4, cb = (size_t)T * s * s * 4;
+    if (overlap(x_out, xb, x, xb) || overlap(x_out, xb, f, fb) || overlap(x_out, xb, post, pb) ||
+        overlap(x_out, xb, comb, cb))
+        return HC_ERR_ALIAS;
+    return cuda_rc(hc::launch_post(x, f, post, comb, x_out, T, s, d, as_stream(stream)));
+}
+
+size_t hc_pre_workspace_bytes(int T, int s, int d)
+{
+    if (!dims_ok(T, s, d))
+        return 0;
+    // Any path may be asked for, so size for the larger of the two.
+    const size_t g = hc::generic_workspace_bytes(T, s, d);
+    return g > kStatusBytes ? g : kStatusBytes;
+}
+
+int hc_workspace_init(void *workspace, size_t ws_bytes, void *stream)
+{
+    if (!workspace)
+        return HC_ERR_NULL;
+    return cuda_rc(cudaMemsetAsync(workspace, 0, ws_bytes, as_stream(stream)));
+}
+
+int hc_workspace_status(const void *workspace, void *stream)
+{
+    if (!workspace)
+        return HC_ERR_NULL;
+    unsigned int code = 0;
+    cudaError_t e = cudaMemcpyAsync(&code, workspace, sizeof(code), cudaMemcpyDeviceToHost,
+                                    as_stream(stream));
+    if (e == cudaSuccess)
+        e = cudaStreamSynchronize(as_stream(stream));
+    if (e != cudaSuccess)
+        return HC_ERR_CUDA;
+    return code == 0 ? HC_OK : HC_ERR_DEVICE;
+}
+
+int hc_pre_auto_path(int T, int s, int d)
+{
+    (void)T;
+    if (!dims_ok(T, s, d) || d % 4)
+        return HC_PATH_GENERIC;
+    return hc::cluster_supported(s, d) ? HC_PATH_CLUSTER : HC_PATH_GENERIC;
+}
+
+int hc_pre_fused_path(const float *x, const float *fn_w, const float *scale, const float *base,
+                      int T, int s, int d, int iters, float eps, float *pre, float *post,
+                      float *comb, float *y, void *workspace, size_t ws_bytes, void *stream, int path)
+{
+    if (!dims_ok(T, s, d) || iters < 1 || !(eps > 0.f) || !std::isfinite(eps))
+        return HC_ERR_DIM;
+    if (path != HC_PATH_AUTO && path != HC_PATH_GENERIC && path != HC_PATH_CLUSTER)
+        return HC_ERR_DIM;
+    if (T == 0)
+        return HC_OK;
+    if (!x || !fn_w || !scale || !base || !pre || !post || !comb || !y)
+        return HC_ERR_NULL;
+    if (d % 4 || !aligned(x, 16) || !aligned(fn_w, 16) || !aligned(y, 16) || !aligned(scale, 4) ||
+        !aligned(base, 4) || !aligned(pre, 4) || !aligned(post, 4) || !aligned(comb, 4))
+        return HC_ERR_ALIGN;
+    const int R = (2 + s) * s;
+    const size_t xb = (size_t)T * s * d * 4, wb = (size_t)R * s * d * 4;
+    const size_t gb = (size_t)T * s * 4, cb = (size_t)T * s * s * 4, yb = (size_t)T * d * 4;
+    const void *ins[4] = {x, fn_w, scale, base};
+    const size_t in_b[4] = {xb, wb, 12, (size_t)R * 4};
+    const void *outs[4] = {pre, post, comb, y};
+    const size_t out_b[4] = {gb, gb, cb, yb};
+    for (int o = 0; o < 4; ++o) {
+        for (int i = 0; i < 4; ++i)
+            if (overlap(outs[o], out_b[o], ins[i], in_b[i]))
+                return HC_ERR_ALIAS;
+        for (int o2 = o + 1; o2 < 4; ++o2)
+            if (overlap(outs[o], out_b[o], outs[o2], out_b[o2]))
+                return HC_ERR_ALIAS;
+    }
+    if (!workspace || !aligned(workspace, 16) || ws_bytes < hc_pre_workspace_bytes(T, s, d))
+        return HC_ERR_WORKSPACE;
+    for (int o = 0; o < 4; ++o)
+        if (overlap(outs[o], out_b[o], workspace, ws_bytes))
+            return HC_ERR_ALIAS;
+    for (int i = 0; i < 4; ++i)
+        if (overlap(ins[i], in_b[i], workspace, ws_bytes))
+            return HC_ERR_ALIAS;
+
+    if (path == HC_PATH_AUTO)
+        path = hc::cluster_supported(s, d) ? HC_PATH_CLUSTER : HC_PATH_GENERIC;
+    cudaStream_t st = as_stream(stream);
+    if (path == HC_PATH_CLUSTER) {
+        if (!hc::cluster_supported(s, d))
+            return HC_ERR_UNSUPPORTED;
+        return cuda_rc(hc::launch_pre_cluster(x, fn_w, scale, base, T, s, d, iters, eps, pre, post,
+                                              comb, y, workspace, st));
+    }
+    return cuda_rc(hc::launch_pre_generic(x, fn_w, scale, base, T, s, d, iters, eps, pre, post,
+                                          comb, y, workspace, st));
+}
+
+int hc_pre_fused(const float *x, const float *fn_w, const float *scale, const float *base, int T,
+                 int s, int d, int iters, float eps, float *pre, float *post, float *comb, float *y,
+                 void *workspace, size_t ws_bytes, void *stream)
+{
+    return hc_pre_fused_path(x, fn_w, scale, base, T, s, d, iters, eps, pre, post, comb, y,
+                             workspace, ws_bytes, stream, HC_PATH_AUTO);
+}
+
+}  // extern "C"

@@ -1,0 +1,74 @@
+// hc_internal.cuh -- private declarations shared by the library's translation units.
+//
+// Nothing here is part of the C ABI (include/hc.h is).  The library is written
+// for sm_103a only: it is compiled with -gencode arch=compute_103a,code=sm_103a.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/hc.h"
+
+namespace hc {
+
+// ---------------------------------------------------------------- workspace status block
+// The first kStatusBytes of every hc_pre_fused workspace hold a status block.
+// Kernels only ever write a non-zero code into it (first error wins); the host
+// clears it with hc_workspace_init and reads it with hc_workspace_status.
+constexpr size_t kStatusBytes = 256;
+struct StatusBlock {
+    unsigned int code;    // 0 = ok, else a DevErr value
+    unsigned int where;   // kernel-specific location of the first error
+    unsigned int block;   // linear block index that reported it
+    unsigned int pad[61];
+};
+static_assert(sizeof(StatusBlock) == kStatusBytes, "status block is 256 bytes");
+
+enum DevErr : unsigned int {
+    kDevOk = 0,
+    kDevWaitTimeout = 1,   // a bounded wait on an mbarrier gave up
+};
+
+__device__ __forceinline__ void report_error(StatusBlock *sb, unsigned int code, unsigned int where)
+{
+    if (sb != nullptr && atomicCAS(&sb->code, 0u, code) == 0u) {
+        sb->where = where;
+        sb->block = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
+    }
+}
+
+// ---------------------------------------------------------------- device properties (host)
+struct DeviceInfo {
+    int device = -1;
+    int sm_count = 0;
+    int max_smem_optin = 0;
+    int cc_major = 0, cc_minor = 0;
+};
+// Cached per device; returns false if the CUDA runtime fails.
+bool device_info(DeviceInfo &out);
+
+// ---------------------------------------------------------------- launchers (host)
+// All launchers assume validated arguments and return a cudaError_t.
+cudaError_t launch_post(const float *x, const float *f, const float *post, const float *comb,
+                        float *x_out, int T, int s, int d, cudaStream_t st);
+cudaError_t launch_expand(const float *emb, float *x, int T, int s, int d, cudaStream_t st);
+cudaError_t launch_mean(const float *x, float *out, int T, int s, int d, cudaStream_t st);
+
+// Generic pre path: split-K mixes partials, then a per-token finish + collapse.
+size_t generic_workspace_bytes(int T, int s, int d);
+cudaError_t launch_pre_generic(const float *x, const float *fn_w, const float *scale,
+                               const float *base, int T, int s, int d, int iters, float eps,
+                               float *pre, float *post, float *comb, float *y,
+                               void *workspace, cudaStream_t st);
+
+// Cluster pre path (one fused launch).  cluster_supported() says whether the
+// shape fits and the device can co-schedule the clusters.
+bool cluster_shape_ok(int s, int d);
+bool cluster_supported(int s, int d);
+cudaError_t launch_pre_cluster(const float *x, const float *fn_w, const float *scale,
+                               const float *base, int T, int s, int d, int iters, float eps,
+                               float *pre, float *post, float *comb, float *y,
+                               void *workspace, cudaStream_t st);
+
+}  // namespace hc

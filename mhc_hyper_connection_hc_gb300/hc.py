@@ -1,0 +1,164 @@
+"""Thin Python binding of the C ABI in include/hc.h.
+
+Argument marshalling only: each function takes torch CUDA tensors, checks their
+dtype, device and contiguity, passes raw device pointers, sizes and the CUDA
+stream handle to the C entry point of the same name, and raises HcError on a
+non-zero status.  Every step of the site program runs in the library's CUDA
+kernels; there is no fallback.  If the library has not been built the first
+call raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_lib", "libmhc_gb300.so")
+
+HC_OK = 0
+HC_ERR_NULL, HC_ERR_DIM, HC_ERR_ALIGN, HC_ERR_ALIAS = 1, 2, 3, 4
+HC_ERR_WORKSPACE, HC_ERR_CUDA, HC_ERR_DEVICE, HC_ERR_UNSUPPORTED = 5, 6, 7, 8
+HC_PATH_AUTO, HC_PATH_GENERIC, HC_PATH_CLUSTER = 0, 1, 2
+
+EXPORTED = ("hc_status_string", "hc_expand", "hc_pre_workspace_bytes", "hc_workspace_init",
+            "hc_workspace_status", "hc_pre_fused", "hc_pre_fused_path", "hc_pre_auto_path",
+            "hc_post", "hc_mean")
+
+
+class HcError(RuntimeError):
+    def __init__(self, fn: str, rc: int):
+        self.rc = rc
+        super().__init__(f"{fn} failed: status {rc} ({status_string(rc)})")
+
+
+_lib = None
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Open the CUDA library (raises if it is missing)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"CUDA library not built: {path} is missing (run __graft_entry__.build())")
+    lib = ctypes.CDLL(path)
+    vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    lib.hc_status_string.argtypes, lib.hc_status_string.restype = [i], ctypes.c_char_p
+    lib.hc_expand.argtypes = [vp, vp, i, i, i, vp]
+    lib.hc_mean.argtypes = [vp, vp, i, i, i, vp]
+    lib.hc_post.argtypes = [vp, vp, vp, vp, vp, i, i, i, vp]
+    lib.hc_pre_workspace_bytes.argtypes, lib.hc_pre_workspace_bytes.restype = [i, i, i], sz
+    lib.hc_workspace_init.argtypes = [vp, sz, vp]
+    lib.hc_workspace_status.argtypes = [vp, vp]
+    lib.hc_pre_auto_path.argtypes = [i, i, i]
+    pre_args = [vp, vp, vp, vp, i, i, i, i, f, vp, vp, vp, vp, vp, sz, vp]
+    lib.hc_pre_fused.argtypes = pre_args
+    lib.hc_pre_fused_path.argtypes = pre_args + [i]
+    for name in EXPORTED[1:]:
+        if name != "hc_pre_workspace_bytes":
+            getattr(lib, name).restype = i
+    _lib = lib
+    return lib
+
+
+def status_string(rc: int) -> str:
+    return load().hc_status_string(int(rc)).decode()
+
+
+def _check(fn: str, rc: int) -> None:
+    if rc != HC_OK:
+        raise HcError(fn, rc)
+
+
+def _ptr(t: torch.Tensor | None, name: str, dtype=torch.float32):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device.type != "cuda":
+        raise ValueError(f"{name} must be a CUDA tensor (got {t.device})")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype} (got {t.dtype})")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return ctypes.c_void_p(t.data_ptr()) if t.numel() else None
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    return ctypes.c_void_p(handle)
+
+
+def _shape(x: torch.Tensor):
+    if x.dim() != 3:
+        raise ValueError("stream state must be [T, s, d]")
+    return int(x.shape[0]), int(x.shape[1]), int(x.shape[2])
+
+
+def hc_expand(emb: torch.Tensor, x: torch.Tensor, stream=None) -> None:
+    T, s, d = _shape(x)
+    _check("hc_expand", load().hc_expand(_ptr(emb, "emb"), _ptr(x, "x"), T, s, d, _stream(stream)))
+
+
+def hc_mean(x: torch.Tensor, out: torch.Tensor, stream=None) -> None:
+    T, s, d = _shape(x)
+    _check("hc_mean", load().hc_mean(_ptr(x, "x"), _ptr(out, "out"), T, s, d, _stream(stream)))
+
+
+def hc_post(x, f, post, comb, x_out, stream=None) -> None:
+    T, s, d = _shape(x)
+    _check("hc_post", load().hc_post(_ptr(x, "x"), _ptr(f, "f"), _ptr(post, "post"),
+                                     _ptr(comb, "comb"), _ptr(x_out, "x_out"), T, s, d,
+                                     _stream(stream)))
+
+
+def hc_pre_workspace_bytes(T: int, s: int, d: int) -> int:
+    return int(load().hc_pre_workspace_bytes(T, s, d))
+
+
+def hc_workspace_init(workspace: torch.Tensor, stream=None) -> None:
+    _check("hc_workspace_init", load().hc_workspace_init(
+        _ptr(workspace, "workspace", torch.uint8), workspace.numel(), _stream(stream)))
+
+
+def hc_workspace_status(workspace: torch.Tensor, stream=None) -> int:
+    return int(load().hc_workspace_status(_ptr(workspace, "workspace", torch.uint8), _stream(stream)))
+
+
+def hc_pre_auto_path(T: int, s: int, d: int) -> int:
+    return int(load().hc_pre_auto_path(T, s, d))
+
+
+def hc_pre_fused(x, fn_w, scale, base, iters: int, eps: float, pre, post, comb, y, workspace,
+                 stream=None, path: int | None = None) -> None:
+    T, s, d = _shape(x)
+    args = (_ptr(x, "x"), _ptr(fn_w, "fn_w"), _ptr(scale, "scale"), _ptr(base, "base"), T, s, d,
+            int(iters), float(eps), _ptr(pre, "pre"), _ptr(post, "post"), _ptr(comb, "comb"),
+            _ptr(y, "y"), _ptr(workspace, "workspace", torch.uint8), workspace.numel(),
+            _stream(stream))
+    if path is None:
+        _check("hc_pre_fused", load().hc_pre_fused(*args))
+    else:
+        _check("hc_pre_fused_path", load().hc_pre_fused_path(*args, int(path)))
+
+
+# ----------------------------------------------------------------------------- conveniences
+# Allocation helpers (PyTorch owns device memory; the library never allocates).
+
+
+def new_workspace(T: int, s: int, d: int, device="cuda", stream=None) -> torch.Tensor:
+    """A zero-initialised workspace of hc_pre_workspace_bytes(T, s, d) bytes."""
+    ws = torch.empty(max(256, hc_pre_workspace_bytes(T, s, d)), dtype=torch.uint8, device=device)
+    hc_workspace_init(ws, stream)
+    return ws
+
+
+def new_pre_outputs(T: int, s: int, d: int, device="cuda"):
+    kw = dict(dtype=torch.float32, device=device)
+    return dict(pre=torch.empty(T, s, **kw), post=torch.empty(T, s, **kw),
+                comb=torch.empty(T, s, s, **kw), y=torch.empty(T, d, **kw))

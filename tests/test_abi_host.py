@@ -1,0 +1,118 @@
+"""CPU-only checks of the C ABI: the library loads, exports every function that
+include/hc.h declares, and refuses bad arguments on the host before any CUDA
+call (fake pointers are passed; none of these cases reaches a launch)."""
+
+import ctypes
+import math
+import os
+import re
+
+import pytest
+
+from mhc_hyper_connection_hc_gb300 import hc
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "hc.h")
+
+A = 0x10000000   # fake, 16-byte aligned "device" addresses; never dereferenced
+MB = 1 << 20
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(hc_\w+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from mhc_hyper_connection_hc_gb300 import build
+    build.build()
+    return hc.load()
+
+
+def test_every_declared_function_is_exported(lib):
+    names = declared_functions()
+    assert len(names) >= 10
+    for name in names:
+        assert hasattr(lib, name), f"{name} declared in include/hc.h but not exported"
+    assert set(names) >= set(hc.EXPORTED)
+
+
+def test_status_strings(lib):
+    for rc in range(0, 9):
+        assert len(hc.status_string(rc)) >= 2
+    assert hc.status_string(99) == "unknown status"
+
+
+def post_rc(lib, x=A, f=A + 64 * MB, post=A + 96 * MB, comb=A + 97 * MB, out=A + 128 * MB,
+            T=2, s=4, d=4096):
+    return lib.hc_post(x, f, post, comb, out, T, s, d, None)
+
+
+def test_post_validation(lib):
+    assert post_rc(lib, x=0) == hc.HC_ERR_NULL
+    assert post_rc(lib, out=0) == hc.HC_ERR_NULL
+    assert post_rc(lib, T=-1) == hc.HC_ERR_DIM
+    assert post_rc(lib, s=0) == hc.HC_ERR_DIM
+    assert post_rc(lib, s=9) == hc.HC_ERR_DIM
+    assert post_rc(lib, d=2) == hc.HC_ERR_DIM
+    assert post_rc(lib, d=4098) == hc.HC_ERR_ALIGN
+    assert post_rc(lib, x=A + 4) == hc.HC_ERR_ALIGN
+    assert post_rc(lib, comb=A + 97 * MB + 2) == hc.HC_ERR_ALIGN
+    assert post_rc(lib, out=A) == hc.HC_ERR_ALIAS                    # in place
+    assert post_rc(lib, out=A + 64 * MB - 16) == hc.HC_ERR_ALIAS     # partial overlap with f
+    assert post_rc(lib, T=1 << 20, d=4096) == hc.HC_ERR_DIM          # T*s*d >= 2^31
+    assert post_rc(lib, T=0, x=0, f=0, out=0) == hc.HC_OK            # empty batch
+
+
+def test_expand_mean_validation(lib):
+    assert lib.hc_expand(A, A, 2, 4, 64, None) == hc.HC_ERR_ALIAS
+    assert lib.hc_expand(0, A, 2, 4, 64, None) == hc.HC_ERR_NULL
+    assert lib.hc_mean(A, A + 8, 2, 4, 64, None) == hc.HC_ERR_ALIGN
+    assert lib.hc_mean(A, A + 1024, 2, 4, 64, None) == hc.HC_ERR_ALIAS
+    assert lib.hc_mean(A, A + MB, 0, 4, 64, None) == hc.HC_OK
+
+
+def pre_rc(lib, T=3, s=4, d=4096, iters=20, eps=1e-6, ws_bytes=None, path=0, **over):
+    R = (2 + s) * s
+    p = dict(x=A, fn_w=A + 16 * MB, scale=A + 32 * MB, base=A + 32 * MB + 64, pre=A + 33 * MB,
+             post=A + 33 * MB + 4096, comb=A + 33 * MB + 8192, y=A + 34 * MB, ws=A + 64 * MB)
+    p.update(over)
+    if ws_bytes is None:
+        ws_bytes = hc.hc_pre_workspace_bytes(max(T, 0), s, d)
+    args = [p["x"], p["fn_w"], p["scale"], p["base"], T, s, d, iters, ctypes.c_float(eps),
+            p["pre"], p["post"], p["comb"], p["y"], p["ws"], ws_bytes, None, path]
+    return lib.hc_pre_fused_path(*args)
+
+
+def test_pre_validation(lib):
+    assert pre_rc(lib, iters=0) == hc.HC_ERR_DIM                     # zero iterations refused
+    assert pre_rc(lib, eps=0.0) == hc.HC_ERR_DIM                     # eps <= 0 refused
+    assert pre_rc(lib, eps=-1e-6) == hc.HC_ERR_DIM
+    assert pre_rc(lib, eps=math.inf) == hc.HC_ERR_DIM
+    assert pre_rc(lib, eps=math.nan) == hc.HC_ERR_DIM
+    assert pre_rc(lib, s=0) == hc.HC_ERR_DIM
+    assert pre_rc(lib, path=7) == hc.HC_ERR_DIM
+    assert pre_rc(lib, x=0) == hc.HC_ERR_NULL
+    assert pre_rc(lib, y=0) == hc.HC_ERR_NULL
+    assert pre_rc(lib, x=A + 8) == hc.HC_ERR_ALIGN
+    assert pre_rc(lib, d=4094) == hc.HC_ERR_ALIGN
+    assert pre_rc(lib, pre=A + 1) == hc.HC_ERR_ALIGN
+    assert pre_rc(lib, y=A + 256) == hc.HC_ERR_ALIAS                  # y inside x
+    assert pre_rc(lib, post=A + 33 * MB + 4) == hc.HC_ERR_ALIAS       # post overlaps pre
+    assert pre_rc(lib, ws=0) == hc.HC_ERR_WORKSPACE
+    assert pre_rc(lib, ws_bytes=16) == hc.HC_ERR_WORKSPACE
+    assert pre_rc(lib, ws=A + 64 * MB + 8) == hc.HC_ERR_WORKSPACE
+    assert pre_rc(lib, ws=A + 34 * MB) == hc.HC_ERR_ALIAS             # workspace over y
+    assert pre_rc(lib, T=0, x=0) == hc.HC_OK                          # empty batch
+
+
+def test_workspace_sizes(lib):
+    assert hc.hc_pre_workspace_bytes(0, 4, 4096) >= 256
+    assert hc.hc_pre_workspace_bytes(1, 9, 4096) == 0
+    for T in (1, 8, 37, 512, 4096):
+        for s, d in ((4, 4096), (8, 7168), (1, 4), (3, 12)):
+            n = hc.hc_pre_workspace_bytes(T, s, d)
+            assert n >= 256 and n % 4 == 0
+            assert n <= 256 + 4 * ((2 + s) * s + 1) * T * 304 + 4 * ((2 + s) * s + 1) * 304

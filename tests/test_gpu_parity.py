@@ -1,0 +1,216 @@
+"""Parity of the CUDA path against the float64 oracle, through the C ABI.
+
+Small shapes are checked element by element on every token (several tiles,
+ragged tails, every stream count 1..8, d not a multiple of the chunk width);
+the full-size workloads are checked on sampled tokens that the oracle computes
+one by one, plus properties that hold at any size.  Bar: max relative error
+<= 1e-4 per output tensor (pre, post, comb, y, x'), float32 GPU math, and
+bit-identical reruns.
+"""
+
+import numpy as np
+import pytest
+
+import oracle
+from hc_testutil import TOL, GpuSite, eps32, rel_err, sample_tokens, to_np
+from mhc_hyper_connection_hc_gb300 import synth
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+SMALL = [  # (T, s, d)
+    (1, 4, 4096), (8, 4, 4096), (37, 4, 4096), (16, 4, 1024), (19, 1, 1024), (3, 2, 64),
+    (17, 3, 4100), (2, 5, 12), (33, 6, 40), (4, 7, 8), (1, 8, 4), (5, 8, 7168), (40, 2, 2048),
+    (21, 3, 3072),
+]
+
+
+def _paths(s, d):
+    from mhc_hyper_connection_hc_gb300 import hc
+    paths = [hc.HC_PATH_GENERIC]
+    if hc.hc_pre_auto_path(1, s, d) == hc.HC_PATH_CLUSTER:
+        paths.append(hc.HC_PATH_CLUSTER)
+    return paths
+
+
+def _check_pre(g, want, idx=None, tol=TOL):
+    for k in ("pre", "post", "comb", "y"):
+        got = to_np(g[k]) if idx is None else to_np(g[k])[idx]
+        err = rel_err(got, want[k])
+        assert err <= tol, f"{k}: rel err {err:.3e} > {tol:g}"
+
+
+@pytest.mark.parametrize("T,s,d", SMALL)
+def test_site_parity_small(T, s, d):
+    cid = 100 + 7 * s + T
+    inp = synth.site_inputs(cid, T, s, d)
+    eps, iters = eps32(1e-6), 20
+    want = oracle.site(inp["x"], inp["fn_w"], inp["scale"], inp["base"], inp["f"], iters, eps)
+    gs = GpuSite(T, s, d)
+    dev = {k: gs.upload(v) for k, v in inp.items()}
+    for path in _paths(s, d):
+        g = gs.pre(dev["x"], dev["fn_w"], dev["scale"], dev["base"], iters, 1e-6, path=path)
+        _check_pre(g, want)
+        # hc_post chained from the GPU's own gates (end to end) ...
+        xo = gs.post(dev["x"], dev["f"], g["post"], g["comb"])
+        assert rel_err(to_np(xo), want["x_out"]) <= TOL
+        assert gs.status() == 0
+    # ... and fed the oracle's own gates rounded to float32 (the kernel alone).
+    xo = gs.post(dev["x"], dev["f"], gs.upload(want["post"]), gs.upload(want["comb"]))
+    want_k = oracle.post(inp["x"], inp["f"], want["post"].astype(np.float32),
+                         want["comb"].astype(np.float32))
+    assert rel_err(to_np(xo), want_k) <= 1e-6
+
+
+def test_two_chained_sites_verify_batch():
+    """T = 8, s = 4, d = 4096, two sites (attention, FFN) each with its own trio:
+    site A's x' is site B's input; every intermediate is checked."""
+    w = synth.WORKLOADS[2]
+    T, s, d, iters, eps = w.T, w.s, w.d, w.iters, eps32(w.eps)
+    x0 = synth.stream_state(w.cid, T, s, d)
+    trios = [synth.site_params(w.cid, site, s, d) for site in (0, 1)]
+    fs = [synth.branch_output(w.cid, site, T, d) for site in (0, 1)]
+    gs = GpuSite(T, s, d)
+    x_dev = gs.upload(x0)
+    x_ref = x0.astype(np.float64)
+    for site in (0, 1):
+        fn_w, scale, base = trios[site]
+        want = oracle.site(x_ref, fn_w, scale, base, fs[site], iters, eps)
+        g = gs.pre(x_dev, gs.upload(fn_w), gs.upload(scale), gs.upload(base), iters, w.eps)
+        _check_pre(g, want)
+        xo = gs.post(x_dev, gs.upload(fs[site]), g["post"], g["comb"])
+        assert rel_err(to_np(xo), want["x_out"]) <= TOL
+        x_dev = xo.clone()
+        x_ref = want["x_out"]
+
+
+@pytest.mark.parametrize("cid", [1, 3, 5])
+def test_full_size_workloads_sampled(cid):
+    """The single-decode, prefill and wide-stream workloads at full size, in the
+    launch configuration the bench times; sampled tokens against the oracle."""
+    w = synth.WORKLOADS[cid]
+    inp = synth.workload_inputs(w)
+    gs = GpuSite(w.T, w.s, w.d)
+    dev = {k: gs.upload(v) for k, v in inp.items()}
+    g = gs.pre(dev["x"], dev["fn_w"], dev["scale"], dev["base"], w.iters, w.eps)
+    xo = gs.post(dev["x"], dev["f"], g["post"], g["comb"])
+    torch.cuda.synchronize()
+    assert gs.status() == 0
+    idx = sample_tokens(w.T)
+    want = oracle.site(inp["x"][idx], inp["fn_w"], inp["scale"], inp["base"], inp["f"][idx],
+                       w.iters, eps32(w.eps))
+    _check_pre(g, want, idx)
+    assert rel_err(to_np(xo)[idx], want["x_out"]) <= TOL
+    # properties that hold for every token
+    comb = to_np(g["comb"])
+    assert np.all(np.isfinite(comb)) and np.all(np.isfinite(to_np(xo)))
+    assert np.max(np.abs(comb.sum(axis=1) - 1.0)) < 1e-4          # columns normalised last
+    pre = to_np(g["pre"])
+    assert np.all(pre > 0) and np.all(pre < 1 + 2e-6)
+    post = to_np(g["post"])
+    assert np.all(post >= 0) and np.all(post <= 2)
+
+
+@pytest.mark.parametrize("T", [1, 512])
+@pytest.mark.parametrize("iters", [1, 5, 10, 20, 40])
+def test_sinkhorn_iteration_sweep(T, iters):
+    w = synth.WORKLOADS[4]
+    inp = synth.workload_inputs(w, T=T)
+    gs = GpuSite(T, w.s, w.d)
+    dev = {k: gs.upload(v) for k, v in inp.items()}
+    g = gs.pre(dev["x"], dev["fn_w"], dev["scale"], dev["base"], iters, w.eps)
+    idx = sample_tokens(T, n=12)
+    want = oracle.pre(inp["x"][idx], inp["fn_w"], inp["scale"], inp["base"], iters, eps32(w.eps))
+    _check_pre(g, want, idx)
+
+
+def test_bit_identical_reruns():
+    T, s, d = 300, 4, 4096
+    inp = synth.site_inputs(31, T, s, d)
+    gs = GpuSite(T, s, d)
+    dev = {k: gs.upload(v) for k, v in inp.items()}
+    from mhc_hyper_connection_hc_gb300 import hc
+    for path in _paths(s, d):
+        first = None
+        for _ in range(10):
+            g = gs.pre(dev["x"], dev["fn_w"], dev["scale"], dev["base"], 20, 1e-6, path=path)
+            xo = gs.post(dev["x"], dev["f"], g["post"], g["comb"])
+            cur = [t.clone() for t in (g["pre"], g["post"], g["comb"], g["y"], xo)]
+            if first is None:
+                first = cur
+            else:
+                for a, b in zip(first, cur):
+                    assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+
+
+def test_largest_state():
+    """T*s*d just under 2^31 elements (8 GiB of state): 64-bit offsets everywhere."""
+    s, d = 4, 4096
+    T = (2 ** 31 - 1) // (s * d)
+    base_T = 64
+    inp = synth.site_inputs(41, base_T, s, d)
+    gs = GpuSite(T, s, d)
+    x_small = gs.upload(inp["x"])
+    f_small = gs.upload(inp["f"])
+    reps = (T + base_T - 1) // base_T
+    x = x_small.repeat(reps, 1, 1)[:T].contiguous()
+    f = f_small.repeat(reps, 1)[:T].contiguous()
+    g = gs.pre(x, gs.upload(inp["fn_w"]), gs.upload(inp["scale"]), gs.upload(inp["base"]), 20, 1e-6)
+    xo = gs.post(x, f, g["post"], g["comb"])
+    idx = np.array([0, 1, T // 2, T - 2, T - 1])
+    src = idx % base_T
+    want = oracle.site(inp["x"][src], inp["fn_w"], inp["scale"], inp["base"], inp["f"][src], 20,
+                       eps32(1e-6))
+    _check_pre(g, want, idx)
+    assert rel_err(to_np(xo[idx]), want["x_out"]) <= TOL
+    del x, f, xo
+
+
+@pytest.mark.parametrize("s,d", [(1, 4), (3, 12), (4, 4096), (8, 7168)])
+def test_expand_and_mean(s, d):
+    from mhc_hyper_connection_hc_gb300 import hc
+    T = 9
+    e = synth.branch_output(51, 0, T, d)
+    x = torch.empty(T, s, d, device="cuda")
+    hc.hc_expand(torch.from_numpy(e).cuda(), x)
+    want = oracle.expand(e, s)
+    assert np.array_equal(to_np(x), want)
+    xs = synth.stream_state(52, T, s, d)
+    out = torch.empty(T, d, device="cuda")
+    hc.hc_mean(torch.from_numpy(xs).cuda(), out)
+    assert rel_err(to_np(out), oracle.mean(xs)) <= 1e-6
+    m2 = torch.empty(T, d, device="cuda")
+    hc.hc_mean(x, m2)
+    if s & (s - 1) == 0:
+        assert np.array_equal(to_np(m2), e.astype(np.float64))
+    else:
+        assert rel_err(to_np(m2), e) <= 2e-7
+
+
+def test_empty_batch_and_rejections():
+    from mhc_hyper_connection_hc_gb300 import hc
+    s, d = 4, 64
+    gs = GpuSite(0, s, d)
+    z = torch.empty(0, s, d, device="cuda")
+    w = torch.zeros((2 + s) * s, s * d, device="cuda")
+    sc, b = torch.ones(3, device="cuda"), torch.zeros((2 + s) * s, device="cuda")
+    gs.pre(z, w, sc, b, 20, 1e-6)                    # T = 0: nothing to do, no error
+    x = torch.zeros(2, s, d, device="cuda")
+    f = torch.zeros(2, d, device="cuda")
+    p = torch.zeros(2, s, device="cuda")
+    c = torch.zeros(2, s, s, device="cuda")
+    with pytest.raises(hc.HcError) as e:
+        hc.hc_post(x, f, p, c, x)                    # in place is refused
+    assert e.value.rc == hc.HC_ERR_ALIAS
+    ws = hc.new_workspace(2, s, d)
+    o = hc.new_pre_outputs(2, s, d)
+    with pytest.raises(hc.HcError) as e:
+        hc.hc_pre_fused(x, w, sc, b, 0, 1e-6, o["pre"], o["post"], o["comb"], o["y"], ws)
+    assert e.value.rc == hc.HC_ERR_DIM               # zero Sinkhorn iterations refused
+    with pytest.raises(hc.HcError) as e:
+        hc.hc_pre_fused(x, w, sc, b, 20, 0.0, o["pre"], o["post"], o["comb"], o["y"], ws)
+    assert e.value.rc == hc.HC_ERR_DIM               # eps <= 0 refused
+    small_ws = torch.zeros(16, dtype=torch.uint8, device="cuda")
+    with pytest.raises(hc.HcError) as e:
+        hc.hc_pre_fused(x, w, sc, b, 20, 1e-6, o["pre"], o["post"], o["comb"], o["y"], small_ws)
+    assert e.value.rc == hc.HC_ERR_WORKSPACE
