@@ -181,10 +181,8 @@ def test_expand_and_mean(s, d):
     assert rel_err(to_np(out), oracle.mean(xs)) <= 1e-6
     m2 = torch.empty(T, d, device="cuda")
     hc.hc_mean(x, m2)
-    if s & (s - 1) == 0:
-        assert np.array_equal(to_np(m2), e.astype(np.float64))
-    else:
-        assert rel_err(to_np(m2), e) <= 2e-7
+    # a float32 running sum of s equal values is not exact in general (3v rounds)
+    assert rel_err(to_np(m2), e) <= 4e-7
 
 
 def test_empty_batch_and_rejections():
