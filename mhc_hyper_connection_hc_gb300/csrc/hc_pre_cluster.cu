@@ -246,6 +246,7 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const Param
         ptx::tmem_alloc(ptx::smem_u32(tmem_slot), kTmemCols);
         ptx::tmem_relinquish();
     }
+    __syncwarp();
     if (PERSIST)
         ptx::tmem_fence_before_sync();
     ptx::cluster_sync_all();   // barriers initialised in every CTA before any remote arrive
@@ -255,6 +256,7 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const Param
 
     if (warp == kProducerWarp) {
         // -------------------------------------------------------------- producer
+        // Lane 0 does every wait and the warp follows its (broadcast) decision.
         const uint32_t hs_bytes = (uint32_t)p.hs * 4u;
         float *wdst = PERSIST ? stages : wsm;
         if (lane == 0)
@@ -267,16 +269,24 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const Param
                           BAR(kBarWFull));
         }
         bool ok = true;
-        if (PERSIST)   // the fn_w staging area is reused for x tiles once it sits in TMEM
-            ok = wait_bar<false>(BAR(kBarWFree), 0, abort_flag, sb, kSiteWFree);
+        if (PERSIST) {   // the fn_w staging area is reused for x tiles once it sits in TMEM
+            if (lane == 0)
+                ok = wait_bar<false>(BAR(kBarWFree), 0, abort_flag, sb, kSiteWFree);
+            ok = __shfl_sync(kFull, ok, 0);
+        }
         int last_it[kNstPersist] = {-1, -1, -1};
         for (int it = 0; ok; ++it) {
             const int tile = cid + it * ncl;
             if (tile >= p.ntiles)
                 break;
             const int s = it % L.nst, u = it / L.nst;
-            if (u > 0 && !(ok = wait_bar<false>(BAR(kBarXEmpty + s), (u - 1) & 1, abort_flag, sb, kSiteXEmpty)))
-                break;
+            if (u > 0) {
+                if (lane == 0)
+                    ok = wait_bar<false>(BAR(kBarXEmpty + s), (u - 1) & 1, abort_flag, sb, kSiteXEmpty);
+                ok = __shfl_sync(kFull, ok, 0);
+                if (!ok)
+                    break;
+            }
             const int t0 = tile * p.tm_tile, tm = min(p.tm_tile, p.T - t0);
             if (lane == 0)
                 ptx::mbar_arrive_expect_tx(BAR(kBarXFull + s), (uint32_t)(tm * S) * hs_bytes);
@@ -301,9 +311,13 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const Param
         __syncwarp();
     } else if (warp < kNCW) {
         // -------------------------------------------------------------- compute warps
+        // Every thread polls each barrier itself (its own acquire); a named
+        // barrier with an AND reduction then makes the go / give-up decision
+        // identical in all four warps, so they always meet the same barriers.
         const int tg = lane >> 4, kg = lane & 15;
         const uint32_t trow = tmem_base + ((uint32_t)(32 * warp) << 16);
-        bool ok = wait_bar<false>(BAR(kBarWFull), 0, abort_flag, sb, kSiteWFull);
+        bool ok = ptx::named_bar_and(1, kComputeThreads,
+                                     wait_bar<false>(BAR(kBarWFull), 0, abort_flag, sb, kSiteWFull));
         if (PERSIST && ok) {
             // This thread's fixed fn_w values -> its TMEM lane, column j*WQ + 4r + e.
             for (int j = 0; j < p.NJ; ++j) {
@@ -326,7 +340,8 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const Param
 
         auto collapse = [&](int itc) -> bool {
             const int q = itc & 1;
-            if (!wait_bar<true>(BAR(kBarPre + q), (itc >> 1) & 1, abort_flag, sb, kSitePre))
+            const bool got = wait_bar<true>(BAR(kBarPre + q), (itc >> 1) & 1, abort_flag, sb, kSitePre);
+            if (!ptx::named_bar_and(1, kComputeThreads, got))
                 return false;
             const int tile = cid + itc * ncl, t0 = tile * p.tm_tile;
             const int tm = min(p.tm_tile, p.T - t0);
@@ -360,19 +375,22 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const Param
             if (tile >= p.ntiles)
                 break;
             const int s = it % L.nst, u = it / L.nst;
-            if (!(ok = wait_bar<false>(BAR(kBarXFull + s), u & 1, abort_flag, sb, kSiteXFull)))
+            ok = ptx::named_bar_and(1, kComputeThreads,
+                                    wait_bar<false>(BAR(kBarXFull + s), u & 1, abort_flag, sb, kSiteXFull));
+            if (!ok)
                 break;
             const int t0 = tile * p.tm_tile, tm = min(p.tm_tile, p.T - t0);
             const int ntok = min(8, max(0, tm - 8 * tg));
             const float *xs = stages + s * stage_floats + (tg * 8) * p.LK;
 
-            float acc[8][G::B];
-            float ssa0 = 0.f, ssa1 = 0.f;
+            // Packed float32 FMAs: acc[i][r] holds (sum over even columns, sum over odd columns).
+            float2 acc[8][G::B];
+            float2 ssa0 = make_float2(0.f, 0.f), ssa1 = make_float2(0.f, 0.f);
 #pragma unroll
             for (int i = 0; i < 8; ++i)
 #pragma unroll
                 for (int r = 0; r < G::B; ++r)
-                    acc[i][r] = 0.f;
+                    acc[i][r] = make_float2(0.f, 0.f);
             const int ss_i0 = 2 * warp;   // this warp sums the squares of tokens 2w, 2w+1
 
             float w[G::WQ];
@@ -400,23 +418,18 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const Param
                 for (int i = 0; i < 8; ++i) {
                     if (i < ntok) {
                         const float4 xv = *reinterpret_cast<const float4 *>(xs + i * p.LK + c);
+                        const float2 xlo = make_float2(xv.x, xv.y), xhi = make_float2(xv.z, xv.w);
 #pragma unroll
                         for (int r = 0; r < G::B; ++r) {
-                            acc[i][r] = fmaf(xv.x, w[4 * r], acc[i][r]);
-                            acc[i][r] = fmaf(xv.y, w[4 * r + 1], acc[i][r]);
-                            acc[i][r] = fmaf(xv.z, w[4 * r + 2], acc[i][r]);
-                            acc[i][r] = fmaf(xv.w, w[4 * r + 3], acc[i][r]);
+                            acc[i][r] = ptx::ffma2(xlo, make_float2(w[4 * r], w[4 * r + 1]), acc[i][r]);
+                            acc[i][r] = ptx::ffma2(xhi, make_float2(w[4 * r + 2], w[4 * r + 3]), acc[i][r]);
                         }
                         if (i == ss_i0) {
-                            ssa0 = fmaf(xv.x, xv.x, ssa0);
-                            ssa0 = fmaf(xv.y, xv.y, ssa0);
-                            ssa0 = fmaf(xv.z, xv.z, ssa0);
-                            ssa0 = fmaf(xv.w, xv.w, ssa0);
+                            ssa0 = ptx::ffma2(xlo, xlo, ssa0);
+                            ssa0 = ptx::ffma2(xhi, xhi, ssa0);
                         } else if (i == ss_i0 + 1) {
-                            ssa1 = fmaf(xv.x, xv.x, ssa1);
-                            ssa1 = fmaf(xv.y, xv.y, ssa1);
-                            ssa1 = fmaf(xv.z, xv.z, ssa1);
-                            ssa1 = fmaf(xv.w, xv.w, ssa1);
+                            ssa1 = ptx::ffma2(xlo, xlo, ssa1);
+                            ssa1 = ptx::ffma2(xhi, xhi, ssa1);
                         }
                     }
                 }
@@ -434,9 +447,9 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const Param
             for (int i = 0; i < 8; ++i)
 #pragma unroll
                 for (int r = 0; r < G::B; ++r)
-                    v[i * G::B + r] = acc[i][r];
-            v[8 * G::B] = ssa0;
-            v[8 * G::B + 1] = ssa1;
+                    v[i * G::B + r] = acc[i][r].x + acc[i][r].y;
+            v[8 * G::B] = ssa0.x + ssa0.y;
+            v[8 * G::B + 1] = ssa1.x + ssa1.y;
 #pragma unroll
             for (int q = G::NV; q < G::NVP; ++q)
                 v[q] = 0.f;
@@ -471,6 +484,8 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const Param
             collapse(it - 1);
     } else {
         // -------------------------------------------------------------- finisher warps
+        // Lane 0 waits; the acquire it performs, followed by __syncwarp, orders
+        // the other lanes' reads of the remotely written partials after it.
         const int f = warp - kFinisherWarp;
         const int grp = lane < S ? 0 : (lane < 2 * S ? 1 : 2);
         const float my_scale = lane < G::R ? p.scale[grp] : 0.f;
@@ -480,7 +495,12 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const Param
             if (tile >= p.ntiles)
                 break;
             const int qb = it & 1;
-            if (!wait_bar<true>(BAR(kBarRecv + qb), (it >> 1) & 1, abort_flag, sb, kSiteRecv))
+            bool got = true;
+            if (lane == 0)
+                got = wait_bar<true>(BAR(kBarRecv + qb), (it >> 1) & 1, abort_flag, sb, kSiteRecv);
+            got = __shfl_sync(kFull, got, 0);
+            __syncwarp();
+            if (!got)
                 break;
             const int t0 = tile * p.tm_tile, tm = min(p.tm_tile, p.T - t0);
             const bool own = (int)rank < tm;
@@ -531,6 +551,7 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const Param
     }
 
     // ------------------------------------------------------------------ teardown
+    __syncwarp();
     if (PERSIST)
         ptx::tmem_fence_before_sync();
     ptx::cluster_sync_all();   // no CTA leaves while another may still write its shared memory
@@ -590,7 +611,9 @@ int max_clusters_for(int device)
 template <int S, bool PERSIST>
 cudaError_t launch_variant(const Params &p, int nclusters, cudaStream_t st)
 {
-    const Lay L = make_lay<S, PERSIST>(p.LK);
+    // A persistent CTA allocates all 512 TMEM columns, so it must be alone on its
+    // SM: reserve the largest shared-memory footprint whatever the shape.
+    const Lay L = make_lay<S, PERSIST>(PERSIST ? kMaxLK : p.LK);
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute at[1];
     at[0].id = cudaLaunchAttributeClusterDimension;

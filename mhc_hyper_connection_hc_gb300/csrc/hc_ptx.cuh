@@ -124,6 +124,33 @@ __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t threads)
 {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
+// Named barrier that also ANDs a predicate over the participating threads, so a
+// decision taken after a bounded wait is the same in every participating warp.
+__device__ __forceinline__ bool named_bar_and(uint32_t id, uint32_t threads, bool v)
+{
+    uint32_t r;
+    asm volatile("{\n .reg .pred p, q;\n"
+                 " setp.ne.u32 p, %1, 0;\n"
+                 " bar.red.and.pred q, %2, %3, p;\n"
+                 " selp.u32 %0, 1, 0, q;\n}"
+                 : "=r"(r)
+                 : "r"((uint32_t)v), "r"(id), "r"(threads)
+                 : "memory");
+    return r != 0;
+}
+
+// ---------------------------------------------------------------- packed float32 FMA
+// d = a * b + c on two float32 lanes at once (one fma.rn.f32x2, round to nearest).
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c)
+{
+    unsigned long long d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;"
+        : "=l"(d)
+        : "l"(*reinterpret_cast<const unsigned long long *>(&a)),
+          "l"(*reinterpret_cast<const unsigned long long *>(&b)),
+          "l"(*reinterpret_cast<const unsigned long long *>(&c)));
+    return *reinterpret_cast<float2 *>(&d);
+}
 
 // ---------------------------------------------------------------- tensor memory
 // Used here as per-thread storage for each thread's fixed slice of fn_w: with

@@ -21,7 +21,7 @@ pytestmark = pytest.mark.gpu
 SMALL = [  # (T, s, d)
     (1, 4, 4096), (8, 4, 4096), (37, 4, 4096), (16, 4, 1024), (19, 1, 1024), (3, 2, 64),
     (17, 3, 4100), (2, 5, 12), (33, 6, 40), (4, 7, 8), (1, 8, 4), (5, 8, 7168), (40, 2, 2048),
-    (21, 3, 3072),
+    (21, 3, 3072), (200, 4, 4096), (150, 2, 2048), (130, 1, 1024), (133, 3, 3072),
 ]
 
 
@@ -212,3 +212,28 @@ def test_empty_batch_and_rejections():
     with pytest.raises(hc.HcError) as e:
         hc.hc_pre_fused(x, w, sc, b, 20, 1e-6, o["pre"], o["post"], o["comb"], o["y"], small_ws)
     assert e.value.rc == hc.HC_ERR_WORKSPACE
+
+
+def test_cluster_path_token_results_do_not_depend_on_the_batch():
+    """The fused path sums every dot in one fixed order, so token t's outputs are the
+    same bits whether it is alone (T=1), in a one-tile-per-cluster batch, or in a
+    persistent multi-tile batch (the pages' pre_exact guarantee, here by construction)."""
+    from mhc_hyper_connection_hc_gb300 import hc
+    s, d = 4, 4096
+    if hc.hc_pre_auto_path(1, s, d) != hc.HC_PATH_CLUSTER:
+        pytest.skip("fused cluster path not available")
+    T = 300
+    inp = synth.site_inputs(61, T, s, d)
+    big = GpuSite(T, s, d)
+    dev = {k: big.upload(v) for k, v in inp.items()}
+    g = big.pre(dev["x"], dev["fn_w"], dev["scale"], dev["base"], 20, 1e-6, path=hc.HC_PATH_CLUSTER)
+    ref = {k: g[k].clone() for k in ("pre", "post", "comb", "y")}
+    for n in (1, 5, 37):
+        small = GpuSite(n, s, d)
+        for start in (0, 17, T - n):
+            gg = small.pre(dev["x"][start:start + n].contiguous(), dev["fn_w"], dev["scale"],
+                           dev["base"], 20, 1e-6, path=hc.HC_PATH_CLUSTER)
+            for k in ref:
+                a = gg[k].view(torch.int32)
+                b = ref[k][start:start + n].contiguous().view(torch.int32)
+                assert torch.equal(a, b), f"{k} differs for tokens {start}..{start + n}"
