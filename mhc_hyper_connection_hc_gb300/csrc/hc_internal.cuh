@@ -8,7 +8,7 @@
 #include <stddef.h>
 #include <stdint.h>
 
-#include "../../include/hc.h"
+#include "hc.h"
 
 namespace hc {
 

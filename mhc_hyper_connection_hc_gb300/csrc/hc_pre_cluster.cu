@@ -50,10 +50,10 @@ namespace {
 
 constexpr int kCS = 16;              // CTAs per cluster (non-portable cluster size)
 constexpr int kTMT = 16;             // max tokens per tile = one owner CTA per token
-constexpr int kNCW = 4;              // compute warps
-constexpr int kProducerWarp = 4;
-constexpr int kFinisherWarp = 5;     // warps 5 and 6 take even and odd tiles
-constexpr int kThreads = 7 * 32;
+constexpr int kNCW = 8;              // compute warps: two per SM sub-partition
+constexpr int kProducerWarp = 8;
+constexpr int kFinisherWarp = 9;     // warps 9 and 10 take even and odd tiles
+constexpr int kThreads = 11 * 32;
 constexpr int kComputeThreads = kNCW * 32;
 constexpr int kNstPersist = 3;
 constexpr int kMaxLK = 1024;         // s*d/16 <= 1024: three 64 KiB stages fit in shared memory
@@ -68,13 +68,21 @@ enum WaitSite : unsigned { kSiteWFull = 1, kSiteXFull, kSiteXEmpty, kSiteRecv, k
 template <int S>
 struct CG {
     static constexpr int R = (2 + S) * S;
-    static constexpr int RP = (R + kNCW - 1) / kNCW * kNCW;  // rows padded to the 4 compute warps
+    static constexpr int RP = (R + kNCW - 1) / kNCW * kNCW;  // rows padded to the compute warps
     static constexpr int B = RP / kNCW;                        // rows per compute warp
     static constexpr int RV = (R + 1 + 3) / 4 * 4;             // exchange stride: R dots + sum of squares
-    static constexpr int NV = 8 * B + 2;                       // per-thread values before the reduce-scatter
+    static constexpr int WQ = 4 * B;                           // fn_w floats per thread per column group
+};
+
+// NT = token slots per half-warp (a tile holds up to 2*NT tokens, one owner CTA each).
+// Warp w sums the squares of slots w, w+4, ... so NSS values per thread.
+template <int S, int NT>
+struct CT {
+    static constexpr int B = CG<S>::B;
+    static constexpr int NSS = (NT + kNCW - 1) / kNCW;
+    static constexpr int NV = NT * B + NSS;                    // per-thread values before the reduce-scatter
     static constexpr int NVP = (NV + 15) / 16 * 16;
     static constexpr int VPL = NVP / 16;                       // per-lane values after it
-    static constexpr int WQ = 4 * B;                           // fn_w floats per thread per column group
 };
 
 struct Lay {   // shared-memory layout in bytes
@@ -171,30 +179,39 @@ __device__ __forceinline__ void reduce_scatter16(float *v, int kg)
     rs_level<N / 8, 1>(v, kg);
 }
 
+// Pairwise sum of n register values (a fixed tree: short dependency chain).
+template <int N>
+__device__ __forceinline__ float tree_sum(const float *v)
+{
+    if constexpr (N == 1) {
+        return v[0];
+    } else {
+        return tree_sum<N / 2>(v) + tree_sum<N - N / 2>(v + N / 2);
+    }
+}
+
 // Sinkhorn on an S x S matrix held in registers: `iters` rounds of dividing
-// each row by (row sum + eps), then each column by (column sum + eps).
+// each row by (row sum + eps), then each column by (column sum + eps).  The
+// reciprocal is the hardware approximation (__fdividef, within 2 ulp); the
+// Sinkhorn's own error budget against the float64 oracle is 1e-4.
 template <int S>
 __device__ __forceinline__ void sinkhorn_regs(float *c, int iters, float eps)
 {
     for (int it = 0; it < iters; ++it) {
 #pragma unroll
         for (int j = 0; j < S; ++j) {
-            float rs = 0.f;
-#pragma unroll
-            for (int k = 0; k < S; ++k)
-                rs += c[j * S + k];
-            const float inv = __frcp_rn(rs + eps);
+            const float inv = __fdividef(1.0f, tree_sum<S>(c + j * S) + eps);
 #pragma unroll
             for (int k = 0; k < S; ++k)
                 c[j * S + k] *= inv;
         }
 #pragma unroll
         for (int k = 0; k < S; ++k) {
-            float cs = 0.f;
+            float col[S];
 #pragma unroll
             for (int j = 0; j < S; ++j)
-                cs += c[j * S + k];
-            const float inv = __frcp_rn(cs + eps);
+                col[j] = c[j * S + k];
+            const float inv = __fdividef(1.0f, tree_sum<S>(col) + eps);
 #pragma unroll
             for (int j = 0; j < S; ++j)
                 c[j * S + k] *= inv;
@@ -202,10 +219,48 @@ __device__ __forceinline__ void sinkhorn_regs(float *c, int iters, float eps)
     }
 }
 
-template <int S, bool PERSIST>
+// One column group of the dots: 4 columns of the NT token slots of this half-warp,
+// times this warp's B rows, as packed float32 FMAs (acc = (even-column sum,
+// odd-column sum)); plus the sum of squares of this warp's own slot(s).
+template <int S, int NT>
+__device__ __forceinline__ void dots_step(float2 (&acc)[NT][CG<S>::B], float2 (&ssa)[CT<S, NT>::NSS],
+                                          const float (&w)[CG<S>::WQ], uint32_t xs_addr,
+                                          uint32_t xq_addr, uint32_t cofs, int lk4)
+{
+    constexpr int B = CG<S>::B;
+    float4 xv[NT];
+#pragma unroll
+    for (int i = 0; i < NT; ++i)
+        xv[i] = ptx::lds128(xs_addr + (uint32_t)(i * lk4) + cofs);
+    float4 xq[CT<S, NT>::NSS];
+#pragma unroll
+    for (int m = 0; m < CT<S, NT>::NSS; ++m)
+        xq[m] = ptx::lds128(xq_addr + (uint32_t)(m * kNCW * lk4) + cofs);
+    // Even-column halves first, then odd-column halves: consecutive packed FMAs
+    // never depend on each other.
+#pragma unroll
+    for (int i = 0; i < NT; ++i)
+#pragma unroll
+        for (int r = 0; r < B; ++r)
+            acc[i][r] = ptx::ffma2(make_float2(xv[i].x, xv[i].y), make_float2(w[4 * r], w[4 * r + 1]), acc[i][r]);
+#pragma unroll
+    for (int i = 0; i < NT; ++i)
+#pragma unroll
+        for (int r = 0; r < B; ++r)
+            acc[i][r] = ptx::ffma2(make_float2(xv[i].z, xv[i].w), make_float2(w[4 * r + 2], w[4 * r + 3]), acc[i][r]);
+#pragma unroll
+    for (int m = 0; m < CT<S, NT>::NSS; ++m) {
+        const float2 lo = make_float2(xq[m].x, xq[m].y), hi = make_float2(xq[m].z, xq[m].w);
+        ssa[m] = ptx::ffma2(lo, lo, ssa[m]);
+        ssa[m] = ptx::ffma2(hi, hi, ssa[m]);
+    }
+}
+
+template <int S, bool PERSIST, int NT>
 __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const Params p)
 {
     using G = CG<S>;
+    using C = CT<S, NT>;
     extern __shared__ __align__(128) unsigned char smem[];
     const Lay L = make_lay<S, PERSIST>(p.LK);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -315,7 +370,10 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const Param
         // barrier with an AND reduction then makes the go / give-up decision
         // identical in all four warps, so they always meet the same barriers.
         const int tg = lane >> 4, kg = lane & 15;
-        const uint32_t trow = tmem_base + ((uint32_t)(32 * warp) << 16);
+        // TMEM: warp w reads lanes 32*(w%4).. of its sub-partition; the two warps of a
+        // sub-partition use disjoint column ranges.
+        const uint32_t trow = tmem_base + ((uint32_t)(32 * (warp & 3)) << 16) +
+                              (uint32_t)((warp >> 2) * p.NJ * G::WQ);
         bool ok = ptx::named_bar_and(1, kComputeThreads,
                                      wait_bar<false>(BAR(kBarWFull), 0, abort_flag, sb, kSiteWFull));
         if (PERSIST && ok) {
@@ -348,20 +406,31 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const Param
             const int s = itc % L.nst;
             const float *xs = stages + s * stage_floats;
             const int h4n = p.hs / 4;
-            for (int e = threadIdx.x; e < tm * h4n; e += kComputeThreads) {
-                const int t = e / h4n, h4 = e - t * h4n;
-                const float *pr = preb + (q * kTMT + t) * 4;
-                float4 xv = *reinterpret_cast<const float4 *>(xs + t * p.LK + 4 * h4);
+            int t = threadIdx.x / h4n, h4 = threadIdx.x - (threadIdx.x / h4n) * h4n;
+            const uint32_t xs_base = ptx::smem_u32(xs);
+            const uint32_t pre_base = ptx::smem_u32(preb + q * kTMT * 4);
+            for (; t < tm;) {
+                float pr[S];
+#pragma unroll
+                for (int k = 0; k < S; ++k)
+                    pr[k] = ptx::lds32(pre_base + 4u * (uint32_t)(t * 4 + k));
+                const uint32_t xa = xs_base + 4u * (uint32_t)(t * p.LK + 4 * h4);
+                float4 xv = ptx::lds128(xa);
                 float4 a = make_float4(pr[0] * xv.x, pr[0] * xv.y, pr[0] * xv.z, pr[0] * xv.w);
 #pragma unroll
                 for (int k = 1; k < S; ++k) {
-                    xv = *reinterpret_cast<const float4 *>(xs + t * p.LK + k * p.hs + 4 * h4);
+                    xv = ptx::lds128(xa + 4u * (uint32_t)(k * p.hs));
                     a.x = fmaf(pr[k], xv.x, a.x);
                     a.y = fmaf(pr[k], xv.y, a.y);
                     a.z = fmaf(pr[k], xv.z, a.z);
                     a.w = fmaf(pr[k], xv.w, a.w);
                 }
                 *reinterpret_cast<float4 *>(p.y + (size_t)(t0 + t) * p.d + (size_t)rank * p.hs + 4 * h4) = a;
+                h4 += kComputeThreads;
+                while (h4 >= h4n) {
+                    h4 -= h4n;
+                    ++t;
+                }
             }
             ptx::named_bar_sync(1, kComputeThreads);
             if (threadIdx.x == 0)
@@ -380,96 +449,95 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const Param
             if (!ok)
                 break;
             const int t0 = tile * p.tm_tile, tm = min(p.tm_tile, p.T - t0);
-            const int ntok = min(8, max(0, tm - 8 * tg));
-            const float *xs = stages + s * stage_floats + (tg * 8) * p.LK;
+            const int ntok = min(NT, max(0, tm - NT * tg));
+            // Byte address of token slot 0 of this half-warp, at this lane's first column group.
+            const uint32_t xs_addr = ptx::smem_u32(stages + s * stage_floats + (tg * NT) * p.LK) + 16u * kg;
+            const uint32_t ws_addr = ptx::smem_u32(wsm + (warp * G::B) * p.LK) + 16u * kg;
+            // Slots warp, warp+4, ... of this half-warp: the ones whose squares this warp sums.
+            const uint32_t xq_addr = xs_addr + (uint32_t)(warp * p.LK * 4);
 
             // Packed float32 FMAs: acc[i][r] holds (sum over even columns, sum over odd columns).
-            float2 acc[8][G::B];
-            float2 ssa0 = make_float2(0.f, 0.f), ssa1 = make_float2(0.f, 0.f);
+            // Every slot is computed (rows of a stage past the tile's last token hold stale but
+            // harmless data, never pushed), so the loop has no data-dependent branch.
+            float2 acc[NT][G::B];
+            float2 ssa[C::NSS];
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
+            for (int i = 0; i < NT; ++i)
 #pragma unroll
                 for (int r = 0; r < G::B; ++r)
                     acc[i][r] = make_float2(0.f, 0.f);
-            const int ss_i0 = 2 * warp;   // this warp sums the squares of tokens 2w, 2w+1
+#pragma unroll
+            for (int m = 0; m < C::NSS; ++m)
+                ssa[m] = make_float2(0.f, 0.f);
 
-            float w[G::WQ];
+            const int lk4 = p.LK * 4;
             if (PERSIST) {
-                ptx::tmem_ld_issue<G::WQ>(trow, w);
-                ptx::tmem_ld_wait_regs<G::WQ>(w);
-            }
-            for (int j = 0; j < p.NJ; ++j) {
-                const int c = 4 * (kg + 16 * j);
-                float wn[G::WQ];
-                if (PERSIST) {
-                    if (j + 1 < p.NJ)
-                        ptx::tmem_ld_issue<G::WQ>(trow + (uint32_t)((j + 1) * G::WQ), wn);
-                } else {
+                // fn_w from TMEM, double-buffered without copies: wa holds even column
+                // groups, wb odd ones; the load of the next group overlaps this one's FMAs.
+                float wa[G::WQ], wb[G::WQ];
+                ptx::tmem_ld_issue<G::WQ>(trow, wa);
+                ptx::tmem_ld_wait_regs<G::WQ>(wa);
+                for (int j = 0; j < p.NJ; j += 2) {
+                    const bool odd = j + 1 < p.NJ;
+                    if (odd)
+                        ptx::tmem_ld_issue<G::WQ>(trow + (uint32_t)((j + 1) * G::WQ), wb);
+                    dots_step<S, NT>(acc, ssa, wa, xs_addr, xq_addr, 256u * (uint32_t)j, lk4);
+                    if (!odd)
+                        break;
+                    ptx::tmem_ld_wait_regs<G::WQ>(wb);
+                    const bool next = j + 2 < p.NJ;
+                    if (next)
+                        ptx::tmem_ld_issue<G::WQ>(trow + (uint32_t)((j + 2) * G::WQ), wa);
+                    dots_step<S, NT>(acc, ssa, wb, xs_addr, xq_addr, 256u * (uint32_t)(j + 1), lk4);
+                    if (next)
+                        ptx::tmem_ld_wait_regs<G::WQ>(wa);
+                }
+            } else {
+                for (int j = 0; j < p.NJ; ++j) {
+                    const uint32_t cofs = 256u * (uint32_t)j;
+                    float w[G::WQ];
 #pragma unroll
                     for (int r = 0; r < G::B; ++r) {
-                        const float4 v = *reinterpret_cast<const float4 *>(wsm + (warp * G::B + r) * p.LK + c);
+                        const float4 v = ptx::lds128(ws_addr + (uint32_t)(r * lk4) + cofs);
                         w[4 * r] = v.x;
                         w[4 * r + 1] = v.y;
                         w[4 * r + 2] = v.z;
                         w[4 * r + 3] = v.w;
                     }
-                }
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    if (i < ntok) {
-                        const float4 xv = *reinterpret_cast<const float4 *>(xs + i * p.LK + c);
-                        const float2 xlo = make_float2(xv.x, xv.y), xhi = make_float2(xv.z, xv.w);
-#pragma unroll
-                        for (int r = 0; r < G::B; ++r) {
-                            acc[i][r] = ptx::ffma2(xlo, make_float2(w[4 * r], w[4 * r + 1]), acc[i][r]);
-                            acc[i][r] = ptx::ffma2(xhi, make_float2(w[4 * r + 2], w[4 * r + 3]), acc[i][r]);
-                        }
-                        if (i == ss_i0) {
-                            ssa0 = ptx::ffma2(xlo, xlo, ssa0);
-                            ssa0 = ptx::ffma2(xhi, xhi, ssa0);
-                        } else if (i == ss_i0 + 1) {
-                            ssa1 = ptx::ffma2(xlo, xlo, ssa1);
-                            ssa1 = ptx::ffma2(xhi, xhi, ssa1);
-                        }
-                    }
-                }
-                if (PERSIST && j + 1 < p.NJ) {
-                    ptx::tmem_ld_wait_regs<G::WQ>(wn);
-#pragma unroll
-                    for (int q = 0; q < G::WQ; ++q)
-                        w[q] = wn[q];
+                    dots_step<S, NT>(acc, ssa, w, xs_addr, xq_addr, cofs, lk4);
                 }
             }
 
             // Half-warp sums over the 16 K-groups, then push to the owners.
-            float v[G::NVP];
+            float v[C::NVP];
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
+            for (int i = 0; i < NT; ++i)
 #pragma unroll
                 for (int r = 0; r < G::B; ++r)
                     v[i * G::B + r] = acc[i][r].x + acc[i][r].y;
-            v[8 * G::B] = ssa0.x + ssa0.y;
-            v[8 * G::B + 1] = ssa1.x + ssa1.y;
 #pragma unroll
-            for (int q = G::NV; q < G::NVP; ++q)
+            for (int m = 0; m < C::NSS; ++m)
+                v[NT * G::B + m] = ssa[m].x + ssa[m].y;
+#pragma unroll
+            for (int q = C::NV; q < C::NVP; ++q)
                 v[q] = 0.f;
-            reduce_scatter16<G::NVP>(v, kg);
+            reduce_scatter16<C::NVP>(v, kg);
             const int qb = it & 1;
 #pragma unroll
-            for (int q = 0; q < G::VPL; ++q) {
-                const int o = G::VPL * kg + q;
-                int i = 8, vid = -1;
-                if (o < 8 * G::B) {
+            for (int q = 0; q < C::VPL; ++q) {
+                const int o = C::VPL * kg + q;
+                int i = NT, vid = -1;
+                if (o < NT * G::B) {
                     i = o / G::B;
                     const int row = warp * G::B + (o - i * G::B);
                     vid = row < G::R ? row : -1;
-                } else if (o < 8 * G::B + 2) {
-                    i = ss_i0 + (o - 8 * G::B);
+                } else if (o < C::NV) {
+                    i = warp + kNCW * (o - NT * G::B);
                     vid = G::R;
                 }
                 if (vid >= 0 && i < ntok) {
                     const uint32_t local = ptx::smem_u32(recv + (qb * kCS + (int)rank) * G::RV + vid);
-                    ptx::st_cluster_f32(ptx::mapa(local, (uint32_t)(tg * 8 + i)), v[q]);
+                    ptx::st_cluster_f32(ptx::mapa(local, (uint32_t)(tg * NT + i)), v[q]);
                 }
             }
             ptx::named_bar_sync(1, kComputeThreads);
@@ -506,9 +574,12 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const Param
             const bool own = (int)rank < tm;
             float val = 0.f;
             if (own && lane <= G::R) {
+                float part[kCS];
+                const uint32_t a0 = ptx::smem_u32(recv + qb * kCS * G::RV + lane);
 #pragma unroll
                 for (int c = 0; c < kCS; ++c)
-                    val += recv[(qb * kCS + c) * G::RV + lane];
+                    part[c] = ptx::lds32(a0 + 4u * (uint32_t)(c * G::RV));
+                val = tree_sum<kCS>(part);   // sources in a fixed pairwise order
             }
             const float ss = __shfl_sync(kFull, val, G::R);
             const float rinv = rsqrtf(ss / p.Kf + p.eps);
@@ -569,7 +640,7 @@ struct VariantInfo {
     int max_clusters = 0;
 };
 
-template <int S, bool PERSIST>
+template <int S, bool PERSIST, int NT>
 int max_clusters_for(int device)
 {
     static std::mutex mu;
@@ -581,7 +652,7 @@ int max_clusters_for(int device)
     if (!vi.init) {
         vi.init = true;
         const Lay L = make_lay<S, PERSIST>(kMaxLK);
-        auto kern = hc_pre_cluster_kernel<S, PERSIST>;
+        auto kern = hc_pre_cluster_kernel<S, PERSIST, NT>;
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L.total) != cudaSuccess ||
             cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
             cudaGetLastError();
@@ -608,7 +679,7 @@ int max_clusters_for(int device)
     return vi.max_clusters;
 }
 
-template <int S, bool PERSIST>
+template <int S, bool PERSIST, int NT>
 cudaError_t launch_variant(const Params &p, int nclusters, cudaStream_t st)
 {
     // A persistent CTA allocates all 512 TMEM columns, so it must be alone on its
@@ -626,13 +697,15 @@ cudaError_t launch_variant(const Params &p, int nclusters, cudaStream_t st)
     cfg.stream = st;
     cfg.attrs = at;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, hc_pre_cluster_kernel<S, PERSIST>, p);
+    return cudaLaunchKernelEx(&cfg, hc_pre_cluster_kernel<S, PERSIST, NT>, p);
 }
 
 template <int S>
 bool supported_s(int device)
 {
-    return max_clusters_for<S, true>(device) > 0 && max_clusters_for<S, false>(device) > 0;
+    return max_clusters_for<S, true, 8>(device) > 0 && max_clusters_for<S, false, 1>(device) > 0 &&
+           max_clusters_for<S, false, 2>(device) > 0 && max_clusters_for<S, false, 4>(device) > 0 &&
+           max_clusters_for<S, false, 8>(device) > 0;
 }
 
 template <int S>
@@ -658,19 +731,27 @@ cudaError_t run_s(const float *x, const float *fn_w, const float *scale, const f
     p.iters = iters;
     p.eps = eps;
     p.Kf = (float)(S * d);
-    const int nc_decode = max_clusters_for<S, false>(device);
-    const int nc_persist = max_clusters_for<S, true>(device);
+    // Every decode instantiation has the same footprint; NT = 8 bounds the others.
+    const int nc_decode = max_clusters_for<S, false, 8>(device);
+    const int nc_persist = max_clusters_for<S, true, 8>(device);
     if (nc_decode < 1 || nc_persist < 1)
         return cudaErrorNotSupported;
     if (T <= nc_decode * kTMT) {
-        // One tile per cluster, tokens spread over as many clusters as can run at once.
+        // One tile per cluster, tokens spread over as many clusters as can run at once;
+        // the token-slot count is the smallest that holds a tile.
         p.tm_tile = (T + nc_decode - 1) / nc_decode;
         p.ntiles = (T + p.tm_tile - 1) / p.tm_tile;
-        return launch_variant<S, false>(p, p.ntiles, st);
+        if (p.tm_tile <= 2)
+            return launch_variant<S, false, 1>(p, p.ntiles, st);
+        if (p.tm_tile <= 4)
+            return launch_variant<S, false, 2>(p, p.ntiles, st);
+        if (p.tm_tile <= 8)
+            return launch_variant<S, false, 4>(p, p.ntiles, st);
+        return launch_variant<S, false, 8>(p, p.ntiles, st);
     }
     p.tm_tile = kTMT;
     p.ntiles = (T + kTMT - 1) / kTMT;
-    return launch_variant<S, true>(p, min(p.ntiles, nc_persist), st);
+    return launch_variant<S, true, 8>(p, min(p.ntiles, nc_persist), st);
 }
 
 }  // namespace
