@@ -57,7 +57,9 @@ enum hc_status {
     HC_ERR_WORKSPACE = 5,   /* workspace NULL or smaller than hc_pre_workspace_bytes */
     HC_ERR_CUDA = 6,        /* the CUDA runtime reported an error                    */
     HC_ERR_DEVICE = 7,      /* a kernel flagged an error in the workspace status word */
-    HC_ERR_UNSUPPORTED = 8  /* the requested kernel path cannot run this shape here  */
+    HC_ERR_UNSUPPORTED = 8, /* the requested kernel path cannot run this shape here  */
+    HC_ERR_TOO_LARGE = 9    /* hc_pre_fused_noalloc: shape needs more scratch than its
+                               static buffer holds                                   */
 };
 
 /* Kernel paths of hc_pre_fused_path. */
@@ -136,6 +138,31 @@ int hc_pre_fused_path(const float *x, const float *fn_w, const float *scale, con
 
 /* The path HC_PATH_AUTO picks for this shape on the current device. */
 int hc_pre_auto_path(int T, int s, int d);
+
+/*
+ * hc_pre_fused_noalloc -- hc_pre_fused for callers that cannot allocate device
+ * memory when they run a site: an engine whose device memory is all carved into
+ * a fixed arena at start-up, a plugin whose host framework owns every
+ * allocation, a latency-critical loop that cannot pay for cudaMalloc/cudaFree
+ * (they may block or synchronise the device).  It takes no workspace.  (The
+ * pages have no counterpart; this entry point exists for such callers.)
+ *
+ * Same arguments, layouts, validation and results as hc_pre_fused run on the
+ * generic path (HC_PATH_GENERIC), minus workspace and ws_bytes.  The split-K
+ * scratch lives in a 4 MiB static device buffer inside the library, which every
+ * GPU that loads the library holds until the process exits; shapes needing
+ * more than that (hc_pre_workspace_bytes(T, s, d) > 4 MiB, e.g. T above about
+ * 41,000 at s = 4) return HC_ERR_TOO_LARGE before anything runs.  The call
+ * allocates nothing (no cudaMalloc, cudaFree or allocating library routine).
+ * Its first call on a device looks the buffer's address up with that device
+ * current; make that first call before any stream capture.  All calls share the
+ * one buffer, which keeps the last call's contents: calls whose work overlaps on
+ * the GPU (other streams, other threads) race on it and must be serialised by
+ * the caller.
+ */
+int hc_pre_fused_noalloc(const float *x, const float *fn_w, const float *scale, const float *base,
+                         int T, int s, int d, int iters, float eps,
+                         float *pre, float *post, float *comb, float *y, void *stream);
 
 /*
  * hc_post -- the post-branch half of a site (hyper.rs `post`):

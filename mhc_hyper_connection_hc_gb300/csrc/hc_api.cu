@@ -81,6 +81,7 @@ const char *hc_status_string(int rc)
     case HC_ERR_CUDA: return "the CUDA runtime reported an error";
     case HC_ERR_DEVICE: return "a kernel flagged an error in the workspace status word (bounded wait gave up)";
     case HC_ERR_UNSUPPORTED: return "the requested kernel path cannot run this shape on this device";
+    case HC_ERR_TOO_LARGE: return "shape needs more scratch than hc_pre_fused_noalloc's 4 MiB static buffer holds";
     default: return "unknown status";
     }
 }

@@ -21,11 +21,12 @@ LIB_PATH = os.path.join(_HERE, "_lib", "libmhc_gb300.so")
 HC_OK = 0
 HC_ERR_NULL, HC_ERR_DIM, HC_ERR_ALIGN, HC_ERR_ALIAS = 1, 2, 3, 4
 HC_ERR_WORKSPACE, HC_ERR_CUDA, HC_ERR_DEVICE, HC_ERR_UNSUPPORTED = 5, 6, 7, 8
+HC_ERR_TOO_LARGE = 9
 HC_PATH_AUTO, HC_PATH_GENERIC, HC_PATH_CLUSTER = 0, 1, 2
 
 EXPORTED = ("hc_status_string", "hc_expand", "hc_pre_workspace_bytes", "hc_workspace_init",
             "hc_workspace_status", "hc_pre_fused", "hc_pre_fused_path", "hc_pre_auto_path",
-            "hc_post", "hc_mean")
+            "hc_post", "hc_mean", "hc_pre_fused_noalloc")
 
 
 class HcError(RuntimeError):
@@ -57,6 +58,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     pre_args = [vp, vp, vp, vp, i, i, i, i, f, vp, vp, vp, vp, vp, sz, vp]
     lib.hc_pre_fused.argtypes = pre_args
     lib.hc_pre_fused_path.argtypes = pre_args + [i]
+    lib.hc_pre_fused_noalloc.argtypes = [vp, vp, vp, vp, i, i, i, i, f, vp, vp, vp, vp, vp]
     for name in EXPORTED[1:]:
         if name != "hc_pre_workspace_bytes":
             getattr(lib, name).restype = i
@@ -145,6 +147,17 @@ def hc_pre_fused(x, fn_w, scale, base, iters: int, eps: float, pre, post, comb, 
         _check("hc_pre_fused", load().hc_pre_fused(*args))
     else:
         _check("hc_pre_fused_path", load().hc_pre_fused_path(*args, int(path)))
+
+
+def hc_pre_fused_noalloc(x, fn_w, scale, base, iters: int, eps: float, pre, post, comb, y,
+                         stream=None) -> None:
+    """hc_pre_fused without a workspace, for callers that cannot allocate device memory
+    when they run a site (the scratch is a static buffer inside the library; see hc.h)."""
+    T, s, d = _shape(x)
+    _check("hc_pre_fused_noalloc", load().hc_pre_fused_noalloc(
+        _ptr(x, "x"), _ptr(fn_w, "fn_w"), _ptr(scale, "scale"), _ptr(base, "base"), T, s, d,
+        int(iters), float(eps), _ptr(pre, "pre"), _ptr(post, "post"), _ptr(comb, "comb"),
+        _ptr(y, "y"), _stream(stream)))
 
 
 # ----------------------------------------------------------------------------- conveniences
