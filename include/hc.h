@@ -118,9 +118,10 @@ int hc_workspace_status(const void *workspace, void *stream);
  *   y     [T, d]     collapsed branch input (out)
  *   workspace, ws_bytes: device scratch of >= hc_pre_workspace_bytes(T, s, d).
  *   Outputs must not overlap x, fn_w, scale, base or each other.
- * Results are float32; per-token values do not depend on what other tokens
- * are in the batch within one path (each path reduces in a fixed order), and
- * repeated calls are bit-identical.
+ * Results are float32 and repeated calls are bit-identical (every sum has a
+ * fixed order; no floating-point atomics).  On the cluster path a token's
+ * results are also the same bits whatever else is in the batch; the generic
+ * path sizes its K split by T, so there they may differ in the last bits.
  */
 int hc_pre_fused(const float *x, const float *fn_w, const float *scale, const float *base,
                  int T, int s, int d, int iters, float eps,
