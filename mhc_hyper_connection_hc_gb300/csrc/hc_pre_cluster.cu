@@ -18,20 +18,23 @@
 //    tensor memory (TMEM, tcgen05.ld into registers) for the persistent prefill
 //    variant, in shared memory for the one-tile decode variant.  It is read
 //    from L2/HBM once per CTA.
-//  * Four compute warps (one per TMEM sub-partition) each own R/4 rows; in a
-//    warp, lanes 0-15 take tile tokens 0-7 and lanes 16-31 tokens 8-15, and
-//    lane&15 is the K-group owning float4 columns kg, kg+16, ... of the slice.
-//    Per float4 column group a thread does 8 tokens x B rows x 4 FMAs (CUDA
-//    cores, float32, no TF32: the 24-row contraction is too skinny for tensor
-//    cores to pay and must stay in f32).
-//  * The 16 K-groups are summed by an xor reduce-scatter inside each
-//    half-warp, and every CTA pushes its partial dots and sum of squares for
-//    token t to CTA t (the token's owner) through distributed shared memory.
-//  * Two finisher warps (even/odd tiles) of each owner sum the 16 partials in
-//    rank order, apply the rsqrt rescale, form the gates, broadcast pre to all
-//    16 CTAs, and run the Sinkhorn in registers while the compute warps
-//    already work on the next tile.  Compute warps collapse tile i after the
-//    dots of tile i+1, so the exchange latency is hidden.
+//  * Eight compute warps do nothing but the contraction.  Warp w owns rows
+//    [B*(w%4), B*(w%4)+B) (B = 6 for s = 4) and half of the column groups
+//    (w/4); in a warp, lanes 0-15 take the tile's first token slots and lanes
+//    16-31 the rest, and lane&15 is the K-group owning float4 columns kg,
+//    kg+16, ...  Operands: x from shared memory, fn_w from TMEM; packed
+//    float32 FMAs on CUDA cores (no TF32: the 24-row contraction is too skinny
+//    for tensor cores and must stay in f32).  A 16-lane xor reduce-scatter
+//    sums the K-groups, and the partials go to a local shared-memory buffer.
+//  * Two exchange warps (even/odd tiles) add the two column halves, push each
+//    token's partial dots and sum of squares to its owner CTA (token t of a
+//    tile belongs to CTA t) through distributed shared memory, wait for the
+//    pre gates and write the tile's collapse.
+//  * Two finisher warps (even/odd tiles) of each owner sum the 16 CTA
+//    partials in a fixed tree, apply the rsqrt rescale, form the gates,
+//    broadcast pre to all 16 CTAs, then run the Sinkhorn in registers.
+//  * So the compute warps never wait for the exchange: while they do tile i+1,
+//    tile i is pushed, finished and collapsed by the other warps.
 //  * Every wait on an mbarrier is bounded (2 s of %globaltimer); on timeout the
 //    kernel records the site in the workspace status word, stops issuing work,
 //    lets its bulk copies land, meets the other CTAs at the final cluster
@@ -50,10 +53,11 @@ namespace {
 
 constexpr int kCS = 16;              // CTAs per cluster (non-portable cluster size)
 constexpr int kTMT = 16;             // max tokens per tile = one owner CTA per token
+constexpr int kRG = 4;               // row groups (compute warps w and w+4 share one)
 constexpr int kNCW = 8;              // compute warps: two per SM sub-partition
-constexpr int kProducerWarp = 8;
-constexpr int kFinisherWarp = 9;     // warps 9 and 10 take even and odd tiles
-constexpr int kThreads = 11 * 32;
+constexpr int kFinisherWarp = 8;     // warps 8 and 9 take even and odd tiles
+constexpr int kExchangeWarp = 10;    // warps 10 and 11 take even and odd tiles (and load x)
+constexpr int kThreads = 12 * 32;    // three warps per sub-partition: up to 168 registers each
 constexpr int kComputeThreads = kNCW * 32;
 constexpr int kNstPersist = 3;
 constexpr int kMaxLK = 1024;         // s*d/16 <= 1024: three 64 KiB stages fit in shared memory
@@ -62,31 +66,35 @@ constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 constexpr unsigned kFull = 0xffffffffu;
 
 // mbarrier slots
-constexpr int kBarXFull = 0, kBarXEmpty = 3, kBarRecv = 6, kBarPre = 8, kBarWFull = 10, kBarWFree = 11;
-enum WaitSite : unsigned { kSiteWFull = 1, kSiteXFull, kSiteXEmpty, kSiteRecv, kSitePre, kSiteWFree, kSiteDrain };
+constexpr int kBarXFull = 0, kBarRecv = 3, kBarPre = 5, kBarWFull = 7, kBarWFree = 8,
+              kBarPartFull = 9, kBarPartEmpty = 11, kNumBars = 13;
+enum WaitSite : unsigned {
+    kSiteWFull = 1, kSiteXFull, kSiteRecv, kSitePre, kSiteWFree, kSiteDrain, kSitePartFull,
+    kSitePartEmpty
+};
 
 template <int S>
 struct CG {
     static constexpr int R = (2 + S) * S;
-    static constexpr int RP = (R + kNCW - 1) / kNCW * kNCW;  // rows padded to the compute warps
-    static constexpr int B = RP / kNCW;                        // rows per compute warp
-    static constexpr int RV = (R + 1 + 3) / 4 * 4;             // exchange stride: R dots + sum of squares
-    static constexpr int WQ = 4 * B;                           // fn_w floats per thread per column group
+    static constexpr int RP = (R + kRG - 1) / kRG * kRG;   // rows padded to the 4 row groups
+    static constexpr int B = RP / kRG;                      // rows per compute warp
+    static constexpr int RV = (R + 1 + 3) / 4 * 4;          // exchange stride: R dots + sum of squares
+    static constexpr int WQ = 4 * B;                        // fn_w floats per thread per column group
 };
 
 // NT = token slots per half-warp (a tile holds up to 2*NT tokens, one owner CTA each).
-// Warp w sums the squares of slots w, w+4, ... so NSS values per thread.
+// The warps of row group g sum the squares of slots g, g+4, ...: NSS values per thread.
 template <int S, int NT>
 struct CT {
     static constexpr int B = CG<S>::B;
-    static constexpr int NSS = (NT + kNCW - 1) / kNCW;
-    static constexpr int NV = NT * B + NSS;                    // per-thread values before the reduce-scatter
+    static constexpr int NSS = (NT + kRG - 1) / kRG;
+    static constexpr int NV = NT * B + NSS;                 // per-thread values before the reduce-scatter
     static constexpr int NVP = (NV + 15) / 16 * 16;
-    static constexpr int VPL = NVP / 16;                       // per-lane values after it
+    static constexpr int VPL = NVP / 16;                    // per-lane values after it
 };
 
 struct Lay {   // shared-memory layout in bytes
-    int stage_bytes, nst, off_w, off_recv, off_pre, off_bar, off_misc, total;
+    int stage_bytes, nst, off_w, off_recv, off_part, off_pre, off_bar, off_misc, total;
 };
 
 template <int S, bool PERSIST>
@@ -100,14 +108,16 @@ __host__ __device__ inline Lay make_lay(int LK)
     L.off_w = o;
     if (!PERSIST)
         o += G::RP * LK * 4;
-    L.off_recv = o;
+    L.off_recv = o;                  // [2 tile parities][16 source CTAs][RV]
     o += 2 * kCS * G::RV * 4;
-    L.off_pre = o;
+    L.off_part = o;                  // [2 tile parities][2 column halves][16 tokens][RV]
+    o += 2 * 2 * kTMT * G::RV * 4;
+    L.off_pre = o;                   // [2 tile parities][16 tokens][4]
     o += 2 * kTMT * 4 * 4;
     L.off_bar = o;
-    o += 16 * 8;
-    L.off_misc = o;
-    o += 16;
+    o += kNumBars * 8;
+    L.off_misc = o;                  // TMEM address, abort flag, bulk-copy phases issued per stage
+    o += 32;
     L.total = o;
     return L;
 }
@@ -151,6 +161,21 @@ __device__ __noinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile in
             }
         }
     }
+}
+
+// Bounded wait done by lane 0 of a warp; every lane gets the same answer.  The
+// acquire lane 0 performs, followed by __syncwarp, orders the other lanes'
+// later reads after the arrivals it observed.
+template <bool CLUSTER_SCOPE>
+__device__ __forceinline__ bool warp_wait(int lane, uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                          StatusBlock *sb, unsigned site)
+{
+    bool ok = true;
+    if (lane == 0)
+        ok = wait_bar<CLUSTER_SCOPE>(bar, parity, abort_flag, sb, site);
+    ok = __shfl_sync(kFull, ok, 0);
+    __syncwarp();
+    return ok;
 }
 
 // One level of the xor reduce-scatter over the 16 K-groups of a half-warp:
@@ -221,33 +246,39 @@ __device__ __forceinline__ void sinkhorn_regs(float *c, int iters, float eps)
 
 // One column group of the dots: 4 columns of the NT token slots of this half-warp,
 // times this warp's B rows, as packed float32 FMAs (acc = (even-column sum,
-// odd-column sum)); plus the sum of squares of this warp's own slot(s).
+// odd-column sum)); plus the sums of squares of this warp's NSS slots.
 template <int S, int NT>
 __device__ __forceinline__ void dots_step(float2 (&acc)[NT][CG<S>::B], float2 (&ssa)[CT<S, NT>::NSS],
                                           const float (&w)[CG<S>::WQ], uint32_t xs_addr,
                                           uint32_t xq_addr, uint32_t cofs, int lk4)
 {
     constexpr int B = CG<S>::B;
-    float4 xv[NT];
-#pragma unroll
-    for (int i = 0; i < NT; ++i)
-        xv[i] = ptx::lds128(xs_addr + (uint32_t)(i * lk4) + cofs);
+    constexpr int NH = NT > 4 ? 4 : NT;   // token slots per half (fewer live x registers)
     float4 xq[CT<S, NT>::NSS];
 #pragma unroll
     for (int m = 0; m < CT<S, NT>::NSS; ++m)
-        xq[m] = ptx::lds128(xq_addr + (uint32_t)(m * kNCW * lk4) + cofs);
-    // Even-column halves first, then odd-column halves: consecutive packed FMAs
-    // never depend on each other.
+        xq[m] = ptx::lds128(xq_addr + (uint32_t)(m * kRG * lk4) + cofs);
 #pragma unroll
-    for (int i = 0; i < NT; ++i)
+    for (int i0 = 0; i0 < NT; i0 += NH) {
+        float4 xv[NH];
 #pragma unroll
-        for (int r = 0; r < B; ++r)
-            acc[i][r] = ptx::ffma2(make_float2(xv[i].x, xv[i].y), make_float2(w[4 * r], w[4 * r + 1]), acc[i][r]);
+        for (int i = 0; i < NH; ++i)
+            xv[i] = ptx::lds128(xs_addr + (uint32_t)((i0 + i) * lk4) + cofs);
+        // Even-column halves first, then odd-column halves: consecutive packed FMAs
+        // never depend on each other.
 #pragma unroll
-    for (int i = 0; i < NT; ++i)
+        for (int i = 0; i < NH; ++i)
 #pragma unroll
-        for (int r = 0; r < B; ++r)
-            acc[i][r] = ptx::ffma2(make_float2(xv[i].z, xv[i].w), make_float2(w[4 * r + 2], w[4 * r + 3]), acc[i][r]);
+            for (int r = 0; r < B; ++r)
+                acc[i0 + i][r] = ptx::ffma2(make_float2(xv[i].x, xv[i].y), make_float2(w[4 * r], w[4 * r + 1]),
+                                            acc[i0 + i][r]);
+#pragma unroll
+        for (int i = 0; i < NH; ++i)
+#pragma unroll
+            for (int r = 0; r < B; ++r)
+                acc[i0 + i][r] = ptx::ffma2(make_float2(xv[i].z, xv[i].w), make_float2(w[4 * r + 2], w[4 * r + 3]),
+                                            acc[i0 + i][r]);
+    }
 #pragma unroll
     for (int m = 0; m < CT<S, NT>::NSS; ++m) {
         const float2 lo = make_float2(xq[m].x, xq[m].y), hi = make_float2(xq[m].z, xq[m].w);
@@ -269,24 +300,34 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const Param
     float *stages = reinterpret_cast<float *>(smem);
     float *wsm = reinterpret_cast<float *>(smem + L.off_w);
     float *recv = reinterpret_cast<float *>(smem + L.off_recv);
+    float *part = reinterpret_cast<float *>(smem + L.off_part);
     float *preb = reinterpret_cast<float *>(smem + L.off_pre);
     const uint32_t bar0 = ptx::smem_u32(smem + L.off_bar);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L.off_misc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L.off_misc + 4);
+    volatile int *issued = reinterpret_cast<volatile int *>(smem + L.off_misc + 8);   // per stage
     StatusBlock *sb = p.status;
     const int K = S * p.d;
     const int stage_floats = L.stage_bytes / 4;
+    const int njh = (p.NJ + 1) / 2;   // column groups of the first half (the second gets the rest)
     auto BAR = [&](int i) { return bar0 + 8u * (uint32_t)i; };
+    auto tile_tokens = [&](int it, int &t0, int &tm) {
+        t0 = (cid + it * ncl) * p.tm_tile;
+        tm = min(p.tm_tile, p.T - t0);
+    };
+    auto part_at = [&](int q, int h, int t) { return part + ((q * 2 + h) * kTMT + t) * G::RV; };
 
     // ------------------------------------------------------------------ set-up
     if (threadIdx.x == 0) {
         for (int s = 0; s < L.nst; ++s) {
             ptx::mbar_init(BAR(kBarXFull + s), 1);
-            ptx::mbar_init(BAR(kBarXEmpty + s), 1);
+            issued[s] = 0;
         }
         for (int q = 0; q < 2; ++q) {
             ptx::mbar_init(BAR(kBarRecv + q), kCS);
             ptx::mbar_init(BAR(kBarPre + q), kCS);
+            ptx::mbar_init(BAR(kBarPartFull + q), kNCW);
+            ptx::mbar_init(BAR(kBarPartEmpty + q), 1);
         }
         ptx::mbar_init(BAR(kBarWFull), 1);
         ptx::mbar_init(BAR(kBarWFree), 1);
@@ -309,85 +350,32 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const Param
         ptx::tmem_fence_after_sync();
     const uint32_t tmem_base = PERSIST ? *tmem_slot : 0u;
 
-    if (warp == kProducerWarp) {
-        // -------------------------------------------------------------- producer
-        // Lane 0 does every wait and the warp follows its (broadcast) decision.
-        const uint32_t hs_bytes = (uint32_t)p.hs * 4u;
-        float *wdst = PERSIST ? stages : wsm;
-        if (lane == 0)
-            ptx::mbar_arrive_expect_tx(BAR(kBarWFull), (uint32_t)(G::R * S) * hs_bytes);
-        __syncwarp();
-        for (int e = lane; e < G::R * S; e += 32) {
-            const int r = e / S, k = e - (e / S) * S;
-            ptx::bulk_g2s(ptx::smem_u32(wdst + r * p.LK + k * p.hs),
-                          p.fn_w + (size_t)r * K + (size_t)k * p.d + (size_t)rank * p.hs, hs_bytes,
-                          BAR(kBarWFull));
-        }
-        bool ok = true;
-        if (PERSIST) {   // the fn_w staging area is reused for x tiles once it sits in TMEM
-            if (lane == 0)
-                ok = wait_bar<false>(BAR(kBarWFree), 0, abort_flag, sb, kSiteWFree);
-            ok = __shfl_sync(kFull, ok, 0);
-        }
-        int last_it[kNstPersist] = {-1, -1, -1};
-        for (int it = 0; ok; ++it) {
-            const int tile = cid + it * ncl;
-            if (tile >= p.ntiles)
-                break;
-            const int s = it % L.nst, u = it / L.nst;
-            if (u > 0) {
-                if (lane == 0)
-                    ok = wait_bar<false>(BAR(kBarXEmpty + s), (u - 1) & 1, abort_flag, sb, kSiteXEmpty);
-                ok = __shfl_sync(kFull, ok, 0);
-                if (!ok)
-                    break;
-            }
-            const int t0 = tile * p.tm_tile, tm = min(p.tm_tile, p.T - t0);
-            if (lane == 0)
-                ptx::mbar_arrive_expect_tx(BAR(kBarXFull + s), (uint32_t)(tm * S) * hs_bytes);
-            __syncwarp();
-            float *xs = stages + s * stage_floats;
-            for (int e = lane; e < tm * S; e += 32) {
-                const int t = e / S, k = e - (e / S) * S;
-                ptx::bulk_g2s(ptx::smem_u32(xs + t * p.LK + k * p.hs),
-                              p.x + ((size_t)(t0 + t) * S + k) * p.d + (size_t)rank * p.hs, hs_bytes,
-                              BAR(kBarXFull + s));
-            }
-            last_it[s] = it;
-        }
-        // Every bulk copy this CTA issued lands before the CTA may exit.
-        if (lane == 0) {
-            wait_bar<false>(BAR(kBarWFull), 0, abort_flag, sb, kSiteDrain, false);
-            for (int s = 0; s < L.nst; ++s)
-                if (last_it[s] >= 0)
-                    wait_bar<false>(BAR(kBarXFull + s), (last_it[s] / L.nst) & 1, abort_flag, sb,
-                                    kSiteDrain, false);
-        }
-        __syncwarp();
-    } else if (warp < kNCW) {
+    if (warp < kNCW) {
         // -------------------------------------------------------------- compute warps
         // Every thread polls each barrier itself (its own acquire); a named
         // barrier with an AND reduction then makes the go / give-up decision
-        // identical in all four warps, so they always meet the same barriers.
+        // identical in all eight warps, so they always meet the same barriers.
         const int tg = lane >> 4, kg = lane & 15;
-        // TMEM: warp w reads lanes 32*(w%4).. of its sub-partition; the two warps of a
-        // sub-partition use disjoint column ranges.
-        const uint32_t trow = tmem_base + ((uint32_t)(32 * (warp & 3)) << 16) +
-                              (uint32_t)((warp >> 2) * p.NJ * G::WQ);
+        const int rg = warp & (kRG - 1), half = warp / kRG;
+        const int j0 = half * njh, nj = half ? p.NJ - njh : njh;
+        // TMEM: warp w reads lanes 32*(w%4).. of its sub-partition; the two warps of
+        // a sub-partition (the two column halves) use disjoint column ranges.
+        const uint32_t trow = tmem_base + ((uint32_t)(32 * rg) << 16) + (uint32_t)(half * njh * G::WQ);
         bool ok = ptx::named_bar_and(1, kComputeThreads,
                                      wait_bar<false>(BAR(kBarWFull), 0, abort_flag, sb, kSiteWFull));
         if (PERSIST && ok) {
-            // This thread's fixed fn_w values -> its TMEM lane, column j*WQ + 4r + e.
-            for (int j = 0; j < p.NJ; ++j) {
-                const int c = 4 * (kg + 16 * j);
+            // This thread's fixed fn_w values -> its TMEM lane, column jj*WQ + 4r + e.
+            const float *wstage = stages + stage_floats;
+            for (int jj = 0; jj < nj; ++jj) {
+                const int c = 4 * (kg + 16 * (j0 + jj));
 #pragma unroll
                 for (int r = 0; r < G::B; ++r) {
-                    const int row = warp * G::B + r;
+                    const int row = rg * G::B + r;
                     float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
                     if (row < G::R)
-                        v = *reinterpret_cast<const float4 *>(stages + row * p.LK + c);
+                        v = *reinterpret_cast<const float4 *>(wstage + row * p.LK + c);
                     const float a[4] = {v.x, v.y, v.z, v.w};
-                    ptx::tmem_st4(trow + (uint32_t)(j * G::WQ + 4 * r), a);
+                    ptx::tmem_st4(trow + (uint32_t)(jj * G::WQ + 4 * r), a);
                 }
             }
             ptx::tmem_wait_st();
@@ -396,19 +384,177 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const Param
                 ptx::mbar_arrive(BAR(kBarWFree));
         }
 
-        auto collapse = [&](int itc) -> bool {
-            const int q = itc & 1;
-            const bool got = wait_bar<true>(BAR(kBarPre + q), (itc >> 1) & 1, abort_flag, sb, kSitePre);
-            if (!ptx::named_bar_and(1, kComputeThreads, got))
-                return false;
-            const int tile = cid + itc * ncl, t0 = tile * p.tm_tile;
-            const int tm = min(p.tm_tile, p.T - t0);
-            const int s = itc % L.nst;
-            const float *xs = stages + s * stage_floats;
+        const int lk4 = p.LK * 4;
+        for (int it = 0; ok; ++it) {
+            if (cid + it * ncl >= p.ntiles)
+                break;
+            const int s = it % L.nst, u = it / L.nst;
+            ok = ptx::named_bar_and(1, kComputeThreads,
+                                    wait_bar<false>(BAR(kBarXFull + s), u & 1, abort_flag, sb, kSiteXFull));
+            if (!ok)
+                break;
+            int t0, tm;
+            tile_tokens(it, t0, tm);
+            const int ntok = min(NT, max(0, tm - NT * tg));
+            // Byte address of token slot 0 of this half-warp, at this lane's first column group.
+            const uint32_t xs_addr = ptx::smem_u32(stages + s * stage_floats + (tg * NT) * p.LK) + 16u * kg;
+            const uint32_t ws_addr = ptx::smem_u32(wsm + (rg * G::B) * p.LK) + 16u * kg;
+            // Slots rg, rg+4, ... of this half-warp: the ones whose squares this warp sums.
+            const uint32_t xq_addr = xs_addr + (uint32_t)(rg * lk4);
+
+            // Every slot is computed (rows of a stage past the tile's last token hold stale
+            // but harmless data, never pushed), so the loop has no data-dependent branch.
+            float2 acc[NT][G::B];
+            float2 ssa[C::NSS];
+#pragma unroll
+            for (int i = 0; i < NT; ++i)
+#pragma unroll
+                for (int r = 0; r < G::B; ++r)
+                    acc[i][r] = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int m = 0; m < C::NSS; ++m)
+                ssa[m] = make_float2(0.f, 0.f);
+
+            if (PERSIST) {
+                // fn_w from TMEM, one column group at a time; the other compute warp
+                // of this sub-partition runs its FMAs while this one waits for a load.
+                for (int jj = 0; jj < nj; ++jj) {
+                    float w[G::WQ];
+                    ptx::tmem_ld_issue<G::WQ>(trow + (uint32_t)(jj * G::WQ), w);
+                    ptx::tmem_ld_wait_regs<G::WQ>(w);
+                    dots_step<S, NT>(acc, ssa, w, xs_addr, xq_addr, 256u * (uint32_t)(j0 + jj), lk4);
+                }
+            } else {
+                for (int jj = 0; jj < nj; ++jj) {
+                    const uint32_t cofs = 256u * (uint32_t)(j0 + jj);
+                    float w[G::WQ];
+#pragma unroll
+                    for (int r = 0; r < G::B; ++r) {
+                        const float4 v = ptx::lds128(ws_addr + (uint32_t)(r * lk4) + cofs);
+                        w[4 * r] = v.x;
+                        w[4 * r + 1] = v.y;
+                        w[4 * r + 2] = v.z;
+                        w[4 * r + 3] = v.w;
+                    }
+                    dots_step<S, NT>(acc, ssa, w, xs_addr, xq_addr, cofs, lk4);
+                }
+            }
+
+            // Half-warp sums over the 16 K-groups, into the local partial buffer.
+            float v[C::NVP];
+#pragma unroll
+            for (int i = 0; i < NT; ++i)
+#pragma unroll
+                for (int r = 0; r < G::B; ++r)
+                    v[i * G::B + r] = acc[i][r].x + acc[i][r].y;
+#pragma unroll
+            for (int m = 0; m < C::NSS; ++m)
+                v[NT * G::B + m] = ssa[m].x + ssa[m].y;
+#pragma unroll
+            for (int q = C::NV; q < C::NVP; ++q)
+                v[q] = 0.f;
+            reduce_scatter16<C::NVP>(v, kg);
+
+            const int qb = it & 1;
+            if (it >= 2) {   // the exchange warp has read this buffer's previous tile
+                ok = ptx::named_bar_and(1, kComputeThreads,
+                                        wait_bar<false>(BAR(kBarPartEmpty + qb), ((it >> 1) - 1) & 1,
+                                                        abort_flag, sb, kSitePartEmpty));
+                if (!ok)
+                    break;
+            }
+#pragma unroll
+            for (int q = 0; q < C::VPL; ++q) {
+                const int o = C::VPL * kg + q;
+                int i = NT, vid = -1;
+                if (o < NT * G::B) {
+                    i = o / G::B;
+                    const int row = rg * G::B + (o - i * G::B);
+                    vid = row < G::R ? row : -1;
+                } else if (o < C::NV) {
+                    i = rg + kRG * (o - NT * G::B);
+                    vid = G::R;
+                }
+                if (vid >= 0 && i < ntok)
+                    part_at(qb, half, tg * NT + i)[vid] = v[q];
+            }
+            __syncwarp();
+            if (lane == 0)
+                ptx::mbar_arrive(BAR(kBarPartFull + qb));
+        }
+    } else if (warp >= kExchangeWarp) {
+        // -------------------------------------------------------------- exchange warps
+        // Lane 0 does every wait and the warp follows its (broadcast) decision.  The
+        // warps also load x: exchange warp 0 issues the fn_w slice and the first
+        // tiles, and whichever warp collapses tile i refills its stage with tile
+        // i + nst.  The persistent variant stages fn_w in stages 1-2 (TMEM takes
+        // it from there), so the first x tile can land in stage 0 meanwhile.
+        const int e = warp - kExchangeWarp;
+        const uint32_t hs_bytes = (uint32_t)p.hs * 4u;
+        auto load_tile = [&](int it) {   // whole warp; stage it % nst must be free
+            const int s = it % L.nst;
+            int t0, tm;
+            tile_tokens(it, t0, tm);
+            if (lane == 0)
+                ptx::mbar_arrive_expect_tx(BAR(kBarXFull + s), (uint32_t)(tm * S) * hs_bytes);
+            __syncwarp();
+            float *xs = stages + s * stage_floats;
+            for (int q = lane; q < tm * S; q += 32) {
+                const int t = q / S, k = q - (q / S) * S;
+                ptx::bulk_g2s(ptx::smem_u32(xs + t * p.LK + k * p.hs),
+                              p.x + ((size_t)(t0 + t) * S + k) * p.d + (size_t)rank * p.hs, hs_bytes,
+                              BAR(kBarXFull + s));
+            }
+            __syncwarp();
+            if (lane == 0)
+                issued[s] = issued[s] + 1;
+        };
+        bool ok = true;
+        if (e == 0) {
+            float *wdst = PERSIST ? stages + stage_floats : wsm;
+            if (lane == 0)
+                ptx::mbar_arrive_expect_tx(BAR(kBarWFull), (uint32_t)(G::R * S) * hs_bytes);
+            __syncwarp();
+            for (int q = lane; q < G::R * S; q += 32) {
+                const int r = q / S, k = q - (q / S) * S;
+                ptx::bulk_g2s(ptx::smem_u32(wdst + r * p.LK + k * p.hs),
+                              p.fn_w + (size_t)r * K + (size_t)k * p.d + (size_t)rank * p.hs, hs_bytes,
+                              BAR(kBarWFull));
+            }
+            load_tile(0);   // tile 0 always exists (every cluster gets at least one)
+            if (L.nst > 1 && cid + ncl < p.ntiles) {
+                ok = warp_wait<false>(lane, BAR(kBarWFree), 0, abort_flag, sb, kSiteWFree);
+                for (int it = 1; ok && it < L.nst && cid + it * ncl < p.ntiles; ++it)
+                    load_tile(it);
+            }
+        }
+        for (int it = e; ok && cid + it * ncl < p.ntiles; it += 2) {
+            const int qb = it & 1, s = it % L.nst;
+            if (!warp_wait<false>(lane, BAR(kBarPartFull + qb), (it >> 1) & 1, abort_flag, sb, kSitePartFull))
+                break;
+            int t0, tm;
+            tile_tokens(it, t0, tm);
+            // Add the two column halves and push each token's values to its owner CTA.
+            for (int item = lane; item < tm * (G::R + 1); item += 32) {
+                const int t = item / (G::R + 1), vid = item - t * (G::R + 1);
+                const float val = part_at(qb, 0, t)[vid] + part_at(qb, 1, t)[vid];
+                const uint32_t local = ptx::smem_u32(recv + (qb * kCS + (int)rank) * G::RV + vid);
+                ptx::st_cluster_f32(ptx::mapa(local, (uint32_t)t), val);
+            }
+            __syncwarp();
+            if (lane == 0)
+                ptx::mbar_arrive(BAR(kBarPartEmpty + qb));
+            if (lane < kCS) {
+                ptx::fence_acq_rel_cluster();
+                ptx::mbar_arrive_remote(ptx::mapa(BAR(kBarRecv + qb), (uint32_t)lane));
+            }
+            // Collapse this CTA's hidden slice of every token of the tile.
+            if (!warp_wait<true>(lane, BAR(kBarPre + qb), (it >> 1) & 1, abort_flag, sb, kSitePre))
+                break;
+            const uint32_t xs_base = ptx::smem_u32(stages + s * stage_floats);
+            const uint32_t pre_base = ptx::smem_u32(preb + qb * kTMT * 4);
             const int h4n = p.hs / 4;
-            int t = threadIdx.x / h4n, h4 = threadIdx.x - (threadIdx.x / h4n) * h4n;
-            const uint32_t xs_base = ptx::smem_u32(xs);
-            const uint32_t pre_base = ptx::smem_u32(preb + q * kTMT * 4);
+            int t = lane / h4n, h4 = lane - (lane / h4n) * h4n;
             for (; t < tm;) {
                 float pr[S];
 #pragma unroll
@@ -426,160 +572,49 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const Param
                     a.w = fmaf(pr[k], xv.w, a.w);
                 }
                 *reinterpret_cast<float4 *>(p.y + (size_t)(t0 + t) * p.d + (size_t)rank * p.hs + 4 * h4) = a;
-                h4 += kComputeThreads;
+                h4 += 32;
                 while (h4 >= h4n) {
                     h4 -= h4n;
                     ++t;
                 }
             }
-            ptx::named_bar_sync(1, kComputeThreads);
-            if (threadIdx.x == 0)
-                ptx::mbar_arrive(BAR(kBarXEmpty + s));   // stage free for the producer
-            return true;
-        };
-
-        int it = 0;
-        for (; ok; ++it) {
-            const int tile = cid + it * ncl;
-            if (tile >= p.ntiles)
-                break;
-            const int s = it % L.nst, u = it / L.nst;
-            ok = ptx::named_bar_and(1, kComputeThreads,
-                                    wait_bar<false>(BAR(kBarXFull + s), u & 1, abort_flag, sb, kSiteXFull));
-            if (!ok)
-                break;
-            const int t0 = tile * p.tm_tile, tm = min(p.tm_tile, p.T - t0);
-            const int ntok = min(NT, max(0, tm - NT * tg));
-            // Byte address of token slot 0 of this half-warp, at this lane's first column group.
-            const uint32_t xs_addr = ptx::smem_u32(stages + s * stage_floats + (tg * NT) * p.LK) + 16u * kg;
-            const uint32_t ws_addr = ptx::smem_u32(wsm + (warp * G::B) * p.LK) + 16u * kg;
-            // Slots warp, warp+4, ... of this half-warp: the ones whose squares this warp sums.
-            const uint32_t xq_addr = xs_addr + (uint32_t)(warp * p.LK * 4);
-
-            // Packed float32 FMAs: acc[i][r] holds (sum over even columns, sum over odd columns).
-            // Every slot is computed (rows of a stage past the tile's last token hold stale but
-            // harmless data, never pushed), so the loop has no data-dependent branch.
-            float2 acc[NT][G::B];
-            float2 ssa[C::NSS];
-#pragma unroll
-            for (int i = 0; i < NT; ++i)
-#pragma unroll
-                for (int r = 0; r < G::B; ++r)
-                    acc[i][r] = make_float2(0.f, 0.f);
-#pragma unroll
-            for (int m = 0; m < C::NSS; ++m)
-                ssa[m] = make_float2(0.f, 0.f);
-
-            const int lk4 = p.LK * 4;
-            if (PERSIST) {
-                // fn_w from TMEM, double-buffered without copies: wa holds even column
-                // groups, wb odd ones; the load of the next group overlaps this one's FMAs.
-                float wa[G::WQ], wb[G::WQ];
-                ptx::tmem_ld_issue<G::WQ>(trow, wa);
-                ptx::tmem_ld_wait_regs<G::WQ>(wa);
-                for (int j = 0; j < p.NJ; j += 2) {
-                    const bool odd = j + 1 < p.NJ;
-                    if (odd)
-                        ptx::tmem_ld_issue<G::WQ>(trow + (uint32_t)((j + 1) * G::WQ), wb);
-                    dots_step<S, NT>(acc, ssa, wa, xs_addr, xq_addr, 256u * (uint32_t)j, lk4);
-                    if (!odd)
-                        break;
-                    ptx::tmem_ld_wait_regs<G::WQ>(wb);
-                    const bool next = j + 2 < p.NJ;
-                    if (next)
-                        ptx::tmem_ld_issue<G::WQ>(trow + (uint32_t)((j + 2) * G::WQ), wa);
-                    dots_step<S, NT>(acc, ssa, wb, xs_addr, xq_addr, 256u * (uint32_t)(j + 1), lk4);
-                    if (next)
-                        ptx::tmem_ld_wait_regs<G::WQ>(wa);
-                }
-            } else {
-                for (int j = 0; j < p.NJ; ++j) {
-                    const uint32_t cofs = 256u * (uint32_t)j;
-                    float w[G::WQ];
-#pragma unroll
-                    for (int r = 0; r < G::B; ++r) {
-                        const float4 v = ptx::lds128(ws_addr + (uint32_t)(r * lk4) + cofs);
-                        w[4 * r] = v.x;
-                        w[4 * r + 1] = v.y;
-                        w[4 * r + 2] = v.z;
-                        w[4 * r + 3] = v.w;
-                    }
-                    dots_step<S, NT>(acc, ssa, w, xs_addr, xq_addr, cofs, lk4);
-                }
-            }
-
-            // Half-warp sums over the 16 K-groups, then push to the owners.
-            float v[C::NVP];
-#pragma unroll
-            for (int i = 0; i < NT; ++i)
-#pragma unroll
-                for (int r = 0; r < G::B; ++r)
-                    v[i * G::B + r] = acc[i][r].x + acc[i][r].y;
-#pragma unroll
-            for (int m = 0; m < C::NSS; ++m)
-                v[NT * G::B + m] = ssa[m].x + ssa[m].y;
-#pragma unroll
-            for (int q = C::NV; q < C::NVP; ++q)
-                v[q] = 0.f;
-            reduce_scatter16<C::NVP>(v, kg);
-            const int qb = it & 1;
-#pragma unroll
-            for (int q = 0; q < C::VPL; ++q) {
-                const int o = C::VPL * kg + q;
-                int i = NT, vid = -1;
-                if (o < NT * G::B) {
-                    i = o / G::B;
-                    const int row = warp * G::B + (o - i * G::B);
-                    vid = row < G::R ? row : -1;
-                } else if (o < C::NV) {
-                    i = warp + kNCW * (o - NT * G::B);
-                    vid = G::R;
-                }
-                if (vid >= 0 && i < ntok) {
-                    const uint32_t local = ptx::smem_u32(recv + (qb * kCS + (int)rank) * G::RV + vid);
-                    ptx::st_cluster_f32(ptx::mapa(local, (uint32_t)(tg * NT + i)), v[q]);
-                }
-            }
-            ptx::named_bar_sync(1, kComputeThreads);
-            if (threadIdx.x < kCS) {
-                ptx::fence_acq_rel_cluster();
-                ptx::mbar_arrive_remote(ptx::mapa(BAR(kBarRecv + qb), threadIdx.x));
-            }
-            if (it > 0 && !(ok = collapse(it - 1)))
-                break;
+            __syncwarp();
+            // The compute warps are done with this stage (its tile's partials are
+            // in) and so is the collapse: refill it.
+            if (cid + (it + L.nst) * ncl < p.ntiles)
+                load_tile(it + L.nst);
         }
-        if (ok && it > 0)
-            collapse(it - 1);
+        // Every bulk copy this CTA issued lands before the CTA may exit: once both
+        // exchange warps are done issuing, wait for the last phase of each stage.
+        ptx::named_bar_sync(2, 64);
+        if (e == 0 && lane == 0) {
+            wait_bar<false>(BAR(kBarWFull), 0, abort_flag, sb, kSiteDrain, false);
+            for (int s = 0; s < L.nst; ++s)
+                if (issued[s] > 0)
+                    wait_bar<false>(BAR(kBarXFull + s), (issued[s] - 1) & 1, abort_flag, sb, kSiteDrain, false);
+        }
+        __syncwarp();
     } else {
         // -------------------------------------------------------------- finisher warps
-        // Lane 0 waits; the acquire it performs, followed by __syncwarp, orders
-        // the other lanes' reads of the remotely written partials after it.
         const int f = warp - kFinisherWarp;
         const int grp = lane < S ? 0 : (lane < 2 * S ? 1 : 2);
         const float my_scale = lane < G::R ? p.scale[grp] : 0.f;
         const float my_base = lane < G::R ? p.base[lane] : 0.f;
-        for (int it = f;; it += 2) {
-            const int tile = cid + it * ncl;
-            if (tile >= p.ntiles)
-                break;
+        for (int it = f; cid + it * ncl < p.ntiles; it += 2) {
             const int qb = it & 1;
-            bool got = true;
-            if (lane == 0)
-                got = wait_bar<true>(BAR(kBarRecv + qb), (it >> 1) & 1, abort_flag, sb, kSiteRecv);
-            got = __shfl_sync(kFull, got, 0);
-            __syncwarp();
-            if (!got)
+            if (!warp_wait<true>(lane, BAR(kBarRecv + qb), (it >> 1) & 1, abort_flag, sb, kSiteRecv))
                 break;
-            const int t0 = tile * p.tm_tile, tm = min(p.tm_tile, p.T - t0);
+            int t0, tm;
+            tile_tokens(it, t0, tm);
             const bool own = (int)rank < tm;
             float val = 0.f;
             if (own && lane <= G::R) {
-                float part[kCS];
+                float src[kCS];
                 const uint32_t a0 = ptx::smem_u32(recv + qb * kCS * G::RV + lane);
 #pragma unroll
                 for (int c = 0; c < kCS; ++c)
-                    part[c] = ptx::lds32(a0 + 4u * (uint32_t)(c * G::RV));
-                val = tree_sum<kCS>(part);   // sources in a fixed pairwise order
+                    src[c] = ptx::lds32(a0 + 4u * (uint32_t)(c * G::RV));
+                val = tree_sum<kCS>(src);   // sources in a fixed pairwise order
             }
             const float ss = __shfl_sync(kFull, val, G::R);
             const float rinv = rsqrtf(ss / p.Kf + p.eps);
