@@ -108,12 +108,12 @@ __host__ __device__ inline Lay make_lay(int LK)
     L.off_w = o;
     if (!PERSIST)
         o += G::RP * LK * 4;
-    L.off_recv = o;                  // [2 tile parities][16 source CTAs][RV]
-    o += 2 * kCS * G::RV * 4;
+    L.off_recv = o;                  // [2 tile parities][2 column halves][16 source CTAs][RV]
+    o += 2 * 2 * kCS * G::RV * 4;
     L.off_part = o;                  // [2 tile parities][2 column halves][16 tokens][RV]
     o += 2 * 2 * kTMT * G::RV * 4;
-    L.off_pre = o;                   // [2 tile parities][16 tokens][4]
-    o += 2 * kTMT * 4 * 4;
+    L.off_pre = o;                   // [2 tile parities][16 tokens][4], then own pre [2][4]
+    o += 2 * kTMT * 4 * 4 + 2 * 4 * 4;
     L.off_bar = o;
     o += kNumBars * 8;
     L.off_misc = o;                  // TMEM address, abort flag, bulk-copy phases issued per stage
@@ -215,35 +215,6 @@ __device__ __forceinline__ float tree_sum(const float *v)
     }
 }
 
-// Sinkhorn on an S x S matrix held in registers: `iters` rounds of dividing
-// each row by (row sum + eps), then each column by (column sum + eps).  The
-// reciprocal is the hardware approximation (__fdividef, within 2 ulp); the
-// Sinkhorn's own error budget against the float64 oracle is 1e-4.
-template <int S>
-__device__ __forceinline__ void sinkhorn_regs(float *c, int iters, float eps)
-{
-    for (int it = 0; it < iters; ++it) {
-#pragma unroll
-        for (int j = 0; j < S; ++j) {
-            const float inv = __fdividef(1.0f, tree_sum<S>(c + j * S) + eps);
-#pragma unroll
-            for (int k = 0; k < S; ++k)
-                c[j * S + k] *= inv;
-        }
-#pragma unroll
-        for (int k = 0; k < S; ++k) {
-            float col[S];
-#pragma unroll
-            for (int j = 0; j < S; ++j)
-                col[j] = c[j * S + k];
-            const float inv = __fdividef(1.0f, tree_sum<S>(col) + eps);
-#pragma unroll
-            for (int j = 0; j < S; ++j)
-                c[j * S + k] *= inv;
-        }
-    }
-}
-
 // One column group of the dots: 4 columns of the NT token slots of this half-warp,
 // times this warp's B rows, as packed float32 FMAs (acc = (even-column sum,
 // odd-column sum)); plus the sums of squares of this warp's NSS slots.
@@ -324,8 +295,8 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const Param
             issued[s] = 0;
         }
         for (int q = 0; q < 2; ++q) {
-            ptx::mbar_init(BAR(kBarRecv + q), kCS);
-            ptx::mbar_init(BAR(kBarPre + q), kCS);
+            ptx::mbar_init(BAR(kBarRecv + q), 1);   // armed by this CTA; data by bulk copies
+            ptx::mbar_init(BAR(kBarPre + q), 1);
             ptx::mbar_init(BAR(kBarPartFull + q), kNCW);
             ptx::mbar_init(BAR(kBarPartEmpty + q), 1);
         }
@@ -478,6 +449,7 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const Param
                 if (vid >= 0 && i < ntok)
                     part_at(qb, half, tg * NT + i)[vid] = v[q];
             }
+            ptx::fence_proxy_async_smem();   // the exchange warp ships them with bulk copies
             __syncwarp();
             if (lane == 0)
                 ptx::mbar_arrive(BAR(kBarPartFull + qb));
@@ -534,48 +506,51 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const Param
                 break;
             int t0, tm;
             tile_tokens(it, t0, tm);
-            // Add the two column halves and push each token's values to its owner CTA.
-            for (int item = lane; item < tm * (G::R + 1); item += 32) {
-                const int t = item / (G::R + 1), vid = item - t * (G::R + 1);
-                const float val = part_at(qb, 0, t)[vid] + part_at(qb, 1, t)[vid];
-                const uint32_t local = ptx::smem_u32(recv + (qb * kCS + (int)rank) * G::RV + vid);
-                ptx::st_cluster_f32(ptx::mapa(local, (uint32_t)t), val);
+            // Ship each token's two column-half partials to its owner CTA (token t of the
+            // tile belongs to CTA t) with bulk copies that complete on the owner's
+            // recv barrier.  Only a cluster's last tile can be partial, so no later
+            // tile's bytes can reach a CTA that owns nothing in this one.
+            if (lane < 2 * tm) {
+                const int h = lane / tm, t = lane - (lane / tm) * tm;
+                const uint32_t dst = ptx::smem_u32(recv + ((qb * 2 + h) * kCS + (int)rank) * G::RV);
+                ptx::bulk_s2cluster(ptx::mapa(dst, (uint32_t)t), ptx::smem_u32(part_at(qb, h, t)),
+                                    (uint32_t)(G::RV * 4), ptx::mapa(BAR(kBarRecv + qb), (uint32_t)t));
             }
-            __syncwarp();
+            // The owners send back the tile's pre gates (16 bytes each).
+            if (lane == 0)
+                ptx::mbar_arrive_expect_tx(BAR(kBarPre + qb), (uint32_t)(tm * 16));
+            if (!warp_wait<true>(lane, BAR(kBarPre + qb), (it >> 1) & 1, abort_flag, sb, kSitePre)) {
+                // Giving up: still let any gates already on their way land before exit.
+                if (lane == 0)
+                    wait_bar<true>(BAR(kBarPre + qb), (it >> 1) & 1, abort_flag, sb, kSiteDrain, false);
+                __syncwarp();
+                break;
+            }
+            // Every owner has received this CTA's partials (it answered), so the
+            // partial buffer is free for tile it + 2.
             if (lane == 0)
                 ptx::mbar_arrive(BAR(kBarPartEmpty + qb));
-            if (lane < kCS) {
-                ptx::fence_acq_rel_cluster();
-                ptx::mbar_arrive_remote(ptx::mapa(BAR(kBarRecv + qb), (uint32_t)lane));
-            }
             // Collapse this CTA's hidden slice of every token of the tile.
-            if (!warp_wait<true>(lane, BAR(kBarPre + qb), (it >> 1) & 1, abort_flag, sb, kSitePre))
-                break;
             const uint32_t xs_base = ptx::smem_u32(stages + s * stage_floats);
             const uint32_t pre_base = ptx::smem_u32(preb + qb * kTMT * 4);
             const int h4n = p.hs / 4;
-            int t = lane / h4n, h4 = lane - (lane / h4n) * h4n;
-            for (; t < tm;) {
-                float pr[S];
+            for (int t = 0; t < tm; ++t) {
+                const float4 pv = ptx::lds128(pre_base + 16u * (uint32_t)t);
+                const float pr[4] = {pv.x, pv.y, pv.z, pv.w};
+                const uint32_t xt = xs_base + 4u * (uint32_t)(t * p.LK);
+                float *yt = p.y + (size_t)(t0 + t) * p.d + (size_t)rank * p.hs;
+                for (int h4 = lane; h4 < h4n; h4 += 32) {
+                    float4 xv = ptx::lds128(xt + 16u * (uint32_t)h4);
+                    float4 acc4 = make_float4(pr[0] * xv.x, pr[0] * xv.y, pr[0] * xv.z, pr[0] * xv.w);
 #pragma unroll
-                for (int k = 0; k < S; ++k)
-                    pr[k] = ptx::lds32(pre_base + 4u * (uint32_t)(t * 4 + k));
-                const uint32_t xa = xs_base + 4u * (uint32_t)(t * p.LK + 4 * h4);
-                float4 xv = ptx::lds128(xa);
-                float4 a = make_float4(pr[0] * xv.x, pr[0] * xv.y, pr[0] * xv.z, pr[0] * xv.w);
-#pragma unroll
-                for (int k = 1; k < S; ++k) {
-                    xv = ptx::lds128(xa + 4u * (uint32_t)(k * p.hs));
-                    a.x = fmaf(pr[k], xv.x, a.x);
-                    a.y = fmaf(pr[k], xv.y, a.y);
-                    a.z = fmaf(pr[k], xv.z, a.z);
-                    a.w = fmaf(pr[k], xv.w, a.w);
-                }
-                *reinterpret_cast<float4 *>(p.y + (size_t)(t0 + t) * p.d + (size_t)rank * p.hs + 4 * h4) = a;
-                h4 += 32;
-                while (h4 >= h4n) {
-                    h4 -= h4n;
-                    ++t;
+                    for (int k = 1; k < S; ++k) {
+                        xv = ptx::lds128(xt + 4u * (uint32_t)(k * p.hs) + 16u * (uint32_t)h4);
+                        acc4.x = fmaf(pr[k], xv.x, acc4.x);
+                        acc4.y = fmaf(pr[k], xv.y, acc4.y);
+                        acc4.z = fmaf(pr[k], xv.z, acc4.z);
+                        acc4.w = fmaf(pr[k], xv.w, acc4.w);
+                    }
+                    *reinterpret_cast<float4 *>(yt + 4 * h4) = acc4;
                 }
             }
             __syncwarp();
@@ -600,58 +575,71 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const Param
         const int grp = lane < S ? 0 : (lane < 2 * S ? 1 : 2);
         const float my_scale = lane < G::R ? p.scale[grp] : 0.f;
         const float my_base = lane < G::R ? p.base[lane] : 0.f;
+        float *pre_send = preb + 2 * kTMT * 4;   // [2][4]: this CTA's own token's pre gates
         for (int it = f; cid + it * ncl < p.ntiles; it += 2) {
             const int qb = it & 1;
-            if (!warp_wait<true>(lane, BAR(kBarRecv + qb), (it >> 1) & 1, abort_flag, sb, kSiteRecv))
-                break;
             int t0, tm;
             tile_tokens(it, t0, tm);
             const bool own = (int)rank < tm;
+            // Arm this tile's phase: an owner expects two column halves from 16 CTAs.
+            if (lane == 0)
+                ptx::mbar_arrive_expect_tx(BAR(kBarRecv + qb), own ? (uint32_t)(2 * kCS * G::RV * 4) : 0u);
+            if (!warp_wait<true>(lane, BAR(kBarRecv + qb), (it >> 1) & 1, abort_flag, sb, kSiteRecv)) {
+                // Giving up: still let any partials already on their way land before exit.
+                if (lane == 0)
+                    wait_bar<true>(BAR(kBarRecv + qb), (it >> 1) & 1, abort_flag, sb, kSiteDrain, false);
+                __syncwarp();
+                break;
+            }
+            if (!own)
+                continue;
             float val = 0.f;
-            if (own && lane <= G::R) {
-                float src[kCS];
-                const uint32_t a0 = ptx::smem_u32(recv + qb * kCS * G::RV + lane);
+            if (lane <= G::R) {
+                float src[2 * kCS];
+                const uint32_t a0 = ptx::smem_u32(recv + qb * 2 * kCS * G::RV + lane);
 #pragma unroll
-                for (int c = 0; c < kCS; ++c)
+                for (int c = 0; c < 2 * kCS; ++c)
                     src[c] = ptx::lds32(a0 + 4u * (uint32_t)(c * G::RV));
-                val = tree_sum<kCS>(src);   // sources in a fixed pairwise order
+                val = tree_sum<2 * kCS>(src);   // halves and sources in a fixed pairwise order
             }
             const float ss = __shfl_sync(kFull, val, G::R);
             const float rinv = rsqrtf(ss / p.Kf + p.eps);
             const float logit = lane < G::R ? val * rinv * my_scale + my_base : 0.f;
             const float sg = 1.f / (1.f + expf(-logit));
             const float pre_v = sg + p.eps;
-            float pk[S];
-#pragma unroll
-            for (int k = 0; k < S; ++k)
-                pk[k] = __shfl_sync(kFull, pre_v, k);
+            // pre gates of this token -> every CTA of the cluster (16 bytes each).
+            if (lane < 4)
+                pre_send[qb * 4 + lane] = lane < S ? pre_v : 0.f;
+            ptx::fence_proxy_async_smem();
+            __syncwarp();
             if (lane < kCS) {
-                if (own) {
-                    const uint32_t loc = ptx::smem_u32(preb + (qb * kTMT + (int)rank) * 4);
-#pragma unroll
-                    for (int k = 0; k < S; ++k)
-                        ptx::st_cluster_f32(ptx::mapa(loc + 4u * k, (uint32_t)lane), pk[k]);
-                }
-                ptx::mbar_arrive_remote(ptx::mapa(BAR(kBarPre + qb), (uint32_t)lane));
+                const uint32_t dst = ptx::smem_u32(preb + (qb * kTMT + (int)rank) * 4);
+                ptx::bulk_s2cluster(ptx::mapa(dst, (uint32_t)lane), ptx::smem_u32(pre_send + qb * 4), 16u,
+                                    ptx::mapa(BAR(kBarPre + qb), (uint32_t)lane));
             }
-            if (own) {
-                const size_t tok = (size_t)t0 + rank;
-                if (lane < S)
-                    p.pre[tok * S + lane] = pre_v;
-                else if (lane < 2 * S)
-                    p.post[tok * S + (lane - S)] = 2.f * sg;
-                const float e = (lane >= 2 * S && lane < G::R) ? expf(logit) : 0.f;
-                float cm[S * S];
-#pragma unroll
-                for (int q = 0; q < S * S; ++q)
-                    cm[q] = __shfl_sync(kFull, e, 2 * S + q);
-                if (lane == 0) {
-                    sinkhorn_regs<S>(cm, p.iters, p.eps);
-#pragma unroll
-                    for (int q = 0; q < S * S; ++q)
-                        p.comb[tok * S * S + q] = cm[q];
-                }
+            const size_t tok = (size_t)t0 + rank;
+            if (lane < S)
+                p.pre[tok * S + lane] = pre_v;
+            else if (lane < 2 * S)
+                p.post[tok * S + (lane - S)] = 2.f * sg;
+            // Sinkhorn with one matrix entry per lane: lane 4j+k holds comb[j][k]
+            // (entries outside the S x S block are 0); rows sum over xor 1, 2 and
+            // columns over xor 4, 8.
+            const int j = (lane >> 2) & 3, k = lane & 3;
+            const bool in = lane < 16 && j < S && k < S;
+            const float ev = (lane >= 2 * S && lane < G::R) ? expf(logit) : 0.f;
+            float c = __shfl_sync(kFull, ev, 2 * S + (in ? j * S + k : 0));
+            c = in ? c : 0.f;
+            for (int r = 0; r < p.iters; ++r) {
+                float rs = c + __shfl_xor_sync(kFull, c, 1);
+                rs += __shfl_xor_sync(kFull, rs, 2);
+                c *= __fdividef(1.0f, rs + p.eps);
+                float cs = c + __shfl_xor_sync(kFull, c, 4);
+                cs += __shfl_xor_sync(kFull, cs, 8);
+                c *= __fdividef(1.0f, cs + p.eps);
             }
+            if (in)
+                p.comb[tok * S * S + j * S + k] = c;
             __syncwarp();
         }
     }

@@ -116,6 +116,23 @@ __device__ __forceinline__ float lds32(uint32_t addr)
     return v;
 }
 
+// shared memory of this CTA -> shared memory of a CTA of the cluster (dst and its
+// mbarrier given as shared::cluster addresses from mapa); completion counted in
+// bytes on the destination's mbarrier.  16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_s2cluster(uint32_t dst_cluster, uint32_t src_cta, uint32_t bytes,
+                                               uint32_t bar_cluster)
+{
+    asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     dst_cluster),
+                 "r"(src_cta), "r"(bytes), "r"(bar_cluster)
+                 : "memory");
+}
+// Make this thread's earlier generic-proxy shared-memory writes visible to bulk copies.
+__device__ __forceinline__ void fence_proxy_async_smem()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- cluster / DSMEM
 __device__ __forceinline__ uint32_t mapa(uint32_t local_smem, uint32_t rank)
 {
