@@ -56,8 +56,7 @@ constexpr int kTMT = 16;             // max tokens per tile = one owner CTA per 
 constexpr int kRG = 4;               // row groups (compute warps w and w+4 share one)
 constexpr int kNCW = 8;              // compute warps: two per SM sub-partition
 constexpr int kFinisherWarp = 8;     // warps 8 and 9 take even and odd tiles
-constexpr int kExchangeWarp = 10;    // warps 10 and 11 take even and odd tiles (and load x)
-constexpr int kThreads = 12 * 32;    // three warps per sub-partition: up to 168 registers each
+constexpr int kThreads = 10 * 32;    // at most three warps per sub-partition: 168 registers each
 constexpr int kComputeThreads = kNCW * 32;
 constexpr int kNstPersist = 3;
 constexpr int kMaxLK = 1024;         // s*d/16 <= 1024: three 64 KiB stages fit in shared memory
@@ -66,12 +65,9 @@ constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 constexpr unsigned kFull = 0xffffffffu;
 
 // mbarrier slots
-constexpr int kBarXFull = 0, kBarRecv = 3, kBarPre = 5, kBarWFull = 7, kBarWFree = 8,
-              kBarPartFull = 9, kBarPartEmpty = 11, kNumBars = 13;
-enum WaitSite : unsigned {
-    kSiteWFull = 1, kSiteXFull, kSiteRecv, kSitePre, kSiteWFree, kSiteDrain, kSitePartFull,
-    kSitePartEmpty
-};
+constexpr int kBarXFull = 0, kBarRecv = 3, kBarPre = 5, kBarSink = 7, kBarWFull = 8, kBarWFree = 9,
+              kNumBars = 10;
+enum WaitSite : unsigned { kSiteWFull = 1, kSiteXFull, kSiteRecv, kSitePre, kSiteSink, kSiteDrain };
 
 template <int S>
 struct CG {
@@ -94,7 +90,8 @@ struct CT {
 };
 
 struct Lay {   // shared-memory layout in bytes
-    int stage_bytes, nst, off_w, off_recv, off_part, off_pre, off_bar, off_misc, total;
+    int stage_bytes, nst, off_w, off_recv, off_part, off_pre, off_pre_send, off_esend, off_sink, off_bar,
+        off_misc, total;
 };
 
 template <int S, bool PERSIST>
@@ -112,8 +109,14 @@ __host__ __device__ inline Lay make_lay(int LK)
     o += 2 * 2 * kCS * G::RV * 4;
     L.off_part = o;                  // [2 tile parities][2 column halves][16 tokens][RV]
     o += 2 * 2 * kTMT * G::RV * 4;
-    L.off_pre = o;                   // [2 tile parities][16 tokens][4], then own pre [2][4]
-    o += 2 * kTMT * 4 * 4 + 2 * 4 * 4;
+    L.off_pre = o;                   // [2 tile parities][16 tokens][4]: the tile's pre gates
+    o += 2 * kTMT * 4 * 4;
+    L.off_pre_send = o;              // [2][4]: this CTA's own token's pre gates
+    o += 2 * 4 * 4;
+    L.off_esend = o;                 // [4][16]: its exp(comb logits)
+    o += 4 * 16 * 4;
+    L.off_sink = o;                  // [16 tokens][16]: the comb blocks this CTA scales
+    o += kTMT * 16 * 4;
     L.off_bar = o;
     o += kNumBars * 8;
     L.off_misc = o;                  // TMEM address, abort flag, bulk-copy phases issued per stage
@@ -215,6 +218,35 @@ __device__ __forceinline__ float tree_sum(const float *v)
     }
 }
 
+// Sinkhorn on an S x S matrix held in registers: `iters` rounds of dividing
+// each row by (row sum + eps), then each column by (column sum + eps).  The
+// reciprocal is the hardware approximation (__fdividef, within 2 ulp); the
+// Sinkhorn's error budget against the float64 oracle is 1e-4.
+template <int S>
+__device__ __forceinline__ void sinkhorn_regs(float *c, int iters, float eps)
+{
+    for (int it = 0; it < iters; ++it) {
+#pragma unroll
+        for (int j = 0; j < S; ++j) {
+            const float inv = __fdividef(1.0f, tree_sum<S>(c + j * S) + eps);
+#pragma unroll
+            for (int k = 0; k < S; ++k)
+                c[j * S + k] *= inv;
+        }
+#pragma unroll
+        for (int k = 0; k < S; ++k) {
+            float col[S];
+#pragma unroll
+            for (int j = 0; j < S; ++j)
+                col[j] = c[j * S + k];
+            const float inv = __fdividef(1.0f, tree_sum<S>(col) + eps);
+#pragma unroll
+            for (int j = 0; j < S; ++j)
+                c[j * S + k] *= inv;
+        }
+    }
+}
+
 // One column group of the dots: 4 columns of the NT token slots of this half-warp,
 // times this warp's B rows, as packed float32 FMAs (acc = (even-column sum,
 // odd-column sum)); plus the sums of squares of this warp's NSS slots.
@@ -273,6 +305,9 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const Param
     float *recv = reinterpret_cast<float *>(smem + L.off_recv);
     float *part = reinterpret_cast<float *>(smem + L.off_part);
     float *preb = reinterpret_cast<float *>(smem + L.off_pre);
+    float *pre_send = reinterpret_cast<float *>(smem + L.off_pre_send);
+    float *esend = reinterpret_cast<float *>(smem + L.off_esend);
+    float *sinkbuf = reinterpret_cast<float *>(smem + L.off_sink);
     const uint32_t bar0 = ptx::smem_u32(smem + L.off_bar);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L.off_misc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L.off_misc + 4);
@@ -286,7 +321,28 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const Param
         t0 = (cid + it * ncl) * p.tm_tile;
         tm = min(p.tm_tile, p.T - t0);
     };
+    auto tile_exists = [&](int it) { return cid + it * ncl < p.ntiles; };
     auto part_at = [&](int q, int h, int t) { return part + ((q * 2 + h) * kTMT + t) * G::RV; };
+    const uint32_t hs_bytes = (uint32_t)p.hs * 4u;
+    // Bulk-load tile `it` into its stage (whole warp; the stage must be free).
+    auto load_tile = [&](int it) {
+        const int s = it % L.nst;
+        int t0, tm;
+        tile_tokens(it, t0, tm);
+        if (lane == 0)
+            ptx::mbar_arrive_expect_tx(BAR(kBarXFull + s), (uint32_t)(tm * S) * hs_bytes);
+        __syncwarp();
+        float *xs = stages + s * stage_floats;
+        for (int q = lane; q < tm * S; q += 32) {
+            const int t = q / S, k = q - (q / S) * S;
+            ptx::bulk_g2s(ptx::smem_u32(xs + t * p.LK + k * p.hs),
+                          p.x + ((size_t)(t0 + t) * S + k) * p.d + (size_t)rank * p.hs, hs_bytes,
+                          BAR(kBarXFull + s));
+        }
+        __syncwarp();
+        if (lane == 0)
+            issued[s] = issued[s] + 1;
+    };
 
     // ------------------------------------------------------------------ set-up
     if (threadIdx.x == 0) {
@@ -297,9 +353,8 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const Param
         for (int q = 0; q < 2; ++q) {
             ptx::mbar_init(BAR(kBarRecv + q), 1);   // armed by this CTA; data by bulk copies
             ptx::mbar_init(BAR(kBarPre + q), 1);
-            ptx::mbar_init(BAR(kBarPartFull + q), kNCW);
-            ptx::mbar_init(BAR(kBarPartEmpty + q), 1);
         }
+        ptx::mbar_init(BAR(kBarSink), 1);
         ptx::mbar_init(BAR(kBarWFull), 1);
         ptx::mbar_init(BAR(kBarWFree), 1);
         *abort_flag = 0;
@@ -316,7 +371,7 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const Param
     __syncwarp();
     if (PERSIST)
         ptx::tmem_fence_before_sync();
-    ptx::cluster_sync_all();   // barriers initialised in every CTA before any remote arrive
+    ptx::cluster_sync_all();   // barriers initialised in every CTA before any remote bulk copy
     if (PERSIST)
         ptx::tmem_fence_after_sync();
     const uint32_t tmem_base = PERSIST ? *tmem_slot : 0u;
@@ -332,6 +387,21 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const Param
         // TMEM: warp w reads lanes 32*(w%4).. of its sub-partition; the two warps of
         // a sub-partition (the two column halves) use disjoint column ranges.
         const uint32_t trow = tmem_base + ((uint32_t)(32 * rg) << 16) + (uint32_t)(half * njh * G::WQ);
+        if (warp == 0) {
+            // fn_w slice (the persistent variant stages it in stages 1-2, so tile 0
+            // can land in stage 0 meanwhile), then the first tile.
+            float *wdst = PERSIST ? stages + stage_floats : wsm;
+            if (lane == 0)
+                ptx::mbar_arrive_expect_tx(BAR(kBarWFull), (uint32_t)(G::R * S) * hs_bytes);
+            __syncwarp();
+            for (int q = lane; q < G::R * S; q += 32) {
+                const int r = q / S, k = q - (q / S) * S;
+                ptx::bulk_g2s(ptx::smem_u32(wdst + r * p.LK + k * p.hs),
+                              p.fn_w + (size_t)r * K + (size_t)k * p.d + (size_t)rank * p.hs, hs_bytes,
+                              BAR(kBarWFull));
+            }
+            load_tile(0);   // every cluster has at least one tile
+        }
         bool ok = ptx::named_bar_and(1, kComputeThreads,
                                      wait_bar<false>(BAR(kBarWFull), 0, abort_flag, sb, kSiteWFull));
         if (PERSIST && ok) {
@@ -351,13 +421,54 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const Param
             }
             ptx::tmem_wait_st();
             ptx::named_bar_sync(1, kComputeThreads);
-            if (threadIdx.x == 0)
-                ptx::mbar_arrive(BAR(kBarWFree));
+            // Stages 1 and 2 are free now.
+            if (warp == 0)
+                for (int it = 1; it < L.nst && tile_exists(it); ++it)
+                    load_tile(it);
         }
 
+        // Collapse tile itc (its pre gates arrive from the owners), then refill its
+        // stage with tile itc + nst.
+        auto collapse = [&](int itc) -> bool {
+            const int q = itc & 1;
+            const bool got = wait_bar<true>(BAR(kBarPre + q), (itc >> 1) & 1, abort_flag, sb, kSitePre);
+            if (!ptx::named_bar_and(1, kComputeThreads, got))
+                return false;
+            int t0, tm;
+            tile_tokens(itc, t0, tm);
+            const int s = itc % L.nst;
+            const uint32_t xs_base = ptx::smem_u32(stages + s * stage_floats);
+            const uint32_t pre_base = ptx::smem_u32(preb + q * kTMT * 4);
+            const int h4n = p.hs / 4;
+            for (int e = threadIdx.x; e < kTMT * h4n; e += kComputeThreads) {
+                const int t = e / h4n, h4 = e - t * h4n;
+                if (t >= tm)
+                    break;
+                const float4 pv = ptx::lds128(pre_base + 16u * (uint32_t)t);
+                const float pr[4] = {pv.x, pv.y, pv.z, pv.w};
+                const uint32_t xa = xs_base + 4u * (uint32_t)(t * p.LK + 4 * h4);
+                float4 xv = ptx::lds128(xa);
+                float4 a = make_float4(pr[0] * xv.x, pr[0] * xv.y, pr[0] * xv.z, pr[0] * xv.w);
+#pragma unroll
+                for (int k = 1; k < S; ++k) {
+                    xv = ptx::lds128(xa + 4u * (uint32_t)(k * p.hs));
+                    a.x = fmaf(pr[k], xv.x, a.x);
+                    a.y = fmaf(pr[k], xv.y, a.y);
+                    a.z = fmaf(pr[k], xv.z, a.z);
+                    a.w = fmaf(pr[k], xv.w, a.w);
+                }
+                *reinterpret_cast<float4 *>(p.y + (size_t)(t0 + t) * p.d + (size_t)rank * p.hs + 4 * h4) = a;
+            }
+            ptx::named_bar_sync(1, kComputeThreads);
+            if (warp == 0 && tile_exists(itc + L.nst))
+                load_tile(itc + L.nst);
+            return true;
+        };
+
         const int lk4 = p.LK * 4;
-        for (int it = 0; ok; ++it) {
-            if (cid + it * ncl >= p.ntiles)
+        int it = 0;
+        for (; ok; ++it) {
+            if (!tile_exists(it))
                 break;
             const int s = it % L.nst, u = it / L.nst;
             ok = ptx::named_bar_and(1, kComputeThreads,
@@ -374,7 +485,7 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const Param
             const uint32_t xq_addr = xs_addr + (uint32_t)(rg * lk4);
 
             // Every slot is computed (rows of a stage past the tile's last token hold stale
-            // but harmless data, never pushed), so the loop has no data-dependent branch.
+            // but harmless data, never sent), so the loop has no data-dependent branch.
             float2 acc[NT][G::B];
             float2 ssa[C::NSS];
 #pragma unroll
@@ -425,15 +536,9 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const Param
             for (int q = C::NV; q < C::NVP; ++q)
                 v[q] = 0.f;
             reduce_scatter16<C::NVP>(v, kg);
-
+            // (this buffer's previous tile, it - 2, left with the copies that the owners
+            // answered before collapse(it - 2) went ahead)
             const int qb = it & 1;
-            if (it >= 2) {   // the exchange warp has read this buffer's previous tile
-                ok = ptx::named_bar_and(1, kComputeThreads,
-                                        wait_bar<false>(BAR(kBarPartEmpty + qb), ((it >> 1) - 1) & 1,
-                                                        abort_flag, sb, kSitePartEmpty));
-                if (!ok)
-                    break;
-            }
 #pragma unroll
             for (int q = 0; q < C::VPL; ++q) {
                 const int o = C::VPL * kg + q;
@@ -449,139 +554,48 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const Param
                 if (vid >= 0 && i < ntok)
                     part_at(qb, half, tg * NT + i)[vid] = v[q];
             }
-            ptx::fence_proxy_async_smem();   // the exchange warp ships them with bulk copies
-            __syncwarp();
-            if (lane == 0)
-                ptx::mbar_arrive(BAR(kBarPartFull + qb));
-        }
-    } else if (warp >= kExchangeWarp) {
-        // -------------------------------------------------------------- exchange warps
-        // Lane 0 does every wait and the warp follows its (broadcast) decision.  The
-        // warps also load x: exchange warp 0 issues the fn_w slice and the first
-        // tiles, and whichever warp collapses tile i refills its stage with tile
-        // i + nst.  The persistent variant stages fn_w in stages 1-2 (TMEM takes
-        // it from there), so the first x tile can land in stage 0 meanwhile.
-        const int e = warp - kExchangeWarp;
-        const uint32_t hs_bytes = (uint32_t)p.hs * 4u;
-        auto load_tile = [&](int it) {   // whole warp; stage it % nst must be free
-            const int s = it % L.nst;
-            int t0, tm;
-            tile_tokens(it, t0, tm);
-            if (lane == 0)
-                ptx::mbar_arrive_expect_tx(BAR(kBarXFull + s), (uint32_t)(tm * S) * hs_bytes);
-            __syncwarp();
-            float *xs = stages + s * stage_floats;
-            for (int q = lane; q < tm * S; q += 32) {
-                const int t = q / S, k = q - (q / S) * S;
-                ptx::bulk_g2s(ptx::smem_u32(xs + t * p.LK + k * p.hs),
-                              p.x + ((size_t)(t0 + t) * S + k) * p.d + (size_t)rank * p.hs, hs_bytes,
-                              BAR(kBarXFull + s));
-            }
-            __syncwarp();
-            if (lane == 0)
-                issued[s] = issued[s] + 1;
-        };
-        bool ok = true;
-        if (e == 0) {
-            float *wdst = PERSIST ? stages + stage_floats : wsm;
-            if (lane == 0)
-                ptx::mbar_arrive_expect_tx(BAR(kBarWFull), (uint32_t)(G::R * S) * hs_bytes);
-            __syncwarp();
-            for (int q = lane; q < G::R * S; q += 32) {
-                const int r = q / S, k = q - (q / S) * S;
-                ptx::bulk_g2s(ptx::smem_u32(wdst + r * p.LK + k * p.hs),
-                              p.fn_w + (size_t)r * K + (size_t)k * p.d + (size_t)rank * p.hs, hs_bytes,
-                              BAR(kBarWFull));
-            }
-            load_tile(0);   // tile 0 always exists (every cluster gets at least one)
-            if (L.nst > 1 && cid + ncl < p.ntiles) {
-                ok = warp_wait<false>(lane, BAR(kBarWFree), 0, abort_flag, sb, kSiteWFree);
-                for (int it = 1; ok && it < L.nst && cid + it * ncl < p.ntiles; ++it)
-                    load_tile(it);
-            }
-        }
-        for (int it = e; ok && cid + it * ncl < p.ntiles; it += 2) {
-            const int qb = it & 1, s = it % L.nst;
-            if (!warp_wait<false>(lane, BAR(kBarPartFull + qb), (it >> 1) & 1, abort_flag, sb, kSitePartFull))
-                break;
-            int t0, tm;
-            tile_tokens(it, t0, tm);
+            ptx::fence_proxy_async_smem();   // the partials leave by bulk copies
+            if (threadIdx.x == 0)            // the owners will answer with tm pre gates
+                ptx::mbar_arrive_expect_tx(BAR(kBarPre + qb), (uint32_t)(tm * 16));
+            ptx::named_bar_sync(1, kComputeThreads);
             // Ship each token's two column-half partials to its owner CTA (token t of the
-            // tile belongs to CTA t) with bulk copies that complete on the owner's
-            // recv barrier.  Only a cluster's last tile can be partial, so no later
-            // tile's bytes can reach a CTA that owns nothing in this one.
-            if (lane < 2 * tm) {
+            // tile belongs to CTA t); the copies complete on the owner's recv barrier.
+            if (warp == 0 && lane < 2 * tm) {
                 const int h = lane / tm, t = lane - (lane / tm) * tm;
                 const uint32_t dst = ptx::smem_u32(recv + ((qb * 2 + h) * kCS + (int)rank) * G::RV);
                 ptx::bulk_s2cluster(ptx::mapa(dst, (uint32_t)t), ptx::smem_u32(part_at(qb, h, t)),
                                     (uint32_t)(G::RV * 4), ptx::mapa(BAR(kBarRecv + qb), (uint32_t)t));
             }
-            // The owners send back the tile's pre gates (16 bytes each).
-            if (lane == 0)
-                ptx::mbar_arrive_expect_tx(BAR(kBarPre + qb), (uint32_t)(tm * 16));
-            if (!warp_wait<true>(lane, BAR(kBarPre + qb), (it >> 1) & 1, abort_flag, sb, kSitePre)) {
-                // Giving up: still let any gates already on their way land before exit.
-                if (lane == 0)
-                    wait_bar<true>(BAR(kBarPre + qb), (it >> 1) & 1, abort_flag, sb, kSiteDrain, false);
-                __syncwarp();
+            if (it > 0 && !(ok = collapse(it - 1)))
                 break;
-            }
-            // Every owner has received this CTA's partials (it answered), so the
-            // partial buffer is free for tile it + 2.
-            if (lane == 0)
-                ptx::mbar_arrive(BAR(kBarPartEmpty + qb));
-            // Collapse this CTA's hidden slice of every token of the tile.
-            const uint32_t xs_base = ptx::smem_u32(stages + s * stage_floats);
-            const uint32_t pre_base = ptx::smem_u32(preb + qb * kTMT * 4);
-            const int h4n = p.hs / 4;
-            for (int t = 0; t < tm; ++t) {
-                const float4 pv = ptx::lds128(pre_base + 16u * (uint32_t)t);
-                const float pr[4] = {pv.x, pv.y, pv.z, pv.w};
-                const uint32_t xt = xs_base + 4u * (uint32_t)(t * p.LK);
-                float *yt = p.y + (size_t)(t0 + t) * p.d + (size_t)rank * p.hs;
-                for (int h4 = lane; h4 < h4n; h4 += 32) {
-                    float4 xv = ptx::lds128(xt + 16u * (uint32_t)h4);
-                    float4 acc4 = make_float4(pr[0] * xv.x, pr[0] * xv.y, pr[0] * xv.z, pr[0] * xv.w);
-#pragma unroll
-                    for (int k = 1; k < S; ++k) {
-                        xv = ptx::lds128(xt + 4u * (uint32_t)(k * p.hs) + 16u * (uint32_t)h4);
-                        acc4.x = fmaf(pr[k], xv.x, acc4.x);
-                        acc4.y = fmaf(pr[k], xv.y, acc4.y);
-                        acc4.z = fmaf(pr[k], xv.z, acc4.z);
-                        acc4.w = fmaf(pr[k], xv.w, acc4.w);
-                    }
-                    *reinterpret_cast<float4 *>(yt + 4 * h4) = acc4;
-                }
-            }
-            __syncwarp();
-            // The compute warps are done with this stage (its tile's partials are
-            // in) and so is the collapse: refill it.
-            if (cid + (it + L.nst) * ncl < p.ntiles)
-                load_tile(it + L.nst);
         }
-        // Every bulk copy this CTA issued lands before the CTA may exit: once both
-        // exchange warps are done issuing, wait for the last phase of each stage.
-        ptx::named_bar_sync(2, 64);
-        if (e == 0 && lane == 0) {
+        if (ok && it > 0)
+            collapse(it - 1);
+        // Every bulk load this CTA issued lands before the CTA may exit.
+        if (threadIdx.x == 0) {
             wait_bar<false>(BAR(kBarWFull), 0, abort_flag, sb, kSiteDrain, false);
             for (int s = 0; s < L.nst; ++s)
                 if (issued[s] > 0)
                     wait_bar<false>(BAR(kBarXFull + s), (issued[s] - 1) & 1, abort_flag, sb, kSiteDrain, false);
         }
-        __syncwarp();
     } else {
         // -------------------------------------------------------------- finisher warps
+        // Tile it's token t is owned by CTA t: its finisher (warp 8 + it % 2) sums the
+        // 2 x 16 partials, forms the gates, sends pre to every CTA and post to memory,
+        // and hands exp(comb logits) to the tile's Sinkhorn CTA (it % 16), whose
+        // finisher scales all of the tile's tokens at once, one token per lane.
+        // Only a cluster's last tile can be partial, so no later tile's bytes can
+        // reach a CTA that owns nothing in this one.
         const int f = warp - kFinisherWarp;
         const int grp = lane < S ? 0 : (lane < 2 * S ? 1 : 2);
         const float my_scale = lane < G::R ? p.scale[grp] : 0.f;
         const float my_base = lane < G::R ? p.base[lane] : 0.f;
-        float *pre_send = preb + 2 * kTMT * 4;   // [2][4]: this CTA's own token's pre gates
-        for (int it = f; cid + it * ncl < p.ntiles; it += 2) {
+        for (int it = f; tile_exists(it); it += 2) {
             const int qb = it & 1;
             int t0, tm;
             tile_tokens(it, t0, tm);
             const bool own = (int)rank < tm;
-            // Arm this tile's phase: an owner expects two column halves from 16 CTAs.
+            const uint32_t sc = (uint32_t)(it % kCS);
             if (lane == 0)
                 ptx::mbar_arrive_expect_tx(BAR(kBarRecv + qb), own ? (uint32_t)(2 * kCS * G::RV * 4) : 0u);
             if (!warp_wait<true>(lane, BAR(kBarRecv + qb), (it >> 1) & 1, abort_flag, sb, kSiteRecv)) {
@@ -591,55 +605,67 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const Param
                 __syncwarp();
                 break;
             }
-            if (!own)
-                continue;
-            float val = 0.f;
-            if (lane <= G::R) {
-                float src[2 * kCS];
-                const uint32_t a0 = ptx::smem_u32(recv + qb * 2 * kCS * G::RV + lane);
+            if (own) {
+                float val = 0.f;
+                if (lane <= G::R) {
+                    float src[2 * kCS];
+                    const uint32_t a0 = ptx::smem_u32(recv + qb * 2 * kCS * G::RV + lane);
 #pragma unroll
-                for (int c = 0; c < 2 * kCS; ++c)
-                    src[c] = ptx::lds32(a0 + 4u * (uint32_t)(c * G::RV));
-                val = tree_sum<2 * kCS>(src);   // halves and sources in a fixed pairwise order
+                    for (int c = 0; c < 2 * kCS; ++c)
+                        src[c] = ptx::lds32(a0 + 4u * (uint32_t)(c * G::RV));
+                    val = tree_sum<2 * kCS>(src);   // halves and sources in a fixed pairwise order
+                }
+                const float ss = __shfl_sync(kFull, val, G::R);
+                const float rinv = rsqrtf(ss / p.Kf + p.eps);
+                const float logit = lane < G::R ? val * rinv * my_scale + my_base : 0.f;
+                const float sg = 1.f / (1.f + expf(-logit));
+                const float pre_v = sg + p.eps;
+                // pre gates of this token -> every CTA of the cluster (16 bytes each);
+                // exp(comb logits) -> the Sinkhorn CTA (64 bytes).
+                float *es = esend + (it & 3) * 16;
+                if (lane < 4)
+                    pre_send[qb * 4 + lane] = lane < S ? pre_v : 0.f;
+                if (lane >= 2 * S && lane < 2 * S + 16)
+                    es[lane - 2 * S] = lane < G::R ? expf(logit) : 0.f;
+                ptx::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane < kCS) {
+                    const uint32_t dst = ptx::smem_u32(preb + (qb * kTMT + (int)rank) * 4);
+                    ptx::bulk_s2cluster(ptx::mapa(dst, (uint32_t)lane), ptx::smem_u32(pre_send + qb * 4), 16u,
+                                        ptx::mapa(BAR(kBarPre + qb), (uint32_t)lane));
+                } else if (lane == kCS) {
+                    const uint32_t dst = ptx::smem_u32(sinkbuf + (int)rank * 16);
+                    ptx::bulk_s2cluster(ptx::mapa(dst, sc), ptx::smem_u32(es), 64u, ptx::mapa(BAR(kBarSink), sc));
+                }
+                const size_t tok = (size_t)t0 + rank;
+                if (lane < S)
+                    p.pre[tok * S + lane] = pre_v;
+                else if (lane < 2 * S)
+                    p.post[tok * S + (lane - S)] = 2.f * sg;
             }
-            const float ss = __shfl_sync(kFull, val, G::R);
-            const float rinv = rsqrtf(ss / p.Kf + p.eps);
-            const float logit = lane < G::R ? val * rinv * my_scale + my_base : 0.f;
-            const float sg = 1.f / (1.f + expf(-logit));
-            const float pre_v = sg + p.eps;
-            // pre gates of this token -> every CTA of the cluster (16 bytes each).
-            if (lane < 4)
-                pre_send[qb * 4 + lane] = lane < S ? pre_v : 0.f;
-            ptx::fence_proxy_async_smem();
-            __syncwarp();
-            if (lane < kCS) {
-                const uint32_t dst = ptx::smem_u32(preb + (qb * kTMT + (int)rank) * 4);
-                ptx::bulk_s2cluster(ptx::mapa(dst, (uint32_t)lane), ptx::smem_u32(pre_send + qb * 4), 16u,
-                                    ptx::mapa(BAR(kBarPre + qb), (uint32_t)lane));
+            if (rank == sc) {
+                // This CTA scales the tile's comb blocks: lane t holds token t's S x S.
+                if (lane == 0)
+                    ptx::mbar_arrive_expect_tx(BAR(kBarSink), (uint32_t)(tm * 64));
+                if (!warp_wait<true>(lane, BAR(kBarSink), (it / kCS) & 1, abort_flag, sb, kSiteSink)) {
+                    if (lane == 0)
+                        wait_bar<true>(BAR(kBarSink), (it / kCS) & 1, abort_flag, sb, kSiteDrain, false);
+                    __syncwarp();
+                    break;
+                }
+                if (lane < tm) {
+                    float cm[S * S];
+                    const float *src = sinkbuf + lane * 16;
+#pragma unroll
+                    for (int q = 0; q < S * S; ++q)
+                        cm[q] = src[q];
+                    sinkhorn_regs<S>(cm, p.iters, p.eps);
+                    float *dst = p.comb + (size_t)(t0 + lane) * S * S;
+#pragma unroll
+                    for (int q = 0; q < S * S; ++q)
+                        dst[q] = cm[q];
+                }
             }
-            const size_t tok = (size_t)t0 + rank;
-            if (lane < S)
-                p.pre[tok * S + lane] = pre_v;
-            else if (lane < 2 * S)
-                p.post[tok * S + (lane - S)] = 2.f * sg;
-            // Sinkhorn with one matrix entry per lane: lane 4j+k holds comb[j][k]
-            // (entries outside the S x S block are 0); rows sum over xor 1, 2 and
-            // columns over xor 4, 8.
-            const int j = (lane >> 2) & 3, k = lane & 3;
-            const bool in = lane < 16 && j < S && k < S;
-            const float ev = (lane >= 2 * S && lane < G::R) ? expf(logit) : 0.f;
-            float c = __shfl_sync(kFull, ev, 2 * S + (in ? j * S + k : 0));
-            c = in ? c : 0.f;
-            for (int r = 0; r < p.iters; ++r) {
-                float rs = c + __shfl_xor_sync(kFull, c, 1);
-                rs += __shfl_xor_sync(kFull, rs, 2);
-                c *= __fdividef(1.0f, rs + p.eps);
-                float cs = c + __shfl_xor_sync(kFull, c, 4);
-                cs += __shfl_xor_sync(kFull, cs, 8);
-                c *= __fdividef(1.0f, cs + p.eps);
-            }
-            if (in)
-                p.comb[tok * S * S + j * S + k] = c;
             __syncwarp();
         }
     }
