@@ -11,30 +11,31 @@
 //    LK = s*hs column slice of each token's slab and the matching LK columns
 //    of all R rows of fn_w.  Because the slice covers all s streams of its
 //    hidden range, the collapse of that range needs nothing from other CTAs.
-//  * Each token tile (<= 16 tokens) is brought in by bulk copies (the TMA
-//    engine) into a shared-memory stage and stays there until its collapse, so
+//  * Each token tile (<= 16 tokens) arrives by one tiled TMA load (a 4-D tensor
+//    map whose box is the CTA's column slice of every stream of the tile's
+//    tokens) into a shared-memory stage and stays there until its collapse, so
 //    x is read from HBM exactly once.
-//  * The fn_w slice stays resident in the CTA for every tile it processes: in
-//    tensor memory (TMEM, tcgen05.ld into registers) for the persistent prefill
-//    variant, in shared memory for the one-tile decode variant.  It is read
-//    from L2/HBM once per CTA.
-//  * Eight compute warps do nothing but the contraction.  Warp w owns rows
+//  * The fn_w slice (one more TMA box) stays resident in the CTA for every tile
+//    it processes: in tensor memory (TMEM, tcgen05.ld into registers) for the
+//    persistent prefill variant, in shared memory for the one-tile decode
+//    variant.  It is read from L2/HBM once per CTA.
+//  * Eight compute warps run the contraction.  Warp w owns rows
 //    [B*(w%4), B*(w%4)+B) (B = 6 for s = 4) and half of the column groups
 //    (w/4); in a warp, lanes 0-15 take the tile's first token slots and lanes
 //    16-31 the rest, and lane&15 is the K-group owning float4 columns kg,
 //    kg+16, ...  Operands: x from shared memory, fn_w from TMEM; packed
 //    float32 FMAs on CUDA cores (no TF32: the 24-row contraction is too skinny
 //    for tensor cores and must stay in f32).  A 16-lane xor reduce-scatter
-//    sums the K-groups, and the partials go to a local shared-memory buffer.
-//  * Two exchange warps (even/odd tiles) add the two column halves, push each
-//    token's partial dots and sum of squares to its owner CTA (token t of a
-//    tile belongs to CTA t) through distributed shared memory, wait for the
-//    pre gates and write the tile's collapse.
-//  * Two finisher warps (even/odd tiles) of each owner sum the 16 CTA
+//    sums the K-groups into a local buffer, and one bulk copy per token sends
+//    both column halves of its partial dots and sum of squares to the token's
+//    owner CTA (token t of a tile belongs to CTA t) through distributed shared
+//    memory.  The same warps then collapse the previous tile once its pre
+//    gates have arrived, so they never wait for this tile's gates.
+//  * Two finisher warps (even/odd tiles) of each owner sum the 2 x 16
 //    partials in a fixed tree, apply the rsqrt rescale, form the gates,
-//    broadcast pre to all 16 CTAs, then run the Sinkhorn in registers.
-//  * So the compute warps never wait for the exchange: while they do tile i+1,
-//    tile i is pushed, finished and collapsed by the other warps.
+//    broadcast pre to all 16 CTAs and write pre/post; exp(comb logits) go to
+//    the tile's Sinkhorn CTA (tile index mod 16), whose finisher normalises all
+//    the tile's comb blocks at once, one token per lane, in registers.
 //  * Every wait on an mbarrier is bounded (2 s of %globaltimer); on timeout the
 //    kernel records the site in the workspace status word, stops issuing work,
 //    lets its bulk copies land, meets the other CTAs at the final cluster
@@ -43,6 +44,9 @@
 // Determinism: every sum has a fixed order independent of T, of the tile a
 // token lands in and of the variant, so a token's outputs are the same bits
 // whatever batch it is in.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include "hc_internal.cuh"
 #include "hc_ptx.cuh"
 
@@ -105,9 +109,9 @@ __host__ __device__ inline Lay make_lay(int LK)
     L.off_w = o;
     if (!PERSIST)
         o += G::RP * LK * 4;
-    L.off_recv = o;                  // [2 tile parities][2 column halves][16 source CTAs][RV]
+    L.off_recv = o;                  // [2 tile parities][16 source CTAs][2 column halves][RV]
     o += 2 * 2 * kCS * G::RV * 4;
-    L.off_part = o;                  // [2 tile parities][2 column halves][16 tokens][RV]
+    L.off_part = o;                  // [2 tile parities][16 tokens][2 column halves][RV]
     o += 2 * 2 * kTMT * G::RV * 4;
     L.off_pre = o;                   // [2 tile parities][16 tokens][4]: the tile's pre gates
     o += 2 * kTMT * 4 * 4;
@@ -126,10 +130,15 @@ __host__ __device__ inline Lay make_lay(int LK)
 }
 
 struct Params {
+    // Both maps see a [rows][s][d] tensor as 4-D (hc, d/hc, s, rows), hc = hs/hsc a
+    // divisor of hs of at most 256 floats, so a box of (hc, hsc, s, n) is one CTA's
+    // column slice of n rows and every box dimension stays within TMA's 256 limit.
+    CUtensorMap tmap_x;   // x: rows = tokens, box n = tm_tile
+    CUtensorMap tmap_w;   // fn_w: rows = R, box n = R
     const float *x, *fn_w, *scale, *base;
     float *pre, *post, *comb, *y;
     StatusBlock *status;
-    int T, d, hs, LK, NJ, iters, tm_tile, ntiles;
+    int T, d, hs, hsc, LK, NJ, iters, tm_tile, ntiles;
     float eps, Kf;
 };
 
@@ -291,7 +300,7 @@ __device__ __forceinline__ void dots_step(float2 (&acc)[NT][CG<S>::B], float2 (&
 }
 
 template <int S, bool PERSIST, int NT>
-__global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const Params p)
+__global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const __grid_constant__ Params p)
 {
     using G = CG<S>;
     using C = CT<S, NT>;
@@ -313,7 +322,6 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const Param
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L.off_misc + 4);
     volatile int *issued = reinterpret_cast<volatile int *>(smem + L.off_misc + 8);   // per stage
     StatusBlock *sb = p.status;
-    const int K = S * p.d;
     const int stage_floats = L.stage_bytes / 4;
     const int njh = (p.NJ + 1) / 2;   // column groups of the first half (the second gets the rest)
     auto BAR = [&](int i) { return bar0 + 8u * (uint32_t)i; };
@@ -322,26 +330,19 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const Param
         tm = min(p.tm_tile, p.T - t0);
     };
     auto tile_exists = [&](int it) { return cid + it * ncl < p.ntiles; };
-    auto part_at = [&](int q, int h, int t) { return part + ((q * 2 + h) * kTMT + t) * G::RV; };
+    auto part_at = [&](int q, int h, int t) { return part + ((q * kTMT + t) * 2 + h) * G::RV; };
     const uint32_t hs_bytes = (uint32_t)p.hs * 4u;
-    // Bulk-load tile `it` into its stage (whole warp; the stage must be free).
-    auto load_tile = [&](int it) {
+    // TMA-load tile `it` into its stage (one instruction; the stage must be free).
+    // A partial last tile still moves a whole box: rows past T arrive as zeros.
+    const uint32_t tile_box_bytes = (uint32_t)(p.tm_tile * S) * hs_bytes;
+    auto load_tile = [&](int it) {   // lane 0 of one warp
         const int s = it % L.nst;
         int t0, tm;
         tile_tokens(it, t0, tm);
-        if (lane == 0)
-            ptx::mbar_arrive_expect_tx(BAR(kBarXFull + s), (uint32_t)(tm * S) * hs_bytes);
-        __syncwarp();
-        float *xs = stages + s * stage_floats;
-        for (int q = lane; q < tm * S; q += 32) {
-            const int t = q / S, k = q - (q / S) * S;
-            ptx::bulk_g2s(ptx::smem_u32(xs + t * p.LK + k * p.hs),
-                          p.x + ((size_t)(t0 + t) * S + k) * p.d + (size_t)rank * p.hs, hs_bytes,
-                          BAR(kBarXFull + s));
-        }
-        __syncwarp();
-        if (lane == 0)
-            issued[s] = issued[s] + 1;
+        ptx::mbar_arrive_expect_tx(BAR(kBarXFull + s), tile_box_bytes);
+        ptx::tma_load_4d(ptx::smem_u32(stages + s * stage_floats), &p.tmap_x, 0, (int)rank * p.hsc, 0,
+                         t0, BAR(kBarXFull + s));
+        issued[s] = issued[s] + 1;
     };
 
     // ------------------------------------------------------------------ set-up
@@ -387,19 +388,15 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const Param
         // TMEM: warp w reads lanes 32*(w%4).. of its sub-partition; the two warps of
         // a sub-partition (the two column halves) use disjoint column ranges.
         const uint32_t trow = tmem_base + ((uint32_t)(32 * rg) << 16) + (uint32_t)(half * njh * G::WQ);
-        if (warp == 0) {
+        if (threadIdx.x == 0) {
             // fn_w slice (the persistent variant stages it in stages 1-2, so tile 0
             // can land in stage 0 meanwhile), then the first tile.
+            ptx::prefetch_tmap(&p.tmap_x);
+            ptx::prefetch_tmap(&p.tmap_w);
             float *wdst = PERSIST ? stages + stage_floats : wsm;
-            if (lane == 0)
-                ptx::mbar_arrive_expect_tx(BAR(kBarWFull), (uint32_t)(G::R * S) * hs_bytes);
-            __syncwarp();
-            for (int q = lane; q < G::R * S; q += 32) {
-                const int r = q / S, k = q - (q / S) * S;
-                ptx::bulk_g2s(ptx::smem_u32(wdst + r * p.LK + k * p.hs),
-                              p.fn_w + (size_t)r * K + (size_t)k * p.d + (size_t)rank * p.hs, hs_bytes,
-                              BAR(kBarWFull));
-            }
+            ptx::mbar_arrive_expect_tx(BAR(kBarWFull), (uint32_t)(G::R * S) * hs_bytes);
+            ptx::tma_load_4d(ptx::smem_u32(wdst), &p.tmap_w, 0, (int)rank * p.hsc, 0, 0,
+                             BAR(kBarWFull));
             load_tile(0);   // every cluster has at least one tile
         }
         bool ok = ptx::named_bar_and(1, kComputeThreads,
@@ -422,7 +419,7 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const Param
             ptx::tmem_wait_st();
             ptx::named_bar_sync(1, kComputeThreads);
             // Stages 1 and 2 are free now.
-            if (warp == 0)
+            if (threadIdx.x == 0)
                 for (int it = 1; it < L.nst && tile_exists(it); ++it)
                     load_tile(it);
         }
@@ -460,7 +457,7 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const Param
                 *reinterpret_cast<float4 *>(p.y + (size_t)(t0 + t) * p.d + (size_t)rank * p.hs + 4 * h4) = a;
             }
             ptx::named_bar_sync(1, kComputeThreads);
-            if (warp == 0 && tile_exists(itc + L.nst))
+            if (threadIdx.x == 0 && tile_exists(itc + L.nst))
                 load_tile(itc + L.nst);
             return true;
         };
@@ -560,11 +557,11 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const Param
             ptx::named_bar_sync(1, kComputeThreads);
             // Ship each token's two column-half partials to its owner CTA (token t of the
             // tile belongs to CTA t); the copies complete on the owner's recv barrier.
-            if (warp == 0 && lane < 2 * tm) {
-                const int h = lane / tm, t = lane - (lane / tm) * tm;
-                const uint32_t dst = ptx::smem_u32(recv + ((qb * 2 + h) * kCS + (int)rank) * G::RV);
-                ptx::bulk_s2cluster(ptx::mapa(dst, (uint32_t)t), ptx::smem_u32(part_at(qb, h, t)),
-                                    (uint32_t)(G::RV * 4), ptx::mapa(BAR(kBarRecv + qb), (uint32_t)t));
+            if (warp == 0 && lane < tm) {
+                const int t = lane;
+                const uint32_t dst = ptx::smem_u32(recv + (qb * kCS + (int)rank) * 2 * G::RV);
+                ptx::bulk_s2cluster(ptx::mapa(dst, (uint32_t)t), ptx::smem_u32(part_at(qb, 0, t)),
+                                    (uint32_t)(2 * G::RV * 4), ptx::mapa(BAR(kBarRecv + qb), (uint32_t)t));
             }
             if (it > 0 && !(ok = collapse(it - 1)))
                 break;
@@ -757,12 +754,56 @@ bool supported_s(int device)
            max_clusters_for<S, false, 8>(device) > 0;
 }
 
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no libcuda link).
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
+{
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+        else
+            cudaGetLastError();
+    });
+    return fn;
+}
+
+// Chunks per slice row: the fewest hsc with hs/hsc <= 256 floats, a multiple of 4.
+int slice_chunks(int hs)
+{
+    for (int n = (hs + 255) / 256; n <= hs / 4; ++n)
+        if (hs % n == 0 && (hs / n) % 4 == 0)
+            return n;
+    return 0;
+}
+
+// Map a row-major [rows][s][d] float tensor as (hc, d/hc, s, rows), hc = hs/hsc, with
+// a box of (hc, hsc, s, box_rows); reads past the last row are zero-filled.
+bool encode_slab_map(CUtensorMap *m, const float *base, int rows, int s, int d, int hs, int hsc, int box_rows)
+{
+    PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+    if (!enc || hsc < 1)
+        return false;
+    const int hc = hs / hsc;
+    const cuuint64_t dims[4] = {(cuuint64_t)hc, (cuuint64_t)(d / hc), (cuuint64_t)s, (cuuint64_t)rows};
+    const cuuint64_t strides[3] = {(cuuint64_t)hc * 4, (cuuint64_t)d * 4, (cuuint64_t)s * d * 4};   // bytes
+    const cuuint32_t box[4] = {(cuuint32_t)hc, (cuuint32_t)hsc, (cuuint32_t)s, (cuuint32_t)box_rows};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<float *>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int S>
 cudaError_t run_s(const float *x, const float *fn_w, const float *scale, const float *base, int T,
                   int d, int iters, float eps, float *pre, float *post, float *comb, float *y,
                   void *workspace, cudaStream_t st, int device)
 {
-    Params p;
+    Params p = {};
     p.x = x;
     p.fn_w = fn_w;
     p.scale = scale;
@@ -775,6 +816,7 @@ cudaError_t run_s(const float *x, const float *fn_w, const float *scale, const f
     p.T = T;
     p.d = d;
     p.hs = d / kCS;
+    p.hsc = slice_chunks(p.hs);
     p.LK = S * p.hs;
     p.NJ = p.LK / 64;
     p.iters = iters;
@@ -785,11 +827,16 @@ cudaError_t run_s(const float *x, const float *fn_w, const float *scale, const f
     const int nc_persist = max_clusters_for<S, true, 8>(device);
     if (nc_decode < 1 || nc_persist < 1)
         return cudaErrorNotSupported;
-    if (T <= nc_decode * kTMT) {
-        // One tile per cluster, tokens spread over as many clusters as can run at once;
-        // the token-slot count is the smallest that holds a tile.
-        p.tm_tile = (T + nc_decode - 1) / nc_decode;
-        p.ntiles = (T + p.tm_tile - 1) / p.tm_tile;
+    const bool decode = T <= nc_decode * kTMT;
+    // Decode: one tile per cluster, tokens spread over as many clusters as can run
+    // at once; prefill: 16-token tiles on persistent clusters.
+    p.tm_tile = decode ? (T + nc_decode - 1) / nc_decode : kTMT;
+    p.ntiles = (T + p.tm_tile - 1) / p.tm_tile;
+    if (!encode_slab_map(&p.tmap_x, x, T, S, d, p.hs, p.hsc, p.tm_tile) ||
+        !encode_slab_map(&p.tmap_w, fn_w, CG<S>::R, S, d, p.hs, p.hsc, CG<S>::R))
+        return cudaErrorInvalidValue;
+    if (decode) {
+        // The token-slot count is the smallest that holds a tile.
         if (p.tm_tile <= 2)
             return launch_variant<S, false, 1>(p, p.ntiles, st);
         if (p.tm_tile <= 4)
@@ -798,8 +845,6 @@ cudaError_t run_s(const float *x, const float *fn_w, const float *scale, const f
             return launch_variant<S, false, 4>(p, p.ntiles, st);
         return launch_variant<S, false, 8>(p, p.ntiles, st);
     }
-    p.tm_tile = kTMT;
-    p.ntiles = (T + kTMT - 1) / kTMT;
     return launch_variant<S, true, 8>(p, min(p.ntiles, nc_persist), st);
 }
 
@@ -810,7 +855,7 @@ bool cluster_shape_ok(int s, int d)
     if (s < 1 || s > 4 || d % (kCS * 4) != 0)
         return false;
     const int LK = s * (d / kCS);
-    return LK % 64 == 0 && LK <= kMaxLK;
+    return LK % 64 == 0 && LK <= kMaxLK && slice_chunks(d / kCS) > 0;
 }
 
 bool cluster_supported(int s, int d)

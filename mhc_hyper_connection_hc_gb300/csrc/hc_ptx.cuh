@@ -116,6 +116,22 @@ __device__ __forceinline__ float lds32(uint32_t addr)
     return v;
 }
 
+// 4-D tiled TMA load: the box of the tensor map `tmap` (a __grid_constant__
+// kernel parameter) at coordinates (c0, c1, c2, c3), innermost first, into this
+// CTA's shared memory at `dst`; completion counted in bytes on `bar`.
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const void *tmap, int c0, int c1, int c2, int c3,
+                                            uint32_t bar)
+{
+    asm volatile("cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+                 " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
+                 "l"(tmap), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
+                 : "memory");
+}
+__device__ __forceinline__ void prefetch_tmap(const void *tmap)
+{
+    asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
+}
+
 // shared memory of this CTA -> shared memory of a CTA of the cluster (dst and its
 // mbarrier given as shared::cluster addresses from mapa); completion counted in
 // bytes on the destination's mbarrier.  16-byte aligned, bytes a multiple of 16.
