@@ -26,19 +26,20 @@
 //    kg+16, ...  Operands: x from shared memory, fn_w from TMEM; packed
 //    float32 FMAs on CUDA cores (no TF32: the 24-row contraction is too skinny
 //    for tensor cores and must stay in f32).  A 16-lane xor reduce-scatter
-//    sums the K-groups into a local buffer, and one bulk copy per token sends
-//    both column halves of its partial dots and sum of squares to the token's
-//    owner CTA (token t of a tile belongs to CTA t) through distributed shared
-//    memory.  The same warps then collapse the previous tile once its pre
+//    sums the K-groups, and each lane stores its partial dots and sums of
+//    squares straight into the owner CTA's receive buffer (token t of a tile
+//    belongs to CTA t) with st.async, which counts the bytes on the owner's
+//    mbarrier.  The same warps then collapse the previous tile once its pre
 //    gates have arrived, so they never wait for this tile's gates.
 //  * Two finisher warps (even/odd tiles) of each owner sum the 2 x 16
 //    partials in a fixed tree, apply the rsqrt rescale, form the gates,
 //    broadcast pre to all 16 CTAs and write pre/post; exp(comb logits) go to
-//    the tile's Sinkhorn CTA (tile index mod 16), whose finisher normalises all
-//    the tile's comb blocks at once, one token per lane, in registers.
+//    the tile's Sinkhorn CTA (tile index mod 16), whose Sinkhorn warp
+//    normalises all the tile's comb blocks at once, one token per lane, in
+//    registers, off the path that the next tiles' gates take.
 //  * Every wait on an mbarrier is bounded (2 s of %globaltimer); on timeout the
 //    kernel records the site in the workspace status word, stops issuing work,
-//    lets its bulk copies land, meets the other CTAs at the final cluster
+//    lets its TMA loads land, meets the other CTAs at the final cluster
 //    barrier, frees TMEM and returns.
 //
 // Determinism: every sum has a fixed order independent of T, of the tile a
@@ -60,7 +61,9 @@ constexpr int kTMT = 16;             // max tokens per tile = one owner CTA per 
 constexpr int kRG = 4;               // row groups (compute warps w and w+4 share one)
 constexpr int kNCW = 8;              // compute warps: two per SM sub-partition
 constexpr int kFinisherWarp = 8;     // warps 8 and 9 take even and odd tiles
-constexpr int kThreads = 10 * 32;    // at most three warps per sub-partition: 168 registers each
+constexpr int kSinkWarp = 10;        // the Sinkhorn of the tiles this CTA normalises
+constexpr int kThreads = 11 * 32;    // at most three warps per sub-partition: 168 registers each
+constexpr int kSinkLag = 8;          // a finisher waits for the Sinkhorn of the tile 8 before its own
 constexpr int kComputeThreads = kNCW * 32;
 constexpr int kNstPersist = 3;
 constexpr int kMaxLK = 1024;         // s*d/16 <= 1024: three 64 KiB stages fit in shared memory
@@ -69,9 +72,9 @@ constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 constexpr unsigned kFull = 0xffffffffu;
 
 // mbarrier slots
-constexpr int kBarXFull = 0, kBarRecv = 3, kBarPre = 5, kBarSink = 7, kBarWFull = 8, kBarWFree = 9,
+constexpr int kBarXFull = 0, kBarRecv = 3, kBarPre = 5, kBarSink = 7, kBarWFull = 8, kBarSinkDone = 9,
               kNumBars = 10;
-enum WaitSite : unsigned { kSiteWFull = 1, kSiteXFull, kSiteRecv, kSitePre, kSiteSink, kSiteDrain };
+enum WaitSite : unsigned { kSiteWFull = 1, kSiteXFull, kSiteRecv, kSitePre, kSiteSink, kSiteDrain, kSiteSinkDone };
 
 template <int S>
 struct CG {
@@ -94,8 +97,7 @@ struct CT {
 };
 
 struct Lay {   // shared-memory layout in bytes
-    int stage_bytes, nst, off_w, off_recv, off_part, off_pre, off_pre_send, off_esend, off_sink, off_bar,
-        off_misc, total;
+    int stage_bytes, nst, off_w, off_recv, off_pre, off_sink, off_bar, off_misc, total;
 };
 
 template <int S, bool PERSIST>
@@ -111,14 +113,8 @@ __host__ __device__ inline Lay make_lay(int LK)
         o += G::RP * LK * 4;
     L.off_recv = o;                  // [2 tile parities][16 source CTAs][2 column halves][RV]
     o += 2 * 2 * kCS * G::RV * 4;
-    L.off_part = o;                  // [2 tile parities][16 tokens][2 column halves][RV]
-    o += 2 * 2 * kTMT * G::RV * 4;
     L.off_pre = o;                   // [2 tile parities][16 tokens][4]: the tile's pre gates
     o += 2 * kTMT * 4 * 4;
-    L.off_pre_send = o;              // [2][4]: this CTA's own token's pre gates
-    o += 2 * 4 * 4;
-    L.off_esend = o;                 // [4][16]: its exp(comb logits)
-    o += 4 * 16 * 4;
     L.off_sink = o;                  // [16 tokens][16]: the comb blocks this CTA scales
     o += kTMT * 16 * 4;
     L.off_bar = o;
@@ -139,7 +135,7 @@ struct Params {
     float *pre, *post, *comb, *y;
     StatusBlock *status;
     int T, d, hs, hsc, LK, NJ, iters, tm_tile, ntiles;
-    float eps, Kf;
+    float eps, invK;   // invK = 1 / (s*d)
 };
 
 // Bounded wait on an mbarrier phase.  honor_abort = false is used only to let
@@ -312,10 +308,7 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const __gri
     float *stages = reinterpret_cast<float *>(smem);
     float *wsm = reinterpret_cast<float *>(smem + L.off_w);
     float *recv = reinterpret_cast<float *>(smem + L.off_recv);
-    float *part = reinterpret_cast<float *>(smem + L.off_part);
     float *preb = reinterpret_cast<float *>(smem + L.off_pre);
-    float *pre_send = reinterpret_cast<float *>(smem + L.off_pre_send);
-    float *esend = reinterpret_cast<float *>(smem + L.off_esend);
     float *sinkbuf = reinterpret_cast<float *>(smem + L.off_sink);
     const uint32_t bar0 = ptx::smem_u32(smem + L.off_bar);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L.off_misc);
@@ -330,7 +323,6 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const __gri
         tm = min(p.tm_tile, p.T - t0);
     };
     auto tile_exists = [&](int it) { return cid + it * ncl < p.ntiles; };
-    auto part_at = [&](int q, int h, int t) { return part + ((q * kTMT + t) * 2 + h) * G::RV; };
     const uint32_t hs_bytes = (uint32_t)p.hs * 4u;
     // TMA-load tile `it` into its stage (one instruction; the stage must be free).
     // A partial last tile still moves a whole box: rows past T arrive as zeros.
@@ -352,12 +344,12 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const __gri
             issued[s] = 0;
         }
         for (int q = 0; q < 2; ++q) {
-            ptx::mbar_init(BAR(kBarRecv + q), 1);   // armed by this CTA; data by bulk copies
+            ptx::mbar_init(BAR(kBarRecv + q), 1);   // armed by this CTA; data by remote stores
             ptx::mbar_init(BAR(kBarPre + q), 1);
         }
         ptx::mbar_init(BAR(kBarSink), 1);
         ptx::mbar_init(BAR(kBarWFull), 1);
-        ptx::mbar_init(BAR(kBarWFree), 1);
+        ptx::mbar_init(BAR(kBarSinkDone), 1);
         *abort_flag = 0;
         ptx::fence_mbar_init_cluster();
     }
@@ -379,9 +371,9 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const __gri
 
     if (warp < kNCW) {
         // -------------------------------------------------------------- compute warps
-        // Every thread polls each barrier itself (its own acquire); a named
-        // barrier with an AND reduction then makes the go / give-up decision
-        // identical in all eight warps, so they always meet the same barriers.
+        // One thread polls each barrier; a named barrier with an AND reduction then
+        // hands its answer (and, by the barrier's ordering, what it acquired) to all
+        // eight warps, so they always meet the same barriers.
         const int tg = lane >> 4, kg = lane & 15;
         const int rg = warp & (kRG - 1), half = warp / kRG;
         const int j0 = half * njh, nj = half ? p.NJ - njh : njh;
@@ -399,8 +391,8 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const __gri
                              BAR(kBarWFull));
             load_tile(0);   // every cluster has at least one tile
         }
-        bool ok = ptx::named_bar_and(1, kComputeThreads,
-                                     wait_bar<false>(BAR(kBarWFull), 0, abort_flag, sb, kSiteWFull));
+        bool ok = ptx::named_bar_and(
+            1, kComputeThreads, threadIdx.x != 0 || wait_bar<false>(BAR(kBarWFull), 0, abort_flag, sb, kSiteWFull));
         if (PERSIST && ok) {
             // This thread's fixed fn_w values -> its TMEM lane, column jj*WQ + 4r + e.
             const float *wstage = stages + stage_floats;
@@ -428,7 +420,8 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const __gri
         // stage with tile itc + nst.
         auto collapse = [&](int itc) -> bool {
             const int q = itc & 1;
-            const bool got = wait_bar<true>(BAR(kBarPre + q), (itc >> 1) & 1, abort_flag, sb, kSitePre);
+            const bool got =
+                threadIdx.x != 0 || wait_bar<true>(BAR(kBarPre + q), (itc >> 1) & 1, abort_flag, sb, kSitePre);
             if (!ptx::named_bar_and(1, kComputeThreads, got))
                 return false;
             int t0, tm;
@@ -469,7 +462,8 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const __gri
                 break;
             const int s = it % L.nst, u = it / L.nst;
             ok = ptx::named_bar_and(1, kComputeThreads,
-                                    wait_bar<false>(BAR(kBarXFull + s), u & 1, abort_flag, sb, kSiteXFull));
+                                    threadIdx.x != 0 ||
+                                        wait_bar<false>(BAR(kBarXFull + s), u & 1, abort_flag, sb, kSiteXFull));
             if (!ok)
                 break;
             int t0, tm;
@@ -519,7 +513,7 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const __gri
                 }
             }
 
-            // Half-warp sums over the 16 K-groups, into the local partial buffer.
+            // Half-warp sums over the 16 K-groups.
             float v[C::NVP];
 #pragma unroll
             for (int i = 0; i < NT; ++i)
@@ -533,9 +527,13 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const __gri
             for (int q = C::NV; q < C::NVP; ++q)
                 v[q] = 0.f;
             reduce_scatter16<C::NVP>(v, kg);
-            // (this buffer's previous tile, it - 2, left with the copies that the owners
-            // answered before collapse(it - 2) went ahead)
+            // Each value goes straight to its token's owner CTA (token t of the tile belongs
+            // to CTA t), into recv[tile parity][this CTA][column half][row], by an
+            // asynchronous remote store that completes on the owner's recv barrier.  (The
+            // owner consumed that slot's previous tile, it - 2, before it sent the gates
+            // that collapse(it - 2) needed.)
             const int qb = it & 1;
+            const uint32_t recv_slot = ptx::smem_u32(recv + ((qb * kCS + (int)rank) * 2 + half) * G::RV);
 #pragma unroll
             for (int q = 0; q < C::VPL; ++q) {
                 const int o = C::VPL * kg + q;
@@ -548,21 +546,14 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const __gri
                     i = rg + kRG * (o - NT * G::B);
                     vid = G::R;
                 }
-                if (vid >= 0 && i < ntok)
-                    part_at(qb, half, tg * NT + i)[vid] = v[q];
+                if (vid >= 0 && i < ntok) {
+                    const uint32_t t = (uint32_t)(tg * NT + i);
+                    ptx::st_async_f32(ptx::mapa(recv_slot + 4u * (uint32_t)vid, t), v[q],
+                                      ptx::mapa(BAR(kBarRecv + qb), t));
+                }
             }
-            ptx::fence_proxy_async_smem();   // the partials leave by bulk copies
-            if (threadIdx.x == 0)            // the owners will answer with tm pre gates
+            if (threadIdx.x == 0)   // the owners will answer with tm pre gates
                 ptx::mbar_arrive_expect_tx(BAR(kBarPre + qb), (uint32_t)(tm * 16));
-            ptx::named_bar_sync(1, kComputeThreads);
-            // Ship each token's two column-half partials to its owner CTA (token t of the
-            // tile belongs to CTA t); the copies complete on the owner's recv barrier.
-            if (warp == 0 && lane < tm) {
-                const int t = lane;
-                const uint32_t dst = ptx::smem_u32(recv + (qb * kCS + (int)rank) * 2 * G::RV);
-                ptx::bulk_s2cluster(ptx::mapa(dst, (uint32_t)t), ptx::smem_u32(part_at(qb, 0, t)),
-                                    (uint32_t)(2 * G::RV * 4), ptx::mapa(BAR(kBarRecv + qb), (uint32_t)t));
-            }
             if (it > 0 && !(ok = collapse(it - 1)))
                 break;
         }
@@ -575,14 +566,20 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const __gri
                 if (issued[s] > 0)
                     wait_bar<false>(BAR(kBarXFull + s), (issued[s] - 1) & 1, abort_flag, sb, kSiteDrain, false);
         }
-    } else {
+    } else if (warp < kSinkWarp) {
         // -------------------------------------------------------------- finisher warps
         // Tile it's token t is owned by CTA t: its finisher (warp 8 + it % 2) sums the
         // 2 x 16 partials, forms the gates, sends pre to every CTA and post to memory,
         // and hands exp(comb logits) to the tile's Sinkhorn CTA (it % 16), whose
-        // finisher scales all of the tile's tokens at once, one token per lane.
+        // Sinkhorn warp scales all of the tile's tokens at once, one token per lane.
         // Only a cluster's last tile can be partial, so no later tile's bytes can
         // reach a CTA that owns nothing in this one.
+        //
+        // A CTA's Sinkhorn buffer is reused 16 tiles later.  Before this finisher sends
+        // the gates of tile it, it waits until its CTA's Sinkhorn warp is done with tile
+        // it - 8 if that tile was this CTA's: tile it - 8 + 16's exp values can only
+        // come once every CTA has collapsed tile it + 6, which needs gates this finisher
+        // sends after those of tile it.
         const int f = warp - kFinisherWarp;
         const int grp = lane < S ? 0 : (lane < 2 * S ? 1 : 2);
         const float my_scale = lane < G::R ? p.scale[grp] : 0.f;
@@ -593,8 +590,12 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const __gri
             tile_tokens(it, t0, tm);
             const bool own = (int)rank < tm;
             const uint32_t sc = (uint32_t)(it % kCS);
+            const int itl = it - kSinkLag;
+            if (itl >= 0 && itl % kCS == (int)rank &&
+                !warp_wait<false>(lane, BAR(kBarSinkDone), (itl / kCS) & 1, abort_flag, sb, kSiteSinkDone))
+                break;
             if (lane == 0)
-                ptx::mbar_arrive_expect_tx(BAR(kBarRecv + qb), own ? (uint32_t)(2 * kCS * G::RV * 4) : 0u);
+                ptx::mbar_arrive_expect_tx(BAR(kBarRecv + qb), own ? (uint32_t)(2 * kCS * (G::R + 1) * 4) : 0u);
             if (!warp_wait<true>(lane, BAR(kBarRecv + qb), (it >> 1) & 1, abort_flag, sb, kSiteRecv)) {
                 // Giving up: still let any partials already on their way land before exit.
                 if (lane == 0)
@@ -610,29 +611,27 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const __gri
 #pragma unroll
                     for (int c = 0; c < 2 * kCS; ++c)
                         src[c] = ptx::lds32(a0 + 4u * (uint32_t)(c * G::RV));
-                    val = tree_sum<2 * kCS>(src);   // halves and sources in a fixed pairwise order
+                    val = tree_sum<2 * kCS>(src);   // sources and halves in a fixed pairwise order
                 }
                 const float ss = __shfl_sync(kFull, val, G::R);
-                const float rinv = rsqrtf(ss / p.Kf + p.eps);
+                const float rinv = rsqrtf(ss * p.invK + p.eps);
                 const float logit = lane < G::R ? val * rinv * my_scale + my_base : 0.f;
-                const float sg = 1.f / (1.f + expf(-logit));
+                const float sg = __frcp_rn(1.f + expf(-logit));
                 const float pre_v = sg + p.eps;
                 // pre gates of this token -> every CTA of the cluster (16 bytes each);
-                // exp(comb logits) -> the Sinkhorn CTA (64 bytes).
-                float *es = esend + (it & 3) * 16;
-                if (lane < 4)
-                    pre_send[qb * 4 + lane] = lane < S ? pre_v : 0.f;
-                if (lane >= 2 * S && lane < 2 * S + 16)
-                    es[lane - 2 * S] = lane < G::R ? expf(logit) : 0.f;
-                ptx::fence_proxy_async_smem();
-                __syncwarp();
+                // exp(comb logits) -> the Sinkhorn CTA, one value per lane.
+                float4 pv;
+                pv.x = __shfl_sync(kFull, pre_v, 0);
+                pv.y = __shfl_sync(kFull, pre_v, 1 % S);
+                pv.z = __shfl_sync(kFull, pre_v, 2 % S);
+                pv.w = __shfl_sync(kFull, pre_v, 3 % S);
                 if (lane < kCS) {
                     const uint32_t dst = ptx::smem_u32(preb + (qb * kTMT + (int)rank) * 4);
-                    ptx::bulk_s2cluster(ptx::mapa(dst, (uint32_t)lane), ptx::smem_u32(pre_send + qb * 4), 16u,
-                                        ptx::mapa(BAR(kBarPre + qb), (uint32_t)lane));
-                } else if (lane == kCS) {
-                    const uint32_t dst = ptx::smem_u32(sinkbuf + (int)rank * 16);
-                    ptx::bulk_s2cluster(ptx::mapa(dst, sc), ptx::smem_u32(es), 64u, ptx::mapa(BAR(kBarSink), sc));
+                    ptx::st_async_v4(ptx::mapa(dst, (uint32_t)lane), pv, ptx::mapa(BAR(kBarPre + qb), (uint32_t)lane));
+                }
+                if (lane >= 2 * S && lane < G::R) {
+                    const uint32_t dst = ptx::smem_u32(sinkbuf + (int)rank * 16 + (lane - 2 * S));
+                    ptx::st_async_f32(ptx::mapa(dst, sc), expf(logit), ptx::mapa(BAR(kBarSink), sc));
                 }
                 const size_t tok = (size_t)t0 + rank;
                 if (lane < S)
@@ -640,30 +639,38 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const __gri
                 else if (lane < 2 * S)
                     p.post[tok * S + (lane - S)] = 2.f * sg;
             }
-            if (rank == sc) {
-                // This CTA scales the tile's comb blocks: lane t holds token t's S x S.
+            __syncwarp();
+        }
+    } else {
+        // -------------------------------------------------------------- Sinkhorn warp
+        // Tiles rank, rank + 16, ... are this CTA's to normalise: lane t takes token
+        // t's S x S block of exp(comb logits) and runs the Sinkhorn in registers.
+        for (int it = (int)rank; tile_exists(it); it += kCS) {
+            int t0, tm;
+            tile_tokens(it, t0, tm);
+            if (lane == 0)
+                ptx::mbar_arrive_expect_tx(BAR(kBarSink), (uint32_t)(tm * S * S * 4));
+            if (!warp_wait<true>(lane, BAR(kBarSink), (it / kCS) & 1, abort_flag, sb, kSiteSink)) {
                 if (lane == 0)
-                    ptx::mbar_arrive_expect_tx(BAR(kBarSink), (uint32_t)(tm * 64));
-                if (!warp_wait<true>(lane, BAR(kBarSink), (it / kCS) & 1, abort_flag, sb, kSiteSink)) {
-                    if (lane == 0)
-                        wait_bar<true>(BAR(kBarSink), (it / kCS) & 1, abort_flag, sb, kSiteDrain, false);
-                    __syncwarp();
-                    break;
-                }
-                if (lane < tm) {
-                    float cm[S * S];
-                    const float *src = sinkbuf + lane * 16;
+                    wait_bar<true>(BAR(kBarSink), (it / kCS) & 1, abort_flag, sb, kSiteDrain, false);
+                __syncwarp();
+                break;
+            }
+            if (lane < tm) {
+                float cm[S * S];
+                const float *src = sinkbuf + lane * 16;
 #pragma unroll
-                    for (int q = 0; q < S * S; ++q)
-                        cm[q] = src[q];
-                    sinkhorn_regs<S>(cm, p.iters, p.eps);
-                    float *dst = p.comb + (size_t)(t0 + lane) * S * S;
+                for (int q = 0; q < S * S; ++q)
+                    cm[q] = src[q];
+                sinkhorn_regs<S>(cm, p.iters, p.eps);
+                float *dst = p.comb + (size_t)(t0 + lane) * S * S;
 #pragma unroll
-                    for (int q = 0; q < S * S; ++q)
-                        dst[q] = cm[q];
-                }
+                for (int q = 0; q < S * S; ++q)
+                    dst[q] = cm[q];
             }
             __syncwarp();
+            if (lane == 0)
+                ptx::mbar_arrive(BAR(kBarSinkDone));   // the buffer may be refilled
         }
     }
 
@@ -821,7 +828,7 @@ cudaError_t run_s(const float *x, const float *fn_w, const float *scale, const f
     p.NJ = p.LK / 64;
     p.iters = iters;
     p.eps = eps;
-    p.Kf = (float)(S * d);
+    p.invK = 1.0f / (float)(S * d);
     // Every decode instantiation has the same footprint; NT = 8 bounds the others.
     const int nc_decode = max_clusters_for<S, false, 8>(device);
     const int nc_persist = max_clusters_for<S, true, 8>(device);

@@ -132,6 +132,23 @@ __device__ __forceinline__ void prefetch_tmap(const void *tmap)
     asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
 }
 
+// Asynchronous remote stores into the shared memory of a CTA of the cluster
+// (addresses from mapa): the bytes count as completed transactions on the
+// destination CTA's mbarrier `remote_bar`, which releases them at cluster scope.
+__device__ __forceinline__ void st_async_f32(uint32_t remote_addr, float v, uint32_t remote_bar)
+{
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.f32 [%0], %1, [%2];" ::"r"(remote_addr),
+                 "f"(v), "r"(remote_bar)
+                 : "memory");
+}
+__device__ __forceinline__ void st_async_v4(uint32_t remote_addr, float4 v, uint32_t remote_bar)
+{
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+                     remote_addr),
+                 "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(remote_bar)
+                 : "memory");
+}
+
 // shared memory of this CTA -> shared memory of a CTA of the cluster (dst and its
 // mbarrier given as shared::cluster addresses from mapa); completion counted in
 // bytes on the destination's mbarrier.  16-byte aligned, bytes a multiple of 16.
