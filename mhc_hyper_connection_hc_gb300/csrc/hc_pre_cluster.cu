@@ -29,8 +29,14 @@
 //    sums the K-groups, and each lane stores its partial dots and sums of
 //    squares straight into the owner CTA's receive buffer (token t of a tile
 //    belongs to CTA t) with st.async, which counts the bytes on the owner's
-//    mbarrier.  The same warps then collapse the previous tile once its pre
-//    gates have arrived, so they never wait for this tile's gates.
+//    mbarrier.  Then they go on to the next tile: they never wait for gates.
+//  * Persistent variant: four collapse warps (one per SM sub-partition) wait
+//    for each tile's pre gates, write y for the CTA's hidden columns from the
+//    tile's stage and refill the stage, so the stage ring alone couples them
+//    to the compute warps.  The decode variant's single tile is collapsed by
+//    the compute warps.  The sixteen warps launch at 128 registers; the two
+//    compute warpgroups raise theirs to 184 with setmaxnreg while the other
+//    two drop to 72.
 //  * Two finisher warps (even/odd tiles) of each owner sum the 2 x 16
 //    partials in a fixed tree, apply the rsqrt rescale, form the gates,
 //    broadcast pre to all 16 CTAs and write pre/post; exp(comb logits) go to
@@ -62,7 +68,13 @@ constexpr int kRG = 4;               // row groups (compute warps w and w+4 shar
 constexpr int kNCW = 8;              // compute warps: two per SM sub-partition
 constexpr int kFinisherWarp = 8;     // warps 8 and 9 take even and odd tiles
 constexpr int kSinkWarp = 10;        // the Sinkhorn of the tiles this CTA normalises
-constexpr int kThreads = 11 * 32;    // at most three warps per sub-partition: 168 registers each
+constexpr int kCollapseWarp0 = 12;   // persistent variant: warps 12-15 collapse tiles, refill stages
+constexpr int kCollapseThreads = 4 * 32;
+constexpr int kThreads = 16 * 32;    // four warpgroups, launched at 128 registers a thread
+// The two compute warpgroups take registers from the other two (whose warps wait
+// or stream shared memory): 2 x 128 x 184 + 2 x 128 x 72 = 512 x 128.
+constexpr int kRegsCompute = 184, kRegsAux = 72;
+static_assert(2 * 128 * kRegsCompute + 2 * 128 * kRegsAux == kThreads * 128, "register split");
 constexpr int kSinkLag = 8;          // a finisher waits for the Sinkhorn of the tile 8 before its own
 constexpr int kComputeThreads = kNCW * 32;
 constexpr int kNstPersist = 3;
@@ -72,8 +84,12 @@ constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 constexpr unsigned kFull = 0xffffffffu;
 
 // mbarrier slots
-constexpr int kBarXFull = 0, kBarRecv = 3, kBarPre = 5, kBarSink = 7, kBarWFull = 8, kBarSinkDone = 9,
-              kNumBars = 10;
+// Exchange buffers rotate over kNQ tiles (tile it uses slot it % kNQ).  Bytes for
+// tile it + 3 reach this CTA only after it has shipped tile it + 3, whose stage its
+// collapse of tile it released, so three slots would do; four leave a margin.
+constexpr int kNQ = 4;
+constexpr int kBarXFull = 0, kBarRecv = 3, kBarPre = kBarRecv + kNQ, kBarSink = kBarPre + kNQ,
+              kBarWFull = kBarSink + 1, kBarSinkDone = kBarWFull + 1, kNumBars = kBarSinkDone + 1;
 enum WaitSite : unsigned { kSiteWFull = 1, kSiteXFull, kSiteRecv, kSitePre, kSiteSink, kSiteDrain, kSiteSinkDone };
 
 template <int S>
@@ -111,10 +127,10 @@ __host__ __device__ inline Lay make_lay(int LK)
     L.off_w = o;
     if (!PERSIST)
         o += G::RP * LK * 4;
-    L.off_recv = o;                  // [2 tile parities][16 source CTAs][2 column halves][RV]
-    o += 2 * 2 * kCS * G::RV * 4;
-    L.off_pre = o;                   // [2 tile parities][16 tokens][4]: the tile's pre gates
-    o += 2 * kTMT * 4 * 4;
+    L.off_recv = o;                  // [kNQ slots][16 source CTAs][2 column halves][RV]
+    o += kNQ * 2 * kCS * G::RV * 4;
+    L.off_pre = o;                   // [kNQ slots][16 tokens][4]: the tile's pre gates
+    o += kNQ * kTMT * 4 * 4;
     L.off_sink = o;                  // [16 tokens][16]: the comb blocks this CTA scales
     o += kTMT * 16 * 4;
     L.off_bar = o;
@@ -141,7 +157,7 @@ struct Params {
 // Bounded wait on an mbarrier phase.  honor_abort = false is used only to let
 // this CTA's own bulk copies land before it exits.
 template <bool CLUSTER_SCOPE>
-__device__ __noinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int *abort_flag,
                                       StatusBlock *sb, unsigned site, bool honor_abort = true)
 {
     auto probe = [&]() {
@@ -343,7 +359,7 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const __gri
             ptx::mbar_init(BAR(kBarXFull + s), 1);
             issued[s] = 0;
         }
-        for (int q = 0; q < 2; ++q) {
+        for (int q = 0; q < kNQ; ++q) {
             ptx::mbar_init(BAR(kBarRecv + q), 1);   // armed by this CTA; data by remote stores
             ptx::mbar_init(BAR(kBarPre + q), 1);
         }
@@ -370,6 +386,7 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const __gri
     const uint32_t tmem_base = PERSIST ? *tmem_slot : 0u;
 
     if (warp < kNCW) {
+        ptx::setmaxnreg_inc<kRegsCompute>();
         // -------------------------------------------------------------- compute warps
         // One thread polls each barrier; a named barrier with an AND reduction then
         // hands its answer (and, by the barrier's ordering, what it acquired) to all
@@ -416,12 +433,11 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const __gri
                     load_tile(it);
         }
 
-        // Collapse tile itc (its pre gates arrive from the owners), then refill its
-        // stage with tile itc + nst.
+        // Decode variant: collapse its one tile once the owners' pre gates are in.
         auto collapse = [&](int itc) -> bool {
-            const int q = itc & 1;
+            const int q = itc % kNQ;
             const bool got =
-                threadIdx.x != 0 || wait_bar<true>(BAR(kBarPre + q), (itc >> 1) & 1, abort_flag, sb, kSitePre);
+                threadIdx.x != 0 || wait_bar<true>(BAR(kBarPre + q), (itc / kNQ) & 1, abort_flag, sb, kSitePre);
             if (!ptx::named_bar_and(1, kComputeThreads, got))
                 return false;
             int t0, tm;
@@ -449,9 +465,6 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const __gri
                 }
                 *reinterpret_cast<float4 *>(p.y + (size_t)(t0 + t) * p.d + (size_t)rank * p.hs + 4 * h4) = a;
             }
-            ptx::named_bar_sync(1, kComputeThreads);
-            if (threadIdx.x == 0 && tile_exists(itc + L.nst))
-                load_tile(itc + L.nst);
             return true;
         };
 
@@ -530,9 +543,8 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const __gri
             // Each value goes straight to its token's owner CTA (token t of the tile belongs
             // to CTA t), into recv[tile parity][this CTA][column half][row], by an
             // asynchronous remote store that completes on the owner's recv barrier.  (The
-            // owner consumed that slot's previous tile, it - 2, before it sent the gates
-            // that collapse(it - 2) needed.)
-            const int qb = it & 1;
+            // owner consumed that slot's previous tile before this CTA could ship this one.)
+            const int qb = it % kNQ;
             const uint32_t recv_slot = ptx::smem_u32(recv + ((qb * kCS + (int)rank) * 2 + half) * G::RV);
 #pragma unroll
             for (int q = 0; q < C::VPL; ++q) {
@@ -552,21 +564,18 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const __gri
                                       ptx::mapa(BAR(kBarRecv + qb), t));
                 }
             }
-            if (threadIdx.x == 0)   // the owners will answer with tm pre gates
-                ptx::mbar_arrive_expect_tx(BAR(kBarPre + qb), (uint32_t)(tm * 16));
-            if (it > 0 && !(ok = collapse(it - 1)))
-                break;
+            if (!PERSIST) {
+                if (threadIdx.x == 0)   // the owners will answer with tm pre gates
+                    ptx::mbar_arrive_expect_tx(BAR(kBarPre + qb), (uint32_t)(tm * 16));
+                if (!(ok = collapse(it)))
+                    break;
+            }
         }
-        if (ok && it > 0)
-            collapse(it - 1);
-        // Every bulk load this CTA issued lands before the CTA may exit.
-        if (threadIdx.x == 0) {
-            wait_bar<false>(BAR(kBarWFull), 0, abort_flag, sb, kSiteDrain, false);
-            for (int s = 0; s < L.nst; ++s)
-                if (issued[s] > 0)
-                    wait_bar<false>(BAR(kBarXFull + s), (issued[s] - 1) & 1, abort_flag, sb, kSiteDrain, false);
-        }
-    } else if (warp < kSinkWarp) {
+        __syncwarp();
+        ptx::setmaxnreg_dec<128>();
+    } else {
+      ptx::setmaxnreg_dec<kRegsAux>();
+      if (warp < kSinkWarp) {
         // -------------------------------------------------------------- finisher warps
         // Tile it's token t is owned by CTA t: its finisher (warp 8 + it % 2) sums the
         // 2 x 16 partials, forms the gates, sends pre to every CTA and post to memory,
@@ -578,14 +587,14 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const __gri
         // A CTA's Sinkhorn buffer is reused 16 tiles later.  Before this finisher sends
         // the gates of tile it, it waits until its CTA's Sinkhorn warp is done with tile
         // it - 8 if that tile was this CTA's: tile it - 8 + 16's exp values can only
-        // come once every CTA has collapsed tile it + 6, which needs gates this finisher
-        // sends after those of tile it.
+        // come once this CTA has shipped it, after collapsing tile it + 4, which needs
+        // gates this finisher sends after those of tile it.
         const int f = warp - kFinisherWarp;
         const int grp = lane < S ? 0 : (lane < 2 * S ? 1 : 2);
         const float my_scale = lane < G::R ? p.scale[grp] : 0.f;
         const float my_base = lane < G::R ? p.base[lane] : 0.f;
         for (int it = f; tile_exists(it); it += 2) {
-            const int qb = it & 1;
+            const int qb = it % kNQ;
             int t0, tm;
             tile_tokens(it, t0, tm);
             const bool own = (int)rank < tm;
@@ -596,10 +605,10 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const __gri
                 break;
             if (lane == 0)
                 ptx::mbar_arrive_expect_tx(BAR(kBarRecv + qb), own ? (uint32_t)(2 * kCS * (G::R + 1) * 4) : 0u);
-            if (!warp_wait<true>(lane, BAR(kBarRecv + qb), (it >> 1) & 1, abort_flag, sb, kSiteRecv)) {
+            if (!warp_wait<true>(lane, BAR(kBarRecv + qb), (it / kNQ) & 1, abort_flag, sb, kSiteRecv)) {
                 // Giving up: still let any partials already on their way land before exit.
                 if (lane == 0)
-                    wait_bar<true>(BAR(kBarRecv + qb), (it >> 1) & 1, abort_flag, sb, kSiteDrain, false);
+                    wait_bar<true>(BAR(kBarRecv + qb), (it / kNQ) & 1, abort_flag, sb, kSiteDrain, false);
                 __syncwarp();
                 break;
             }
@@ -641,7 +650,7 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const __gri
             }
             __syncwarp();
         }
-    } else {
+    } else if (warp == kSinkWarp) {
         // -------------------------------------------------------------- Sinkhorn warp
         // Tiles rank, rank + 16, ... are this CTA's to normalise: lane t takes token
         // t's S x S block of exp(comb logits) and runs the Sinkhorn in registers.
@@ -672,6 +681,69 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const __gri
             if (lane == 0)
                 ptx::mbar_arrive(BAR(kBarSinkDone));   // the buffer may be refilled
         }
+    } else if (PERSIST && warp >= kCollapseWarp0) {
+        // -------------------------------------------------------------- collapse warps
+        // Tile by tile: wait for the owners' pre gates, write y for this CTA's hidden
+        // columns from the tile's stage, then refill the stage with tile it + nst.  The
+        // compute warps never wait for gates; only the stage ring links them to these.
+        const int ct = threadIdx.x - kCollapseWarp0 * 32;
+        const int h4n = p.hs / 4;
+        constexpr int U = 2;   // outputs per thread in flight
+        for (int it = 0; tile_exists(it); ++it) {
+            const int q = it % kNQ;
+            int t0, tm;
+            tile_tokens(it, t0, tm);
+            bool got = true;
+            if (ct == 0) {   // the owners answer with tm pre gates
+                ptx::mbar_arrive_expect_tx(BAR(kBarPre + q), (uint32_t)(tm * 16));
+                got = wait_bar<true>(BAR(kBarPre + q), (it / kNQ) & 1, abort_flag, sb, kSitePre);
+            }
+            if (!ptx::named_bar_and(2, kCollapseThreads, got))
+                break;
+            const uint32_t xs_base = ptx::smem_u32(stages + (it % L.nst) * stage_floats);
+            const uint32_t pre_base = ptx::smem_u32(preb + q * kTMT * 4);
+            const int n = tm * h4n;
+            for (int e0 = ct; e0 < n; e0 += U * kCollapseThreads) {
+                float4 xv[U][S];
+                float pr[U][4];
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int e = min(e0 + kCollapseThreads * u, n - 1);
+                    const int t = e / h4n, h4 = e - t * h4n;
+                    const float4 pv = ptx::lds128(pre_base + 16u * (uint32_t)t);
+                    pr[u][0] = pv.x;
+                    pr[u][1] = pv.y;
+                    pr[u][2] = pv.z;
+                    pr[u][3] = pv.w;
+#pragma unroll
+                    for (int k = 0; k < S; ++k)
+                        xv[u][k] = ptx::lds128(xs_base + 4u * (uint32_t)(t * p.LK + k * p.hs + 4 * h4));
+                }
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int e = e0 + kCollapseThreads * u;
+                    if (e >= n)
+                        break;
+                    const int t = e / h4n, h4 = e - t * h4n;
+                    float4 a = make_float4(pr[u][0] * xv[u][0].x, pr[u][0] * xv[u][0].y, pr[u][0] * xv[u][0].z,
+                                           pr[u][0] * xv[u][0].w);
+#pragma unroll
+                    for (int k = 1; k < S; ++k) {
+                        a.x = fmaf(pr[u][k], xv[u][k].x, a.x);
+                        a.y = fmaf(pr[u][k], xv[u][k].y, a.y);
+                        a.z = fmaf(pr[u][k], xv[u][k].z, a.z);
+                        a.w = fmaf(pr[u][k], xv[u][k].w, a.w);
+                    }
+                    *reinterpret_cast<float4 *>(p.y + (size_t)(t0 + t) * p.d + (size_t)rank * p.hs + 4 * h4) = a;
+                }
+            }
+            ptx::named_bar_sync(2, kCollapseThreads);
+            if (ct == 0 && tile_exists(it + L.nst))
+                load_tile(it + L.nst);
+        }
+    }
+      __syncwarp();
+      ptx::setmaxnreg_inc<128>();
     }
 
     // ------------------------------------------------------------------ teardown
@@ -679,6 +751,14 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const __gri
     if (PERSIST)
         ptx::tmem_fence_before_sync();
     ptx::cluster_sync_all();   // no CTA leaves while another may still write its shared memory
+    // Every TMA load this CTA issued (by whichever warp) lands before it exits.
+    if (threadIdx.x == 0) {
+        wait_bar<false>(BAR(kBarWFull), 0, abort_flag, sb, kSiteDrain, false);
+        for (int s = 0; s < L.nst; ++s)
+            if (issued[s] > 0)
+                wait_bar<false>(BAR(kBarXFull + s), (issued[s] - 1) & 1, abort_flag, sb, kSiteDrain, false);
+    }
+    __syncwarp();
     if (PERSIST) {
         ptx::tmem_fence_after_sync();
         if (warp == 0)

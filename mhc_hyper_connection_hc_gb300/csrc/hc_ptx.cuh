@@ -227,6 +227,17 @@ __device__ __forceinline__ void tmem_alloc(uint32_t slot_smem, uint32_t ncols)
                  "r"(ncols)
                  : "memory");
 }
+// Hand registers between warpgroups (every warp of a warpgroup executes the same one).
+template <int N>
+__device__ __forceinline__ void setmaxnreg_inc()
+{
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void setmaxnreg_dec()
+{
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
 __device__ __forceinline__ void tmem_relinquish()
 {
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
