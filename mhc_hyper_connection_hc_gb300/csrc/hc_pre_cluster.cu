@@ -30,13 +30,15 @@
 //    squares straight into the owner CTA's receive buffer (token t of a tile
 //    belongs to CTA t) with st.async, which counts the bytes on the owner's
 //    mbarrier.  Then they go on to the next tile: they never wait for gates.
-//  * Persistent variant: four collapse warps (one per SM sub-partition) wait
-//    for each tile's pre gates, write y for the CTA's hidden columns from the
-//    tile's stage and refill the stage, so the stage ring alone couples them
-//    to the compute warps.  The decode variant's single tile is collapsed by
-//    the compute warps.  The sixteen warps launch at 128 registers; the two
-//    compute warpgroups raise theirs to 184 with setmaxnreg while the other
-//    two drop to 72.
+//  * Persistent variant: the two column halves of the compute warps wait for
+//    tiles on their own barriers, half 1 starting a tile later than half 0,
+//    so one half reduces and ships while the other runs its FMAs.  Four
+//    collapse warps (one per SM sub-partition) wait for each tile's pre gates,
+//    write y for the CTA's hidden columns from the tile's stage and refill the
+//    stage, so the stage ring alone couples them to the compute warps.  The
+//    decode variant's single tile is collapsed by the compute warps.  The
+//    sixteen warps launch at 128 registers; the two compute warpgroups raise
+//    theirs to 184 with setmaxnreg while the other two drop to 72.
 //  * Two finisher warps (even/odd tiles) of each owner sum the 2 x 16
 //    partials in a fixed tree, apply the rsqrt rescale, form the gates,
 //    broadcast pre to all 16 CTAs and write pre/post; exp(comb logits) go to
@@ -75,6 +77,9 @@ constexpr int kThreads = 16 * 32;    // four warpgroups, launched at 128 registe
 // or stream shared memory): 2 x 128 x 184 + 2 x 128 x 72 = 512 x 128.
 constexpr int kRegsCompute = 184, kRegsAux = 72;
 static_assert(2 * 128 * kRegsCompute + 2 * 128 * kRegsAux == kThreads * 128, "register split");
+// Named barriers: 1 all compute warps, 2 collapse warps, 3 + h column half h of the
+// persistent variant, 5 the halves' one-off start stagger.
+constexpr uint32_t kNbCompute = 1, kNbCollapse = 2, kNbHalf0 = 3, kNbStagger = 5;
 constexpr int kSinkLag = 8;          // a finisher waits for the Sinkhorn of the tile 8 before its own
 constexpr int kComputeThreads = kNCW * 32;
 constexpr int kNstPersist = 3;
@@ -468,14 +473,24 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const __gri
             return true;
         };
 
+        // Persistent variant: the two column halves (warpgroups) wait for tiles on
+        // their own barriers, and half 1 starts once half 0 has done its first dots,
+        // so one half reduces and ships while the other runs its FMAs.  The decode
+        // variant keeps all eight warps together (its collapse needs them all).
+        const uint32_t tbar = PERSIST ? kNbHalf0 + (uint32_t)half : kNbCompute;
+        const uint32_t tthreads = PERSIST ? kComputeThreads / 2 : kComputeThreads;
+        const int tpoll = PERSIST ? half * (kComputeThreads / 2) : 0;   // the thread that polls
+        bool arrived = !(PERSIST && half == 0);
+        if (PERSIST && half == 1)
+            ptx::named_bar_sync(kNbStagger, kComputeThreads);
         const int lk4 = p.LK * 4;
         int it = 0;
         for (; ok; ++it) {
             if (!tile_exists(it))
                 break;
             const int s = it % L.nst, u = it / L.nst;
-            ok = ptx::named_bar_and(1, kComputeThreads,
-                                    threadIdx.x != 0 ||
+            ok = ptx::named_bar_and(tbar, tthreads,
+                                    (int)threadIdx.x != tpoll ||
                                         wait_bar<false>(BAR(kBarXFull + s), u & 1, abort_flag, sb, kSiteXFull));
             if (!ok)
                 break;
@@ -525,6 +540,10 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const __gri
                     dots_step<S, NT>(acc, ssa, w, xs_addr, xq_addr, cofs, lk4);
                 }
             }
+            if (!arrived) {
+                ptx::named_bar_arrive(kNbStagger, kComputeThreads);
+                arrived = true;
+            }
 
             // Half-warp sums over the 16 K-groups.
             float v[C::NVP];
@@ -571,6 +590,8 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const __gri
                     break;
             }
         }
+        if (!arrived)
+            ptx::named_bar_arrive(kNbStagger, kComputeThreads);
         __syncwarp();
         ptx::setmaxnreg_dec<128>();
     } else {
@@ -698,7 +719,7 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const __gri
                 ptx::mbar_arrive_expect_tx(BAR(kBarPre + q), (uint32_t)(tm * 16));
                 got = wait_bar<true>(BAR(kBarPre + q), (it / kNQ) & 1, abort_flag, sb, kSitePre);
             }
-            if (!ptx::named_bar_and(2, kCollapseThreads, got))
+            if (!ptx::named_bar_and(kNbCollapse, kCollapseThreads, got))
                 break;
             const uint32_t xs_base = ptx::smem_u32(stages + (it % L.nst) * stage_floats);
             const uint32_t pre_base = ptx::smem_u32(preb + q * kTMT * 4);
@@ -737,7 +758,7 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const __gri
                     *reinterpret_cast<float4 *>(p.y + (size_t)(t0 + t) * p.d + (size_t)rank * p.hs + 4 * h4) = a;
                 }
             }
-            ptx::named_bar_sync(2, kCollapseThreads);
+            ptx::named_bar_sync(kNbCollapse, kCollapseThreads);
             if (ct == 0 && tile_exists(it + L.nst))
                 load_tile(it + L.nst);
         }

@@ -190,6 +190,11 @@ __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t threads)
 {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
+// Arrive on a named barrier without waiting (the other participants bar.sync on it).
+__device__ __forceinline__ void named_bar_arrive(uint32_t id, uint32_t threads)
+{
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
 // Named barrier that also ANDs a predicate over the participating threads, so a
 // decision taken after a bounded wait is the same in every participating warp.
 __device__ __forceinline__ bool named_bar_and(uint32_t id, uint32_t threads, bool v)
