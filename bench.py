@@ -20,6 +20,7 @@ CPU oracle on the host cores instead (rank 0 only).
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import os
@@ -199,7 +200,7 @@ def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
         return 0
-    w = synth.WORKLOADS[WORKLOAD_IDS[args.workload]]
+    w = selected_workload(args)
     sample = min(w.T, args.ref_tokens)
     for _ in range(args.warmup):
         time_oracle(w, max_tokens=min(sample, 64), budget_s=0.0, max_reps=1)
@@ -219,6 +220,16 @@ def run_reference(args):
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
+
+
+def selected_workload(args) -> synth.Workload:
+    """The workload named on the command line, with --iters overriding its Sinkhorn iterations."""
+    w = synth.WORKLOADS[WORKLOAD_IDS[args.workload]]
+    if args.iters is not None:
+        if args.iters < 1:
+            raise SystemExit("--iters must be >= 1")
+        w = dataclasses.replace(w, iters=args.iters)
+    return w
 
 
 def workload_config(w: synth.Workload, sample_tokens=None):
@@ -246,7 +257,7 @@ def run_gpu(args):
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     dev = torch.device("cuda", local if world > 1 else 0)
     torch.cuda.set_device(dev)
-    w = synth.WORKLOADS[WORKLOAD_IDS[args.workload]]
+    w = selected_workload(args)
     T, s, d, iters = w.T, w.s, w.d, w.iters
     stream = torch.cuda.Stream(device=dev)
 
@@ -333,7 +344,7 @@ def run_gpu(args):
     if not args.no_e2e:
         line["e2e"] = measure_e2e(w, dv, ws, out, x_out, stream, K, pre, post)
     if not args.no_decode:
-        line["decode_t1"] = measure_decode(dev)
+        line["decode_t1"] = measure_decode(dev, args.iters)
     if rank == 0 and world == 1 and not args.no_cpu:
         line["cpu_baseline"] = time_oracle(w, max_tokens=args.cpu_tokens, budget_s=10.0, max_reps=3)
     if rank == 0:
@@ -379,12 +390,15 @@ def measure_e2e(w, dv, ws, out, x_out, stream, K, pre, post):
             "d2h_bytes_per_step": d2h, "ms_per_step": 1e3 * sec / K}
 
 
-def measure_decode(dev, n_sites: int = 300):
+def measure_decode(dev, iters=None, n_sites: int = 300):
     """T = 1 site latency: 300 back-to-back sites (pre + post) replayed as one CUDA
-    graph, and the same launches issued eagerly on a stream."""
+    graph, and the same launches issued eagerly on a stream (iters: Sinkhorn
+    iterations, default the single-decode workload's)."""
     import torch
     from mhc_hyper_connection_hc_gb300 import hc
     w = synth.WORKLOADS[1]
+    if iters is not None:
+        w = dataclasses.replace(w, iters=iters)
     inp = synth.workload_inputs(w)
     stream = torch.cuda.Stream(device=dev)
     with torch.cuda.stream(stream):
@@ -438,6 +452,7 @@ def measure_decode(dev, n_sites: int = 300):
     res["us_per_site_wall_sync"] = statistics.median(walls)
     if hc.hc_workspace_status(ws, stream) != 0:
         raise RuntimeError("a kernel flagged an error in the decode measurement")
+    res["iters"] = w.iters
     res["path"] = "cluster" if hc.hc_pre_auto_path(1, w.s, w.d) == hc.HC_PATH_CLUSTER else "generic"
     return res
 
@@ -449,6 +464,7 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("gb300", "reference"), default="gb300")
     ap.add_argument("--workload", choices=tuple(WORKLOAD_IDS), default="prefill")
+    ap.add_argument("--iters", type=int, default=None, help="override the workload's Sinkhorn iterations")
     ap.add_argument("--cpu-tokens", type=int, default=4096, help="tokens of the CPU-oracle sample")
     ap.add_argument("--ref-tokens", type=int, default=256, help="tokens per reference-arm step")
     ap.add_argument("--no-e2e", action="store_true")
