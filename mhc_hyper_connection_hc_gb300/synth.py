@@ -32,6 +32,7 @@ _M2 = np.uint64(0x94D049BB133111EB)
 _CHUNK = 1 << 22
 
 TENSOR_X, TENSOR_FN_W, TENSOR_SCALE, TENSOR_BASE, TENSOR_F = 1, 2, 3, 4, 5
+TENSOR_HEAD_FN_W, TENSOR_HEAD_SCALE, TENSOR_HEAD_BASE = 6, 7, 8
 
 
 def tensor_seed(config: int, site: int, tensor_id: int) -> int:
@@ -105,6 +106,16 @@ def site_params(cid: int, site: int, s: int, d: int):
     fn_w = normal(tensor_seed(cid, site, TENSOR_FN_W), R * K, 0.0, 1.0 / math.sqrt(K)).reshape(R, K)
     scale = uniform(tensor_seed(cid, site, TENSOR_SCALE), 3, 0.5, 1.5)
     base = normal(tensor_seed(cid, site, TENSOR_BASE), R, 0.0, 0.1)
+    return fn_w, scale, base
+
+
+def head_params(cid: int, s: int, d: int):
+    """Gated-head exit trio: fn_w [s, s*d] ~ N(0, 1/(s*d)) (variance, as a site's),
+    scale [1] ~ U[0.5, 1.5), base [s] ~ N(0, 0.1)."""
+    K = s * d
+    fn_w = normal(tensor_seed(cid, 0, TENSOR_HEAD_FN_W), s * K, 0.0, 1.0 / math.sqrt(K)).reshape(s, K)
+    scale = uniform(tensor_seed(cid, 0, TENSOR_HEAD_SCALE), 1, 0.5, 1.5)
+    base = normal(tensor_seed(cid, 0, TENSOR_HEAD_BASE), s, 0.0, 0.1)
     return fn_w, scale, base
 
 

@@ -32,7 +32,9 @@ def _load():
                                  ctypes.c_int]
         lib.hco_expand.argtypes = [dp, dp, ctypes.c_long, ctypes.c_int, ctypes.c_long]
         lib.hco_mean.argtypes = [dp, dp, ctypes.c_long, ctypes.c_int, ctypes.c_long]
-        for fn in (lib.hco_pre, lib.hco_post, lib.hco_expand, lib.hco_mean):
+        lib.hco_head.argtypes = [dp, dp, dp, dp, ctypes.c_long, ctypes.c_int, ctypes.c_long,
+                                 ctypes.c_double, dp, dp, ctypes.c_int]
+        for fn in (lib.hco_pre, lib.hco_post, lib.hco_expand, lib.hco_mean, lib.hco_head):
             fn.restype = ctypes.c_int
         lib.hco_max_threads.restype = ctypes.c_int
         _lib = lib
@@ -90,6 +92,21 @@ def post(x, f, post_gates, comb, threads: int | None = None) -> np.ndarray:
                           threads or default_threads())
     if rc != 0:
         raise ValueError(f"hco_post failed with code {rc}")
+    return out
+
+
+def head(x, fn_w, scale, base, eps: float, threads: int | None = None):
+    """Gated-head trunk exit: x [T, s, d], fn_w [s, s*d], scale [1], base [s]
+    -> dict(gates [T, s], y [T, d])."""
+    x = _f64(x)
+    T, s, d = x.shape
+    fn_w = _f64(fn_w).reshape(s, s * d)
+    scale, base = _f64(scale).reshape(1), _f64(base).reshape(s)
+    out = dict(gates=np.empty((T, s)), y=np.empty((T, d)))
+    rc = _load().hco_head(_p(x), _p(fn_w), _p(scale), _p(base), T, s, d, float(eps),
+                          _p(out["gates"]), _p(out["y"]), threads or default_threads())
+    if rc != 0:
+        raise ValueError(f"hco_head failed with code {rc}")
     return out
 
 

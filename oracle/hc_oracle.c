@@ -29,6 +29,9 @@
  * both Sinkhorn denominators (hyper.rs pre_finish_into passes one eps to
  * rowsq_scale and to hc_sinkhorn_m).
  *
+ * The gated-head trunk exit (hco_head) is the pre gate and collapse of a head
+ * whose rows equal its streams, with one scale; see its comment.
+ *
  * Parity status: every exported function is pinned by tests/test_oracle_pins.py
  * (closed forms, hand-derived golden values, invariants, brute force).
  */
@@ -195,6 +198,53 @@ int hco_post(const double *x, const double *f, const double *post, const double 
                     acc += ct[j * s + k] * xt[(long)j * d + i];
                 ot[i] = acc;
             }
+        }
+    }
+    return HCO_OK;
+}
+
+/*
+ * Gated-head trunk exit (hyper.rs `collapse`, case HcCollapse::GatedHead; the
+ * head trio of HyperHead::load: fn_w [s, s*d] -- rows equal to streams -- base [s]
+ * and ONE scale).  The pages chain a linear (mixes = fn_w . x[t]), rowsq_scale
+ * (mixes *= rsqrt(mean(x[t]^2) + eps)), hc_head_pre (gates) and hc_collapse
+ * (y = sum_c gate_c * x[t, c, :]); they print no formula for the gates.  The
+ * reading used is the site's pre gate with the head's single scale:
+ *   gate[c] = sigmoid(mixes[c] * scale + base[c]) + eps.
+ * x [T, s, d], fn_w [s, s*d], scale [1], base [s] -> gates [T, s], y [T, d].
+ */
+int hco_head(const double *x, const double *fn_w, const double *scale, const double *base,
+             long T, int s, long d, double eps, double *gates, double *y, int nthreads)
+{
+    if (T < 0 || s < 1 || d < 1 || !(eps >= 0.0))
+        return HCO_EINVAL;
+    if (T == 0)
+        return HCO_OK;
+    if (!x || !fn_w || !scale || !base || !gates || !y)
+        return HCO_EINVAL;
+    if (nthreads < 1)
+        nthreads = 1;
+    const long K = (long)s * d;
+#pragma omp parallel for num_threads(nthreads) schedule(static)
+    for (long t = 0; t < T; ++t) {
+        const double *xt = x + t * K;
+        double ss = 0.0;
+        for (long q = 0; q < K; ++q)
+            ss += xt[q] * xt[q];
+        const double rinv = 1.0 / sqrt(ss / (double)K + eps);
+        double *g = gates + t * s;
+        for (int c = 0; c < s; ++c) {
+            const double *wr = fn_w + (long)c * K;
+            double dot = 0.0;
+            for (long q = 0; q < K; ++q)
+                dot += wr[q] * xt[q];
+            g[c] = sigmoid(rinv * dot * scale[0] + base[c]) + eps;
+        }
+        for (long i = 0; i < d; ++i) {
+            double acc = 0.0;
+            for (int c = 0; c < s; ++c)
+                acc += g[c] * xt[(long)c * d + i];
+            y[t * d + i] = acc;
         }
     }
     return HCO_OK;

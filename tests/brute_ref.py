@@ -48,3 +48,20 @@ def site(x, fn_w, scale, base, f, iters, eps):
                  for k in range(s)]
         out.append(dict(pre=pre, post=post, comb=m, y=y, x_out=x_out))
     return out
+
+
+def head(x, fn_w, scale, base, eps):
+    """Gated-head exit: rows = streams, one scale; gate = sigmoid(logit) + eps, then the
+    collapse.  x: [T][s][d], fn_w: [s][s*d].  Returns per-token dicts (gates, y)."""
+    out = []
+    for xt in x:
+        s, d = len(xt), len(xt[0])
+        flat = [xt[c][i] for c in range(s) for i in range(d)]
+        r = 1.0 / math.sqrt(sum(v * v for v in flat) / len(flat) + eps)
+        gates = []
+        for c in range(s):
+            dot = sum(fn_w[c][q] * flat[q] for q in range(s * d))
+            gates.append(1.0 / (1.0 + math.exp(-(dot * r * scale[0] + base[c]))) + eps)
+        y = [sum(gates[c] * xt[c][i] for c in range(s)) for i in range(d)]
+        out.append(dict(gates=gates, y=y))
+    return out

@@ -242,3 +242,78 @@ def test_oracle_rejects_bad_arguments():
         oracle.pre(x, np.zeros((8, 8)), [1, 1, 1], np.zeros(8), -1, 1e-6)
     r = oracle.pre(np.zeros((0, 2, 4)), np.zeros((8, 8)), [1, 1, 1], np.zeros(8), 3, 1e-6)
     assert r["y"].shape == (0, 4)
+
+
+# ----------------------------------------------------------------------------- gated-head exit
+
+
+def test_head_closed_form_zero_weights():
+    """fn_w = 0: every gate is sigmoid(base_c) + eps whatever x is, and y is that weighted
+    sum of the streams.  Pins the +eps, the sigmoid and the collapse's stream indexing."""
+    s, d, eps = 3, 8, 0.125
+    x = synth.stream_state(930, 4, s, d).astype(np.float64)
+    base = np.array([-1.0, 0.0, 2.0])
+    r = oracle.head(x, np.zeros((s, s * d)), [1.7], base, eps)
+    g = 1.0 / (1.0 + np.exp(-base)) + eps
+    np.testing.assert_allclose(r["gates"], np.tile(g, (4, 1)), rtol=1e-15)
+    np.testing.assert_allclose(r["y"], np.einsum("c,tcd->td", g, x), rtol=1e-14)
+
+
+def test_head_rescale_and_single_scale_closed_form():
+    """Constant x = 1/2, fn_w row c constant (c+1)/16 over K = 16, eps = 1/4:
+    mixes_c = (c+1)/sqrt(2) (as in the site test), and the ONE scale multiplies every row."""
+    s, d = 2, 8
+    x = np.full((1, s, d), 0.5)
+    fn_w = np.repeat(((np.arange(s) + 1) / 16.0)[:, None], s * d, axis=1)
+    base = np.array([0.01, -0.02])
+    r = oracle.head(x, fn_w, [3.0], base, 0.25)
+    logit = (np.arange(s) + 1) / math.sqrt(2.0) * 3.0 + base
+    np.testing.assert_allclose(r["gates"][0], 1.0 / (1.0 + np.exp(-logit)) + 0.25, rtol=1e-14)
+    np.testing.assert_allclose(r["y"][0], np.full(d, 0.5 * r["gates"][0].sum()), rtol=1e-15)
+
+
+def test_head_equals_site_pre_rows():
+    """A site whose pre rows, pre scale and pre bases are the head's computes the same gates
+    (its pre) and the same collapse y, whatever its other rows hold."""
+    s, d, T = 3, 16, 5
+    inp = synth.site_inputs(931, T, s, d)
+    hw, hs, hb = synth.head_params(931, s, d)
+    fn_w = inp["fn_w"].astype(np.float64).copy()
+    fn_w[:s] = hw
+    scale = np.array([hs[0], 0.7, 1.3])
+    base = inp["base"].astype(np.float64).copy()
+    base[:s] = hb
+    site = oracle.pre(inp["x"], fn_w, scale, base, 20, 1e-6)
+    head = oracle.head(inp["x"], hw, hs, hb, 1e-6)
+    np.testing.assert_allclose(head["gates"], site["pre"], rtol=1e-14)
+    np.testing.assert_allclose(head["y"], site["y"], rtol=1e-13, atol=1e-15)
+
+
+def test_head_uniform_streams():
+    """Identical streams: y = (sum of gates) * x_0."""
+    s, d = 4, 8
+    x0 = synth.stream_state(932, 3, 1, d).astype(np.float64)
+    x = np.repeat(x0, s, axis=1)
+    hw, hs, hb = synth.head_params(932, s, d)
+    r = oracle.head(x, hw, hs, hb, 1e-6)
+    np.testing.assert_allclose(r["y"], r["gates"].sum(axis=1)[:, None] * x0[:, 0], rtol=1e-13)
+
+
+@pytest.mark.parametrize("s,d,T", [(2, 8, 3), (3, 4, 2), (1, 8, 2)])
+def test_head_brute_force_restatement(s, d, T):
+    x = synth.stream_state(933 + s, T, s, d)
+    hw, hs, hb = synth.head_params(933 + s, s, d)
+    eps = float(np.float32(1e-6))
+    a = oracle.head(x, hw, hs, hb, eps)
+    b = brute_ref.head(x.astype(float).tolist(), hw.astype(float).tolist(), hs.astype(float).tolist(),
+                       hb.astype(float).tolist(), eps)
+    for t in range(T):
+        np.testing.assert_allclose(a["gates"][t], np.array(b[t]["gates"]), rtol=1e-13, atol=1e-15)
+        np.testing.assert_allclose(a["y"][t], np.array(b[t]["y"]), rtol=1e-13, atol=1e-15)
+
+
+def test_head_rejects_bad_arguments():
+    with pytest.raises(ValueError):
+        oracle.head(np.zeros((1, 2, 4)), np.zeros((2, 8)), [1.0], np.zeros(2), -1.0)
+    r = oracle.head(np.zeros((0, 2, 4)), np.zeros((2, 8)), [1.0], np.zeros(2), 1e-6)
+    assert r["y"].shape == (0, 4)
