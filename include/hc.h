@@ -177,6 +177,31 @@ int hc_post(const float *x, const float *f, const float *post, const float *comb
             float *x_out, int T, int s, int d, void *stream);
 
 /*
+ * hc_head -- gated-head trunk exit [T, s, d] -> [T, d] (hyper.rs `collapse`, case
+ * HcCollapse::GatedHead: the head trio of HyperHead::load -- fn_w with rows equal
+ * to the streams, base [s] and ONE scale -- then rowsq_scale, hc_head_pre and
+ * hc_collapse).  Per token:
+ *   mixes[c] = rsqrt(mean(x[t]^2) + eps) * (fn_w[c, :] . x[t, :, :])   c < s
+ *   gate[c]  = sigmoid(mixes[c] * scale[0] + base[c]) + eps
+ *   y[t, :]  = sum_c gate[c] * x[t, c, :]
+ * The pages print no formula for the head gates; the one above is the site's pre
+ * gate with the head's single scale.
+ *   x [T, s, d] (in), fn_w [s, s*d] row-major (in), scale [1] (in), base [s] (in),
+ *   gates [T, s] (out, optional: NULL skips it), y [T, d] (out),
+ *   workspace, ws_bytes: >= hc_pre_workspace_bytes(T, s, d), as for hc_pre_fused.
+ * Same conventions, limits, determinism and batch invariance (cluster path) as
+ * hc_pre_fused; the cluster path takes the shapes it takes there.
+ */
+int hc_head(const float *x, const float *fn_w, const float *scale, const float *base,
+            int T, int s, int d, float eps, float *gates, float *y,
+            void *workspace, size_t ws_bytes, void *stream);
+
+/* hc_head with an explicit kernel path (enum hc_pre_path). */
+int hc_head_path(const float *x, const float *fn_w, const float *scale, const float *base,
+                 int T, int s, int d, float eps, float *gates, float *y,
+                 void *workspace, size_t ws_bytes, void *stream, int path);
+
+/*
  * hc_mean -- unweighted stream mean [T, s, d] -> [T, d] (hyper.rs
  * `contract_mean`, the glm5_next trunk exit `HcCollapse::Mean`).
  *   x [T, s, d] (in), out [T, d] (out, must not overlap x).

@@ -228,6 +228,60 @@ int hc_pre_fused_path(const float *x, const float *fn_w, const float *scale, con
                                           comb, y, workspace, st));
 }
 
+int hc_head_path(const float *x, const float *fn_w, const float *scale, const float *base, int T,
+                 int s, int d, float eps, float *gates, float *y, void *workspace, size_t ws_bytes,
+                 void *stream, int path)
+{
+    if (!dims_ok(T, s, d) || !(eps > 0.f) || !std::isfinite(eps))
+        return HC_ERR_DIM;
+    if (path != HC_PATH_AUTO && path != HC_PATH_GENERIC && path != HC_PATH_CLUSTER)
+        return HC_ERR_DIM;
+    if (T == 0)
+        return HC_OK;
+    if (!x || !fn_w || !scale || !base || !y)
+        return HC_ERR_NULL;
+    if (d % 4 || !aligned(x, 16) || !aligned(fn_w, 16) || !aligned(y, 16) || !aligned(scale, 4) ||
+        !aligned(base, 4) || (gates && !aligned(gates, 4)))
+        return HC_ERR_ALIGN;
+    const size_t xb = (size_t)T * s * d * 4, wb = (size_t)s * s * d * 4;
+    const size_t gb = gates ? (size_t)T * s * 4 : 0, yb = (size_t)T * d * 4;
+    const void *ins[4] = {x, fn_w, scale, base};
+    const size_t in_b[4] = {xb, wb, 4, (size_t)s * 4};
+    const void *outs[2] = {gates, y};
+    const size_t out_b[2] = {gb, yb};
+    for (int o = 0; o < 2; ++o)
+        for (int i = 0; i < 4; ++i)
+            if (overlap(outs[o], out_b[o], ins[i], in_b[i]))
+                return HC_ERR_ALIAS;
+    if (overlap(gates, gb, y, yb))
+        return HC_ERR_ALIAS;
+    if (!workspace || !aligned(workspace, 16) || ws_bytes < hc_pre_workspace_bytes(T, s, d))
+        return HC_ERR_WORKSPACE;
+    for (int o = 0; o < 2; ++o)
+        if (overlap(outs[o], out_b[o], workspace, ws_bytes))
+            return HC_ERR_ALIAS;
+    for (int i = 0; i < 4; ++i)
+        if (overlap(ins[i], in_b[i], workspace, ws_bytes))
+            return HC_ERR_ALIAS;
+
+    if (path == HC_PATH_AUTO)
+        path = hc::cluster_supported(s, d, true) ? HC_PATH_CLUSTER : HC_PATH_GENERIC;
+    cudaStream_t st = as_stream(stream);
+    if (path == HC_PATH_CLUSTER) {
+        if (!hc::cluster_supported(s, d, true))
+            return HC_ERR_UNSUPPORTED;
+        return cuda_rc(hc::launch_head_cluster(x, fn_w, scale, base, T, s, d, eps, gates, y, workspace, st));
+    }
+    return cuda_rc(hc::launch_head_generic(x, fn_w, scale, base, T, s, d, eps, gates, y, workspace, st));
+}
+
+int hc_head(const float *x, const float *fn_w, const float *scale, const float *base, int T, int s,
+            int d, float eps, float *gates, float *y, void *workspace, size_t ws_bytes, void *stream)
+{
+    return hc_head_path(x, fn_w, scale, base, T, s, d, eps, gates, y, workspace, ws_bytes, stream,
+                        HC_PATH_AUTO);
+}
+
 int hc_pre_fused(const float *x, const float *fn_w, const float *scale, const float *base, int T,
                  int s, int d, int iters, float eps, float *pre, float *post, float *comb, float *y,
                  void *workspace, size_t ws_bytes, void *stream)

@@ -66,9 +66,18 @@ cudaError_t launch_pre_generic(const float *x, const float *fn_w, const float *s
 // shape fits and the device can co-schedule the clusters.
 bool cluster_shape_ok(int s, int d);
 bool cluster_supported(int s, int d);
+bool cluster_supported(int s, int d, bool head);
 cudaError_t launch_pre_cluster(const float *x, const float *fn_w, const float *scale,
                                const float *base, int T, int s, int d, int iters, float eps,
                                float *pre, float *post, float *comb, float *y,
                                void *workspace, cudaStream_t st);
+
+// Gated-head trunk exit: rows = streams, one scale, gates (optional output) + collapse.
+cudaError_t launch_head_cluster(const float *x, const float *fn_w, const float *scale,
+                                const float *base, int T, int s, int d, float eps, float *gates,
+                                float *y, void *workspace, cudaStream_t st);
+cudaError_t launch_head_generic(const float *x, const float *fn_w, const float *scale,
+                                const float *base, int T, int s, int d, float eps, float *gates,
+                                float *y, void *workspace, cudaStream_t st);
 
 }  // namespace hc

@@ -74,7 +74,10 @@ constexpr int kCollapseWarp0 = 12;   // persistent variant: warps 12-15 collapse
 constexpr int kCollapseThreads = 4 * 32;
 constexpr int kThreads = 16 * 32;    // four warpgroups, launched at 128 registers a thread
 // The two compute warpgroups take registers from the other two (whose warps wait
-// or stream shared memory): 2 x 128 x 184 + 2 x 128 x 72 = 512 x 128.
+// or stream shared memory): 2 x 128 x 184 + 2 x 128 x 72 = 512 x 128.  The split
+// is made once, at the role dispatch, and kept until exit: a warpgroup that gave
+// registers back and then asked for them again could take them before the compute
+// warpgroups had theirs, and those would then wait for registers forever.
 constexpr int kRegsCompute = 184, kRegsAux = 72;
 static_assert(2 * 128 * kRegsCompute + 2 * 128 * kRegsAux == kThreads * 128, "register split");
 // Named barriers: 1 all compute warps, 2 collapse warps, 3 + h column half h of the
@@ -97,9 +100,10 @@ constexpr int kBarXFull = 0, kBarRecv = 3, kBarPre = kBarRecv + kNQ, kBarSink = 
               kBarWFull = kBarSink + 1, kBarSinkDone = kBarWFull + 1, kNumBars = kBarSinkDone + 1;
 enum WaitSite : unsigned { kSiteWFull = 1, kSiteXFull, kSiteRecv, kSitePre, kSiteSink, kSiteDrain, kSiteSinkDone };
 
-template <int S>
+// HEAD: the gated-head trunk exit, whose rows equal its streams (pre gates only).
+template <int S, bool HEAD = false>
 struct CG {
-    static constexpr int R = (2 + S) * S;
+    static constexpr int R = HEAD ? S : (2 + S) * S;
     static constexpr int RP = (R + kRG - 1) / kRG * kRG;   // rows padded to the 4 row groups
     static constexpr int B = RP / kRG;                      // rows per compute warp
     static constexpr int RV = (R + 1 + 3) / 4 * 4;          // exchange stride: R dots + sum of squares
@@ -108,9 +112,9 @@ struct CG {
 
 // NT = token slots per half-warp (a tile holds up to 2*NT tokens, one owner CTA each).
 // The warps of row group g sum the squares of slots g, g+4, ...: NSS values per thread.
-template <int S, int NT>
+template <int S, int NT, bool HEAD = false>
 struct CT {
-    static constexpr int B = CG<S>::B;
+    static constexpr int B = CG<S, HEAD>::B;
     static constexpr int NSS = (NT + kRG - 1) / kRG;
     static constexpr int NV = NT * B + NSS;                 // per-thread values before the reduce-scatter
     static constexpr int NVP = (NV + 15) / 16 * 16;
@@ -121,10 +125,10 @@ struct Lay {   // shared-memory layout in bytes
     int stage_bytes, nst, off_w, off_recv, off_pre, off_sink, off_bar, off_misc, total;
 };
 
-template <int S, bool PERSIST>
+template <int S, bool PERSIST, bool HEAD>
 __host__ __device__ inline Lay make_lay(int LK)
 {
-    using G = CG<S>;
+    using G = CG<S, HEAD>;
     Lay L;
     L.stage_bytes = kTMT * LK * 4;
     L.nst = PERSIST ? kNstPersist : 1;
@@ -276,16 +280,15 @@ __device__ __forceinline__ void sinkhorn_regs(float *c, int iters, float eps)
 // One column group of the dots: 4 columns of the NT token slots of this half-warp,
 // times this warp's B rows, as packed float32 FMAs (acc = (even-column sum,
 // odd-column sum)); plus the sums of squares of this warp's NSS slots.
-template <int S, int NT>
-__device__ __forceinline__ void dots_step(float2 (&acc)[NT][CG<S>::B], float2 (&ssa)[CT<S, NT>::NSS],
-                                          const float (&w)[CG<S>::WQ], uint32_t xs_addr,
+template <int B, int NT, int NSS>
+__device__ __forceinline__ void dots_step(float2 (&acc)[NT][B], float2 (&ssa)[NSS],
+                                          const float (&w)[4 * B], uint32_t xs_addr,
                                           uint32_t xq_addr, uint32_t cofs, int lk4)
 {
-    constexpr int B = CG<S>::B;
     constexpr int NH = NT > 4 ? 4 : NT;   // token slots per half (fewer live x registers)
-    float4 xq[CT<S, NT>::NSS];
+    float4 xq[NSS];
 #pragma unroll
-    for (int m = 0; m < CT<S, NT>::NSS; ++m)
+    for (int m = 0; m < NSS; ++m)
         xq[m] = ptx::lds128(xq_addr + (uint32_t)(m * kRG * lk4) + cofs);
 #pragma unroll
     for (int i0 = 0; i0 < NT; i0 += NH) {
@@ -309,20 +312,20 @@ __device__ __forceinline__ void dots_step(float2 (&acc)[NT][CG<S>::B], float2 (&
                                             acc[i0 + i][r]);
     }
 #pragma unroll
-    for (int m = 0; m < CT<S, NT>::NSS; ++m) {
+    for (int m = 0; m < NSS; ++m) {
         const float2 lo = make_float2(xq[m].x, xq[m].y), hi = make_float2(xq[m].z, xq[m].w);
         ssa[m] = ptx::ffma2(lo, lo, ssa[m]);
         ssa[m] = ptx::ffma2(hi, hi, ssa[m]);
     }
 }
 
-template <int S, bool PERSIST, int NT>
+template <int S, bool PERSIST, int NT, bool HEAD>
 __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const __grid_constant__ Params p)
 {
-    using G = CG<S>;
-    using C = CT<S, NT>;
+    using G = CG<S, HEAD>;
+    using C = CT<S, NT, HEAD>;
     extern __shared__ __align__(128) unsigned char smem[];
-    const Lay L = make_lay<S, PERSIST>(p.LK);
+    const Lay L = make_lay<S, PERSIST, HEAD>(p.LK);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = ptx::cluster_ctarank();
     const int cid = (int)ptx::cluster_id_x(), ncl = (int)ptx::ncluster_x();
@@ -523,7 +526,7 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const __gri
                     float w[G::WQ];
                     ptx::tmem_ld_issue<G::WQ>(trow + (uint32_t)(jj * G::WQ), w);
                     ptx::tmem_ld_wait_regs<G::WQ>(w);
-                    dots_step<S, NT>(acc, ssa, w, xs_addr, xq_addr, 256u * (uint32_t)(j0 + jj), lk4);
+                    dots_step<G::B, NT, C::NSS>(acc, ssa, w, xs_addr, xq_addr, 256u * (uint32_t)(j0 + jj), lk4);
                 }
             } else {
                 for (int jj = 0; jj < nj; ++jj) {
@@ -537,7 +540,7 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const __gri
                         w[4 * r + 2] = v.z;
                         w[4 * r + 3] = v.w;
                     }
-                    dots_step<S, NT>(acc, ssa, w, xs_addr, xq_addr, cofs, lk4);
+                    dots_step<G::B, NT, C::NSS>(acc, ssa, w, xs_addr, xq_addr, cofs, lk4);
                 }
             }
             if (!arrived) {
@@ -592,179 +595,177 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const __gri
         }
         if (!arrived)
             ptx::named_bar_arrive(kNbStagger, kComputeThreads);
-        __syncwarp();
-        ptx::setmaxnreg_dec<128>();
     } else {
-      ptx::setmaxnreg_dec<kRegsAux>();
-      if (warp < kSinkWarp) {
-        // -------------------------------------------------------------- finisher warps
-        // Tile it's token t is owned by CTA t: its finisher (warp 8 + it % 2) sums the
-        // 2 x 16 partials, forms the gates, sends pre to every CTA and post to memory,
-        // and hands exp(comb logits) to the tile's Sinkhorn CTA (it % 16), whose
-        // Sinkhorn warp scales all of the tile's tokens at once, one token per lane.
-        // Only a cluster's last tile can be partial, so no later tile's bytes can
-        // reach a CTA that owns nothing in this one.
-        //
-        // A CTA's Sinkhorn buffer is reused 16 tiles later.  Before this finisher sends
-        // the gates of tile it, it waits until its CTA's Sinkhorn warp is done with tile
-        // it - 8 if that tile was this CTA's: tile it - 8 + 16's exp values can only
-        // come once this CTA has shipped it, after collapsing tile it + 4, which needs
-        // gates this finisher sends after those of tile it.
-        const int f = warp - kFinisherWarp;
-        const int grp = lane < S ? 0 : (lane < 2 * S ? 1 : 2);
-        const float my_scale = lane < G::R ? p.scale[grp] : 0.f;
-        const float my_base = lane < G::R ? p.base[lane] : 0.f;
-        for (int it = f; tile_exists(it); it += 2) {
-            const int qb = it % kNQ;
-            int t0, tm;
-            tile_tokens(it, t0, tm);
-            const bool own = (int)rank < tm;
-            const uint32_t sc = (uint32_t)(it % kCS);
-            const int itl = it - kSinkLag;
-            if (itl >= 0 && itl % kCS == (int)rank &&
-                !warp_wait<false>(lane, BAR(kBarSinkDone), (itl / kCS) & 1, abort_flag, sb, kSiteSinkDone))
-                break;
-            if (lane == 0)
-                ptx::mbar_arrive_expect_tx(BAR(kBarRecv + qb), own ? (uint32_t)(2 * kCS * (G::R + 1) * 4) : 0u);
-            if (!warp_wait<true>(lane, BAR(kBarRecv + qb), (it / kNQ) & 1, abort_flag, sb, kSiteRecv)) {
-                // Giving up: still let any partials already on their way land before exit.
+        ptx::setmaxnreg_dec<kRegsAux>();
+        if (warp < kSinkWarp) {
+            // -------------------------------------------------------------- finisher warps
+            // Tile it's token t is owned by CTA t: its finisher (warp 8 + it % 2) sums the
+            // 2 x 16 partials, forms the gates, sends pre to every CTA and post to memory,
+            // and hands exp(comb logits) to the tile's Sinkhorn CTA (it % 16), whose
+            // Sinkhorn warp scales all of the tile's tokens at once, one token per lane.
+            // Only a cluster's last tile can be partial, so no later tile's bytes can
+            // reach a CTA that owns nothing in this one.
+            //
+            // A CTA's Sinkhorn buffer is reused 16 tiles later.  Before this finisher sends
+            // the gates of tile it, it waits until its CTA's Sinkhorn warp is done with tile
+            // it - 8 if that tile was this CTA's: tile it - 8 + 16's exp values can only
+            // come once this CTA has shipped it, after collapsing tile it + 4, which needs
+            // gates this finisher sends after those of tile it.
+            const int f = warp - kFinisherWarp;
+            const int grp = lane < S ? 0 : (lane < 2 * S ? 1 : 2);
+            const float my_scale = lane < G::R ? p.scale[grp] : 0.f;
+            const float my_base = lane < G::R ? p.base[lane] : 0.f;
+            for (int it = f; tile_exists(it); it += 2) {
+                const int qb = it % kNQ;
+                int t0, tm;
+                tile_tokens(it, t0, tm);
+                const bool own = (int)rank < tm;
+                const uint32_t sc = (uint32_t)(it % kCS);
+                const int itl = it - kSinkLag;
+                if (!HEAD && itl >= 0 && itl % kCS == (int)rank &&
+                    !warp_wait<false>(lane, BAR(kBarSinkDone), (itl / kCS) & 1, abort_flag, sb, kSiteSinkDone))
+                    break;
                 if (lane == 0)
-                    wait_bar<true>(BAR(kBarRecv + qb), (it / kNQ) & 1, abort_flag, sb, kSiteDrain, false);
-                __syncwarp();
-                break;
-            }
-            if (own) {
-                float val = 0.f;
-                if (lane <= G::R) {
-                    float src[2 * kCS];
-                    const uint32_t a0 = ptx::smem_u32(recv + qb * 2 * kCS * G::RV + lane);
-#pragma unroll
-                    for (int c = 0; c < 2 * kCS; ++c)
-                        src[c] = ptx::lds32(a0 + 4u * (uint32_t)(c * G::RV));
-                    val = tree_sum<2 * kCS>(src);   // sources and halves in a fixed pairwise order
+                    ptx::mbar_arrive_expect_tx(BAR(kBarRecv + qb), own ? (uint32_t)(2 * kCS * (G::R + 1) * 4) : 0u);
+                if (!warp_wait<true>(lane, BAR(kBarRecv + qb), (it / kNQ) & 1, abort_flag, sb, kSiteRecv)) {
+                    // Giving up: still let any partials already on their way land before exit.
+                    if (lane == 0)
+                        wait_bar<true>(BAR(kBarRecv + qb), (it / kNQ) & 1, abort_flag, sb, kSiteDrain, false);
+                    __syncwarp();
+                    break;
                 }
-                const float ss = __shfl_sync(kFull, val, G::R);
-                const float rinv = rsqrtf(ss * p.invK + p.eps);
-                const float logit = lane < G::R ? val * rinv * my_scale + my_base : 0.f;
-                const float sg = __frcp_rn(1.f + expf(-logit));
-                const float pre_v = sg + p.eps;
-                // pre gates of this token -> every CTA of the cluster (16 bytes each);
-                // exp(comb logits) -> the Sinkhorn CTA, one value per lane.
-                float4 pv;
-                pv.x = __shfl_sync(kFull, pre_v, 0);
-                pv.y = __shfl_sync(kFull, pre_v, 1 % S);
-                pv.z = __shfl_sync(kFull, pre_v, 2 % S);
-                pv.w = __shfl_sync(kFull, pre_v, 3 % S);
-                if (lane < kCS) {
-                    const uint32_t dst = ptx::smem_u32(preb + (qb * kTMT + (int)rank) * 4);
-                    ptx::st_async_v4(ptx::mapa(dst, (uint32_t)lane), pv, ptx::mapa(BAR(kBarPre + qb), (uint32_t)lane));
-                }
-                if (lane >= 2 * S && lane < G::R) {
-                    const uint32_t dst = ptx::smem_u32(sinkbuf + (int)rank * 16 + (lane - 2 * S));
-                    ptx::st_async_f32(ptx::mapa(dst, sc), expf(logit), ptx::mapa(BAR(kBarSink), sc));
-                }
-                const size_t tok = (size_t)t0 + rank;
-                if (lane < S)
-                    p.pre[tok * S + lane] = pre_v;
-                else if (lane < 2 * S)
-                    p.post[tok * S + (lane - S)] = 2.f * sg;
-            }
-            __syncwarp();
-        }
-    } else if (warp == kSinkWarp) {
-        // -------------------------------------------------------------- Sinkhorn warp
-        // Tiles rank, rank + 16, ... are this CTA's to normalise: lane t takes token
-        // t's S x S block of exp(comb logits) and runs the Sinkhorn in registers.
-        for (int it = (int)rank; tile_exists(it); it += kCS) {
-            int t0, tm;
-            tile_tokens(it, t0, tm);
-            if (lane == 0)
-                ptx::mbar_arrive_expect_tx(BAR(kBarSink), (uint32_t)(tm * S * S * 4));
-            if (!warp_wait<true>(lane, BAR(kBarSink), (it / kCS) & 1, abort_flag, sb, kSiteSink)) {
-                if (lane == 0)
-                    wait_bar<true>(BAR(kBarSink), (it / kCS) & 1, abort_flag, sb, kSiteDrain, false);
-                __syncwarp();
-                break;
-            }
-            if (lane < tm) {
-                float cm[S * S];
-                const float *src = sinkbuf + lane * 16;
-#pragma unroll
-                for (int q = 0; q < S * S; ++q)
-                    cm[q] = src[q];
-                sinkhorn_regs<S>(cm, p.iters, p.eps);
-                float *dst = p.comb + (size_t)(t0 + lane) * S * S;
-#pragma unroll
-                for (int q = 0; q < S * S; ++q)
-                    dst[q] = cm[q];
-            }
-            __syncwarp();
-            if (lane == 0)
-                ptx::mbar_arrive(BAR(kBarSinkDone));   // the buffer may be refilled
-        }
-    } else if (PERSIST && warp >= kCollapseWarp0) {
-        // -------------------------------------------------------------- collapse warps
-        // Tile by tile: wait for the owners' pre gates, write y for this CTA's hidden
-        // columns from the tile's stage, then refill the stage with tile it + nst.  The
-        // compute warps never wait for gates; only the stage ring links them to these.
-        const int ct = threadIdx.x - kCollapseWarp0 * 32;
-        const int h4n = p.hs / 4;
-        constexpr int U = 2;   // outputs per thread in flight
-        for (int it = 0; tile_exists(it); ++it) {
-            const int q = it % kNQ;
-            int t0, tm;
-            tile_tokens(it, t0, tm);
-            bool got = true;
-            if (ct == 0) {   // the owners answer with tm pre gates
-                ptx::mbar_arrive_expect_tx(BAR(kBarPre + q), (uint32_t)(tm * 16));
-                got = wait_bar<true>(BAR(kBarPre + q), (it / kNQ) & 1, abort_flag, sb, kSitePre);
-            }
-            if (!ptx::named_bar_and(kNbCollapse, kCollapseThreads, got))
-                break;
-            const uint32_t xs_base = ptx::smem_u32(stages + (it % L.nst) * stage_floats);
-            const uint32_t pre_base = ptx::smem_u32(preb + q * kTMT * 4);
-            const int n = tm * h4n;
-            for (int e0 = ct; e0 < n; e0 += U * kCollapseThreads) {
-                float4 xv[U][S];
-                float pr[U][4];
-#pragma unroll
-                for (int u = 0; u < U; ++u) {
-                    const int e = min(e0 + kCollapseThreads * u, n - 1);
-                    const int t = e / h4n, h4 = e - t * h4n;
-                    const float4 pv = ptx::lds128(pre_base + 16u * (uint32_t)t);
-                    pr[u][0] = pv.x;
-                    pr[u][1] = pv.y;
-                    pr[u][2] = pv.z;
-                    pr[u][3] = pv.w;
-#pragma unroll
-                    for (int k = 0; k < S; ++k)
-                        xv[u][k] = ptx::lds128(xs_base + 4u * (uint32_t)(t * p.LK + k * p.hs + 4 * h4));
-                }
-#pragma unroll
-                for (int u = 0; u < U; ++u) {
-                    const int e = e0 + kCollapseThreads * u;
-                    if (e >= n)
-                        break;
-                    const int t = e / h4n, h4 = e - t * h4n;
-                    float4 a = make_float4(pr[u][0] * xv[u][0].x, pr[u][0] * xv[u][0].y, pr[u][0] * xv[u][0].z,
-                                           pr[u][0] * xv[u][0].w);
-#pragma unroll
-                    for (int k = 1; k < S; ++k) {
-                        a.x = fmaf(pr[u][k], xv[u][k].x, a.x);
-                        a.y = fmaf(pr[u][k], xv[u][k].y, a.y);
-                        a.z = fmaf(pr[u][k], xv[u][k].z, a.z);
-                        a.w = fmaf(pr[u][k], xv[u][k].w, a.w);
+                if (own) {
+                    float val = 0.f;
+                    if (lane <= G::R) {
+                        float src[2 * kCS];
+                        const uint32_t a0 = ptx::smem_u32(recv + qb * 2 * kCS * G::RV + lane);
+    #pragma unroll
+                        for (int c = 0; c < 2 * kCS; ++c)
+                            src[c] = ptx::lds32(a0 + 4u * (uint32_t)(c * G::RV));
+                        val = tree_sum<2 * kCS>(src);   // sources and halves in a fixed pairwise order
                     }
-                    *reinterpret_cast<float4 *>(p.y + (size_t)(t0 + t) * p.d + (size_t)rank * p.hs + 4 * h4) = a;
+                    const float ss = __shfl_sync(kFull, val, G::R);
+                    const float rinv = rsqrtf(ss * p.invK + p.eps);
+                    const float logit = lane < G::R ? val * rinv * my_scale + my_base : 0.f;
+                    const float sg = __frcp_rn(1.f + expf(-logit));
+                    const float pre_v = sg + p.eps;
+                    // pre gates of this token -> every CTA of the cluster (16 bytes each);
+                    // exp(comb logits) -> the Sinkhorn CTA, one value per lane.
+                    float4 pv;
+                    pv.x = __shfl_sync(kFull, pre_v, 0);
+                    pv.y = __shfl_sync(kFull, pre_v, 1 % S);
+                    pv.z = __shfl_sync(kFull, pre_v, 2 % S);
+                    pv.w = __shfl_sync(kFull, pre_v, 3 % S);
+                    if (lane < kCS) {
+                        const uint32_t dst = ptx::smem_u32(preb + (qb * kTMT + (int)rank) * 4);
+                        ptx::st_async_v4(ptx::mapa(dst, (uint32_t)lane), pv, ptx::mapa(BAR(kBarPre + qb), (uint32_t)lane));
+                    }
+                    if (!HEAD && lane >= 2 * S && lane < G::R) {
+                        const uint32_t dst = ptx::smem_u32(sinkbuf + (int)rank * 16 + (lane - 2 * S));
+                        ptx::st_async_f32(ptx::mapa(dst, sc), expf(logit), ptx::mapa(BAR(kBarSink), sc));
+                    }
+                    const size_t tok = (size_t)t0 + rank;
+                    if (lane < S) {
+                        if (p.pre)   // the head's gates are an optional output
+                            p.pre[tok * S + lane] = pre_v;
+                    } else if (!HEAD && lane < 2 * S) {
+                        p.post[tok * S + (lane - S)] = 2.f * sg;
+                    }
                 }
+                __syncwarp();
             }
-            ptx::named_bar_sync(kNbCollapse, kCollapseThreads);
-            if (ct == 0 && tile_exists(it + L.nst))
-                load_tile(it + L.nst);
+        } else if (!HEAD && warp == kSinkWarp) {
+            // -------------------------------------------------------------- Sinkhorn warp
+            // Tiles rank, rank + 16, ... are this CTA's to normalise: lane t takes token
+            // t's S x S block of exp(comb logits) and runs the Sinkhorn in registers.
+            for (int it = (int)rank; tile_exists(it); it += kCS) {
+                int t0, tm;
+                tile_tokens(it, t0, tm);
+                if (lane == 0)
+                    ptx::mbar_arrive_expect_tx(BAR(kBarSink), (uint32_t)(tm * S * S * 4));
+                if (!warp_wait<true>(lane, BAR(kBarSink), (it / kCS) & 1, abort_flag, sb, kSiteSink)) {
+                    if (lane == 0)
+                        wait_bar<true>(BAR(kBarSink), (it / kCS) & 1, abort_flag, sb, kSiteDrain, false);
+                    __syncwarp();
+                    break;
+                }
+                if (lane < tm) {
+                    float cm[S * S];
+                    const float *src = sinkbuf + lane * 16;
+    #pragma unroll
+                    for (int q = 0; q < S * S; ++q)
+                        cm[q] = src[q];
+                    sinkhorn_regs<S>(cm, p.iters, p.eps);
+                    float *dst = p.comb + (size_t)(t0 + lane) * S * S;
+    #pragma unroll
+                    for (int q = 0; q < S * S; ++q)
+                        dst[q] = cm[q];
+                }
+                __syncwarp();
+                if (lane == 0)
+                    ptx::mbar_arrive(BAR(kBarSinkDone));   // the buffer may be refilled
+            }
+        } else if (PERSIST && warp >= kCollapseWarp0) {
+            // -------------------------------------------------------------- collapse warps
+            // Tile by tile: wait for the owners' pre gates, write y for this CTA's hidden
+            // columns from the tile's stage, then refill the stage with tile it + nst.  The
+            // compute warps never wait for gates; only the stage ring links them to these.
+            const int ct = threadIdx.x - kCollapseWarp0 * 32;
+            const int h4n = p.hs / 4;
+            constexpr int U = 2;   // outputs per thread in flight
+            for (int it = 0; tile_exists(it); ++it) {
+                const int q = it % kNQ;
+                int t0, tm;
+                tile_tokens(it, t0, tm);
+                bool got = true;
+                if (ct == 0) {   // the owners answer with tm pre gates
+                    ptx::mbar_arrive_expect_tx(BAR(kBarPre + q), (uint32_t)(tm * 16));
+                    got = wait_bar<true>(BAR(kBarPre + q), (it / kNQ) & 1, abort_flag, sb, kSitePre);
+                }
+                if (!ptx::named_bar_and(kNbCollapse, kCollapseThreads, got))
+                    break;
+                const uint32_t xs_base = ptx::smem_u32(stages + (it % L.nst) * stage_floats);
+                const uint32_t pre_base = ptx::smem_u32(preb + q * kTMT * 4);
+                const int n = tm * h4n;
+                for (int e0 = ct; e0 < n; e0 += U * kCollapseThreads) {
+                    float4 xv[U][S];
+                    float pr[U][4];
+    #pragma unroll
+                    for (int u = 0; u < U; ++u) {
+                        const int e = min(e0 + kCollapseThreads * u, n - 1);
+                        const int t = e / h4n, h4 = e - t * h4n;
+                        const float4 pv = ptx::lds128(pre_base + 16u * (uint32_t)t);
+                        pr[u][0] = pv.x;
+                        pr[u][1] = pv.y;
+                        pr[u][2] = pv.z;
+                        pr[u][3] = pv.w;
+    #pragma unroll
+                        for (int k = 0; k < S; ++k)
+                            xv[u][k] = ptx::lds128(xs_base + 4u * (uint32_t)(t * p.LK + k * p.hs + 4 * h4));
+                    }
+    #pragma unroll
+                    for (int u = 0; u < U; ++u) {
+                        const int e = e0 + kCollapseThreads * u;
+                        if (e >= n)
+                            break;
+                        const int t = e / h4n, h4 = e - t * h4n;
+                        float4 a = make_float4(pr[u][0] * xv[u][0].x, pr[u][0] * xv[u][0].y, pr[u][0] * xv[u][0].z,
+                                               pr[u][0] * xv[u][0].w);
+    #pragma unroll
+                        for (int k = 1; k < S; ++k) {
+                            a.x = fmaf(pr[u][k], xv[u][k].x, a.x);
+                            a.y = fmaf(pr[u][k], xv[u][k].y, a.y);
+                            a.z = fmaf(pr[u][k], xv[u][k].z, a.z);
+                            a.w = fmaf(pr[u][k], xv[u][k].w, a.w);
+                        }
+                        *reinterpret_cast<float4 *>(p.y + (size_t)(t0 + t) * p.d + (size_t)rank * p.hs + 4 * h4) = a;
+                    }
+                }
+                ptx::named_bar_sync(kNbCollapse, kCollapseThreads);
+                if (ct == 0 && tile_exists(it + L.nst))
+                    load_tile(it + L.nst);
+            }
         }
-    }
-      __syncwarp();
-      ptx::setmaxnreg_inc<128>();
     }
 
     // ------------------------------------------------------------------ teardown
@@ -794,7 +795,7 @@ struct VariantInfo {
     int max_clusters = 0;
 };
 
-template <int S, bool PERSIST, int NT>
+template <int S, bool PERSIST, int NT, bool HEAD>
 int max_clusters_for(int device)
 {
     static std::mutex mu;
@@ -805,8 +806,8 @@ int max_clusters_for(int device)
     VariantInfo &vi = info[device];
     if (!vi.init) {
         vi.init = true;
-        const Lay L = make_lay<S, PERSIST>(kMaxLK);
-        auto kern = hc_pre_cluster_kernel<S, PERSIST, NT>;
+        const Lay L = make_lay<S, PERSIST, HEAD>(kMaxLK);
+        auto kern = hc_pre_cluster_kernel<S, PERSIST, NT, HEAD>;
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L.total) != cudaSuccess ||
             cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
             cudaGetLastError();
@@ -833,12 +834,12 @@ int max_clusters_for(int device)
     return vi.max_clusters;
 }
 
-template <int S, bool PERSIST, int NT>
+template <int S, bool PERSIST, int NT, bool HEAD>
 cudaError_t launch_variant(const Params &p, int nclusters, cudaStream_t st)
 {
     // A persistent CTA allocates all 512 TMEM columns, so it must be alone on its
     // SM: reserve the largest shared-memory footprint whatever the shape.
-    const Lay L = make_lay<S, PERSIST>(PERSIST ? kMaxLK : p.LK);
+    const Lay L = make_lay<S, PERSIST, HEAD>(PERSIST ? kMaxLK : p.LK);
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute at[1];
     at[0].id = cudaLaunchAttributeClusterDimension;
@@ -851,15 +852,15 @@ cudaError_t launch_variant(const Params &p, int nclusters, cudaStream_t st)
     cfg.stream = st;
     cfg.attrs = at;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, hc_pre_cluster_kernel<S, PERSIST, NT>, p);
+    return cudaLaunchKernelEx(&cfg, hc_pre_cluster_kernel<S, PERSIST, NT, HEAD>, p);
 }
 
-template <int S>
+template <int S, bool HEAD>
 bool supported_s(int device)
 {
-    return max_clusters_for<S, true, 8>(device) > 0 && max_clusters_for<S, false, 1>(device) > 0 &&
-           max_clusters_for<S, false, 2>(device) > 0 && max_clusters_for<S, false, 4>(device) > 0 &&
-           max_clusters_for<S, false, 8>(device) > 0;
+    return max_clusters_for<S, true, 8, HEAD>(device) > 0 && max_clusters_for<S, false, 1, HEAD>(device) > 0 &&
+           max_clusters_for<S, false, 2, HEAD>(device) > 0 && max_clusters_for<S, false, 4, HEAD>(device) > 0 &&
+           max_clusters_for<S, false, 8, HEAD>(device) > 0;
 }
 
 // cuTensorMapEncodeTiled through the runtime's driver entry point (no libcuda link).
@@ -906,7 +907,7 @@ bool encode_slab_map(CUtensorMap *m, const float *base, int rows, int s, int d, 
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int S>
+template <int S, bool HEAD>
 cudaError_t run_s(const float *x, const float *fn_w, const float *scale, const float *base, int T,
                   int d, int iters, float eps, float *pre, float *post, float *comb, float *y,
                   void *workspace, cudaStream_t st, int device)
@@ -931,8 +932,8 @@ cudaError_t run_s(const float *x, const float *fn_w, const float *scale, const f
     p.eps = eps;
     p.invK = 1.0f / (float)(S * d);
     // Every decode instantiation has the same footprint; NT = 8 bounds the others.
-    const int nc_decode = max_clusters_for<S, false, 8>(device);
-    const int nc_persist = max_clusters_for<S, true, 8>(device);
+    const int nc_decode = max_clusters_for<S, false, 8, HEAD>(device);
+    const int nc_persist = max_clusters_for<S, true, 8, HEAD>(device);
     if (nc_decode < 1 || nc_persist < 1)
         return cudaErrorNotSupported;
     const bool decode = T <= nc_decode * kTMT;
@@ -941,19 +942,19 @@ cudaError_t run_s(const float *x, const float *fn_w, const float *scale, const f
     p.tm_tile = decode ? (T + nc_decode - 1) / nc_decode : kTMT;
     p.ntiles = (T + p.tm_tile - 1) / p.tm_tile;
     if (!encode_slab_map(&p.tmap_x, x, T, S, d, p.hs, p.hsc, p.tm_tile) ||
-        !encode_slab_map(&p.tmap_w, fn_w, CG<S>::R, S, d, p.hs, p.hsc, CG<S>::R))
+        !encode_slab_map(&p.tmap_w, fn_w, CG<S, HEAD>::R, S, d, p.hs, p.hsc, CG<S, HEAD>::R))
         return cudaErrorInvalidValue;
     if (decode) {
         // The token-slot count is the smallest that holds a tile.
         if (p.tm_tile <= 2)
-            return launch_variant<S, false, 1>(p, p.ntiles, st);
+            return launch_variant<S, false, 1, HEAD>(p, p.ntiles, st);
         if (p.tm_tile <= 4)
-            return launch_variant<S, false, 2>(p, p.ntiles, st);
+            return launch_variant<S, false, 2, HEAD>(p, p.ntiles, st);
         if (p.tm_tile <= 8)
-            return launch_variant<S, false, 4>(p, p.ntiles, st);
-        return launch_variant<S, false, 8>(p, p.ntiles, st);
+            return launch_variant<S, false, 4, HEAD>(p, p.ntiles, st);
+        return launch_variant<S, false, 8, HEAD>(p, p.ntiles, st);
     }
-    return launch_variant<S, true, 8>(p, min(p.ntiles, nc_persist), st);
+    return launch_variant<S, true, 8, HEAD>(p, min(p.ntiles, nc_persist), st);
 }
 
 }  // namespace
@@ -966,7 +967,7 @@ bool cluster_shape_ok(int s, int d)
     return LK % 64 == 0 && LK <= kMaxLK && slice_chunks(d / kCS) > 0;
 }
 
-bool cluster_supported(int s, int d)
+bool cluster_supported(int s, int d, bool head)
 {
     if (!cluster_shape_ok(s, d))
         return false;
@@ -974,13 +975,15 @@ bool cluster_supported(int s, int d)
     if (!device_info(di) || di.cc_major != 10)
         return false;
     switch (s) {
-    case 1: return supported_s<1>(di.device);
-    case 2: return supported_s<2>(di.device);
-    case 3: return supported_s<3>(di.device);
-    case 4: return supported_s<4>(di.device);
+    case 1: return head ? supported_s<1, true>(di.device) : supported_s<1, false>(di.device);
+    case 2: return head ? supported_s<2, true>(di.device) : supported_s<2, false>(di.device);
+    case 3: return head ? supported_s<3, true>(di.device) : supported_s<3, false>(di.device);
+    case 4: return head ? supported_s<4, true>(di.device) : supported_s<4, false>(di.device);
     default: return false;
     }
 }
+
+bool cluster_supported(int s, int d) { return cluster_supported(s, d, false); }
 
 cudaError_t launch_pre_cluster(const float *x, const float *fn_w, const float *scale,
                                const float *base, int T, int s, int d, int iters, float eps,
@@ -991,10 +994,30 @@ cudaError_t launch_pre_cluster(const float *x, const float *fn_w, const float *s
     if (!device_info(di))
         return cudaErrorNoDevice;
     switch (s) {
-    case 1: return run_s<1>(x, fn_w, scale, base, T, d, iters, eps, pre, post, comb, y, workspace, st, di.device);
-    case 2: return run_s<2>(x, fn_w, scale, base, T, d, iters, eps, pre, post, comb, y, workspace, st, di.device);
-    case 3: return run_s<3>(x, fn_w, scale, base, T, d, iters, eps, pre, post, comb, y, workspace, st, di.device);
-    case 4: return run_s<4>(x, fn_w, scale, base, T, d, iters, eps, pre, post, comb, y, workspace, st, di.device);
+#define HC_CASE(S)                                                                                  \
+    case S:                                                                                         \
+        return run_s<S, false>(x, fn_w, scale, base, T, d, iters, eps, pre, post, comb, y, workspace, st, \
+                               di.device);
+        HC_CASE(1) HC_CASE(2) HC_CASE(3) HC_CASE(4)
+#undef HC_CASE
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t launch_head_cluster(const float *x, const float *fn_w, const float *scale,
+                                const float *base, int T, int s, int d, float eps, float *gates,
+                                float *y, void *workspace, cudaStream_t st)
+{
+    DeviceInfo di;
+    if (!device_info(di))
+        return cudaErrorNoDevice;
+    switch (s) {
+#define HC_CASE(S)                                                                                  \
+    case S:                                                                                         \
+        return run_s<S, true>(x, fn_w, scale, base, T, d, 1, eps, gates, nullptr, nullptr, y, workspace, \
+                              st, di.device);
+        HC_CASE(1) HC_CASE(2) HC_CASE(3) HC_CASE(4)
+#undef HC_CASE
     default: return cudaErrorInvalidValue;
     }
 }

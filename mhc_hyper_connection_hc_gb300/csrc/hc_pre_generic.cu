@@ -1,4 +1,6 @@
 // hc_pre_generic.cu -- the generic pre-chain path: any 1 <= s <= 8, d % 4 == 0.
+// The same two kernels, with HEAD set, serve the gated-head trunk exit (rows =
+// streams, one scale, pre-style gates and the collapse; no post, no Sinkhorn).
 //
 // Two launches per site:
 //   1. mixes_partial_kernel: for a tile of kTM tokens and one slice of the
@@ -29,10 +31,11 @@ constexpr int kKC = 128;           // columns per K chunk staged in shared memor
 constexpr int kTargetCtas = 304;   // split-K sizing: two CTAs per SM of a 152-SM GB300
 constexpr int kFinishThreads = 256;
 
-template <int S>
+// HEAD: the gated-head trunk exit (rows = streams, pre-style gates only).
+template <int S, bool HEAD = false>
 struct Geo {
-    static constexpr int R = (2 + S) * S;
-    static constexpr int NW = S + 2;             // one warp per row group of S rows
+    static constexpr int R = HEAD ? S : (2 + S) * S;
+    static constexpr int NW = R / S;             // one warp per row group of S rows
     static constexpr int NT = 32 * NW;
     static constexpr int XS = kTM * kKC;         // floats of x per stage
     static constexpr int WS = R * kKC;           // floats of fn_w per stage
@@ -76,12 +79,12 @@ __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_gr
 // lane & 15 is the K-group, which owns float4 columns kg and kg+16 of every
 // 128-column chunk.  Per chunk a thread does 2 x 8 x S x 4 FMAs from 2*(8+S)
 // 128-bit shared loads; warp 0 also accumulates the sums of squares.
-template <int S>
-__global__ void __launch_bounds__(Geo<S>::NT)
+template <int S, bool HEAD>
+__global__ void __launch_bounds__(Geo<S, HEAD>::NT)
 mixes_partial_kernel(const float *__restrict__ x, const float *__restrict__ fn_w, int T, int K,
                      int nck, int ck_per, float *__restrict__ part)
 {
-    using G = Geo<S>;
+    using G = Geo<S, HEAD>;
     extern __shared__ float4 smem4[];
     float *sm = reinterpret_cast<float *>(smem4);
     const int t0 = blockIdx.x * kTM;
@@ -191,8 +194,82 @@ mixes_partial_kernel(const float *__restrict__ x, const float *__restrict__ fn_w
     }
 }
 
-// One block per token: reduce the K slices, gates, Sinkhorn, collapse.
+// Sinkhorn of one token (warp 0 of its block): lane j < S holds row j of
+// exp(comb logits); every round divides rows, then columns, by (sum + eps).
 template <int S>
+__device__ __forceinline__ void sinkhorn_comb(const float *mix, float rinv, const float *__restrict__ scale,
+                                              const float *__restrict__ base, int iters, float eps, int lane,
+                                              float *cm, float *cinv, float *__restrict__ comb_t)
+{
+    float c[S];
+    if (lane < S) {
+#pragma unroll
+        for (int k = 0; k < S; ++k) {
+            const int r = 2 * S + lane * S + k;
+            c[k] = expf(mix[r] * rinv * scale[2] + base[r]);
+        }
+    }
+    for (int it = 0; it < iters; ++it) {
+        if (lane < S) {
+            float rs = 0.f;
+#pragma unroll
+            for (int k = 0; k < S; ++k)
+                rs += c[k];
+            const float inv = 1.f / (rs + eps);
+#pragma unroll
+            for (int k = 0; k < S; ++k) {
+                c[k] *= inv;
+                cm[lane * S + k] = c[k];
+            }
+        }
+        __syncwarp();
+        if (lane < S) {
+            float cs = 0.f;
+#pragma unroll
+            for (int j = 0; j < S; ++j)
+                cs += cm[j * S + lane];
+            cinv[lane] = 1.f / (cs + eps);
+        }
+        __syncwarp();
+        if (lane < S) {
+#pragma unroll
+            for (int k = 0; k < S; ++k)
+                c[k] *= cinv[k];
+        }
+        __syncwarp();
+    }
+    if (lane < S) {
+#pragma unroll
+        for (int k = 0; k < S; ++k)
+            comb_t[lane * S + k] = c[k];
+    }
+}
+
+// Collapse of one token by its whole block: y[t, :] = sum_c pre_c * x[t, c, :].
+template <int S>
+__device__ __forceinline__ void collapse_token(const float *__restrict__ x, const float *pre_s, int t, int d,
+                                               float *__restrict__ y)
+{
+    const int d4 = d / 4;
+    const float4 *xt = reinterpret_cast<const float4 *>(x + (size_t)t * S * d);
+    float4 *yt = reinterpret_cast<float4 *>(y + (size_t)t * d);
+    for (int i = threadIdx.x; i < d4; i += kFinishThreads) {
+        float4 v = xt[i];
+        float4 a = make_float4(pre_s[0] * v.x, pre_s[0] * v.y, pre_s[0] * v.z, pre_s[0] * v.w);
+#pragma unroll
+        for (int c2 = 1; c2 < S; ++c2) {
+            v = xt[(size_t)c2 * d4 + i];
+            a.x = fmaf(pre_s[c2], v.x, a.x);
+            a.y = fmaf(pre_s[c2], v.y, a.y);
+            a.z = fmaf(pre_s[c2], v.z, a.z);
+            a.w = fmaf(pre_s[c2], v.w, a.w);
+        }
+        yt[i] = a;
+    }
+}
+
+// One block per token: reduce the K slices, gates, Sinkhorn (sites), collapse.
+template <int S, bool HEAD>
 __global__ void __launch_bounds__(kFinishThreads)
 finish_collapse_kernel(const float *__restrict__ part, int nks, const float *__restrict__ x,
                        const float *__restrict__ scale, const float *__restrict__ base, int T,
@@ -200,7 +277,7 @@ finish_collapse_kernel(const float *__restrict__ part, int nks, const float *__r
                        float *__restrict__ post_out, float *__restrict__ comb_out,
                        float *__restrict__ y)
 {
-    constexpr int R = (2 + S) * S;
+    constexpr int R = Geo<S, HEAD>::R;
     __shared__ float mix[R + 1];
     __shared__ float pre_s[S];
     __shared__ float cm[S * S];
@@ -220,95 +297,38 @@ finish_collapse_kernel(const float *__restrict__ part, int nks, const float *__r
         const int lane = tid;
         // rsqrt(mean(x^2) + eps) over the whole s*d slab (rowsq_scale).
         const float rinv = rsqrtf(mix[R] / (float)(S * d) + eps);
-        if (lane < 2 * S) {
+        if (lane < (HEAD ? S : 2 * S)) {
             const float l = mix[lane] * rinv * scale[lane < S ? 0 : 1] + base[lane];
             const float sg = 1.f / (1.f + expf(-l));
             if (lane < S) {
                 const float p = sg + eps;
-                pre_out[(size_t)t * S + lane] = p;
+                if (pre_out)   // the head's gates are an optional output
+                    pre_out[(size_t)t * S + lane] = p;
                 pre_s[lane] = p;
             } else {
                 post_out[(size_t)t * S + (lane - S)] = 2.f * sg;
             }
         }
-        // Sinkhorn: lane j < S holds row j of exp(logits); every round divides
-        // rows, then columns, by (sum + eps).
-        float c[S];
-        if (lane < S) {
-#pragma unroll
-            for (int k = 0; k < S; ++k) {
-                const int r = 2 * S + lane * S + k;
-                c[k] = expf(mix[r] * rinv * scale[2] + base[r]);
-            }
-        }
-        for (int it = 0; it < iters; ++it) {
-            if (lane < S) {
-                float rs = 0.f;
-#pragma unroll
-                for (int k = 0; k < S; ++k)
-                    rs += c[k];
-                const float inv = 1.f / (rs + eps);
-#pragma unroll
-                for (int k = 0; k < S; ++k) {
-                    c[k] *= inv;
-                    cm[lane * S + k] = c[k];
-                }
-            }
-            __syncwarp();
-            if (lane < S) {
-                float cs = 0.f;
-#pragma unroll
-                for (int j = 0; j < S; ++j)
-                    cs += cm[j * S + lane];
-                cinv[lane] = 1.f / (cs + eps);
-            }
-            __syncwarp();
-            if (lane < S) {
-#pragma unroll
-                for (int k = 0; k < S; ++k)
-                    c[k] *= cinv[k];
-            }
-            __syncwarp();
-        }
-        if (lane < S) {
-#pragma unroll
-            for (int k = 0; k < S; ++k)
-                comb_out[((size_t)t * S + lane) * S + k] = c[k];
-        }
+        if (!HEAD)
+            sinkhorn_comb<S>(mix, rinv, scale, base, iters, eps, lane, cm, cinv, comb_out + (size_t)t * S * S);
     }
     __syncthreads();
-
-    const int d4 = d / 4;
-    const float4 *xt = reinterpret_cast<const float4 *>(x + (size_t)t * S * d);
-    float4 *yt = reinterpret_cast<float4 *>(y + (size_t)t * d);
-    for (int i = tid; i < d4; i += kFinishThreads) {
-        float4 v = xt[i];
-        float4 a = make_float4(pre_s[0] * v.x, pre_s[0] * v.y, pre_s[0] * v.z, pre_s[0] * v.w);
-#pragma unroll
-        for (int c2 = 1; c2 < S; ++c2) {
-            v = xt[(size_t)c2 * d4 + i];
-            a.x = fmaf(pre_s[c2], v.x, a.x);
-            a.y = fmaf(pre_s[c2], v.y, a.y);
-            a.z = fmaf(pre_s[c2], v.z, a.z);
-            a.w = fmaf(pre_s[c2], v.w, a.w);
-        }
-        yt[i] = a;
-    }
+    collapse_token<S>(x, pre_s, t, d, y);
 }
 
-template <int S>
+template <int S, bool HEAD>
 cudaError_t run_generic(const float *x, const float *fn_w, const float *scale, const float *base,
                         int T, int d, int iters, float eps, float *pre, float *post, float *comb,
                         float *y, void *workspace, cudaStream_t st)
 {
-    using G = Geo<S>;
+    using G = Geo<S, HEAD>;
     const Split sp = make_split(T, S, d);
     float *part = reinterpret_cast<float *>(static_cast<char *>(workspace) + kStatusBytes);
     static bool smem_set[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
     if (G::SMEM > 48 * 1024 && dev < 64 && !smem_set[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(mixes_partial_kernel<S>,
+        cudaError_t e = cudaFuncSetAttribute(mixes_partial_kernel<S, HEAD>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)G::SMEM);
         if (e != cudaSuccess)
@@ -316,11 +336,11 @@ cudaError_t run_generic(const float *x, const float *fn_w, const float *scale, c
         smem_set[dev] = true;
     }
     dim3 grid1(sp.nt, sp.nks);
-    mixes_partial_kernel<S><<<grid1, G::NT, G::SMEM, st>>>(x, fn_w, T, S * d, sp.nck, sp.ck_per, part);
+    mixes_partial_kernel<S, HEAD><<<grid1, G::NT, G::SMEM, st>>>(x, fn_w, T, S * d, sp.nck, sp.ck_per, part);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess)
         return e;
-    finish_collapse_kernel<S><<<T, kFinishThreads, 0, st>>>(part, sp.nks, x, scale, base, T, d, iters,
+    finish_collapse_kernel<S, HEAD><<<T, kFinishThreads, 0, st>>>(part, sp.nks, x, scale, base, T, d, iters,
                                                             eps, pre, post, comb, y);
     return cudaGetLastError();
 }
@@ -342,8 +362,24 @@ cudaError_t launch_pre_generic(const float *x, const float *fn_w, const float *s
     switch (s) {
 #define HC_CASE(S)                                                                              \
     case S:                                                                                     \
-        return run_generic<S>(x, fn_w, scale, base, T, d, iters, eps, pre, post, comb, y,      \
-                              workspace, st);
+        return run_generic<S, false>(x, fn_w, scale, base, T, d, iters, eps, pre, post, comb, y, \
+                                     workspace, st);
+        HC_CASE(1) HC_CASE(2) HC_CASE(3) HC_CASE(4) HC_CASE(5) HC_CASE(6) HC_CASE(7) HC_CASE(8)
+#undef HC_CASE
+    default:
+        return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t launch_head_generic(const float *x, const float *fn_w, const float *scale,
+                                const float *base, int T, int s, int d, float eps, float *gates,
+                                float *y, void *workspace, cudaStream_t st)
+{
+    switch (s) {
+#define HC_CASE(S)                                                                               \
+    case S:                                                                                      \
+        return run_generic<S, true>(x, fn_w, scale, base, T, d, 1, eps, gates, nullptr, nullptr, y, \
+                                    workspace, st);
         HC_CASE(1) HC_CASE(2) HC_CASE(3) HC_CASE(4) HC_CASE(5) HC_CASE(6) HC_CASE(7) HC_CASE(8)
 #undef HC_CASE
     default:

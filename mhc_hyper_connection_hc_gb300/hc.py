@@ -26,7 +26,7 @@ HC_PATH_AUTO, HC_PATH_GENERIC, HC_PATH_CLUSTER = 0, 1, 2
 
 EXPORTED = ("hc_status_string", "hc_expand", "hc_pre_workspace_bytes", "hc_workspace_init",
             "hc_workspace_status", "hc_pre_fused", "hc_pre_fused_path", "hc_pre_auto_path",
-            "hc_post", "hc_mean", "hc_pre_fused_noalloc")
+            "hc_post", "hc_mean", "hc_pre_fused_noalloc", "hc_head", "hc_head_path")
 
 
 class HcError(RuntimeError):
@@ -59,6 +59,9 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.hc_pre_fused.argtypes = pre_args
     lib.hc_pre_fused_path.argtypes = pre_args + [i]
     lib.hc_pre_fused_noalloc.argtypes = [vp, vp, vp, vp, i, i, i, i, f, vp, vp, vp, vp, vp]
+    head_args = [vp, vp, vp, vp, i, i, i, f, vp, vp, vp, sz, vp]
+    lib.hc_head.argtypes = head_args
+    lib.hc_head_path.argtypes = head_args + [i]
     for name in EXPORTED[1:]:
         if name != "hc_pre_workspace_bytes":
             getattr(lib, name).restype = i
@@ -158,6 +161,19 @@ def hc_pre_fused_noalloc(x, fn_w, scale, base, iters: int, eps: float, pre, post
         _ptr(x, "x"), _ptr(fn_w, "fn_w"), _ptr(scale, "scale"), _ptr(base, "base"), T, s, d,
         int(iters), float(eps), _ptr(pre, "pre"), _ptr(post, "post"), _ptr(comb, "comb"),
         _ptr(y, "y"), _stream(stream)))
+
+
+def hc_head(x, fn_w, scale, base, eps: float, y, workspace, gates=None, stream=None,
+            path: int | None = None) -> None:
+    """Gated-head trunk exit: x [T, s, d] -> y [T, d] (and gates [T, s] if given)."""
+    T, s, d = _shape(x)
+    args = (_ptr(x, "x"), _ptr(fn_w, "fn_w"), _ptr(scale, "scale"), _ptr(base, "base"), T, s, d,
+            float(eps), _ptr(gates, "gates"), _ptr(y, "y"), _ptr(workspace, "workspace", torch.uint8),
+            workspace.numel(), _stream(stream))
+    if path is None:
+        _check("hc_head", load().hc_head(*args))
+    else:
+        _check("hc_head_path", load().hc_head_path(*args, int(path)))
 
 
 # ----------------------------------------------------------------------------- conveniences

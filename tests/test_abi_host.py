@@ -116,3 +116,26 @@ def test_workspace_sizes(lib):
             n = hc.hc_pre_workspace_bytes(T, s, d)
             assert n >= 256 and n % 4 == 0
             assert n <= 256 + 4 * ((2 + s) * s + 1) * T * 304 + 4 * ((2 + s) * s + 1) * 304
+
+
+def head_rc(lib, x=A, fn_w=A + 32 * MB, scale=A + 40 * MB, base=A + 40 * MB + 64, gates=A + 41 * MB,
+            y=A + 42 * MB, ws=A + 64 * MB, ws_bytes=16 * MB, T=2, s=4, d=4096, eps=1e-6, path=0):
+    return lib.hc_head_path(x, fn_w, scale, base, T, s, d, eps, gates, y, ws, ws_bytes, None, path)
+
+
+def test_head_validation(lib):
+    assert head_rc(lib, eps=0.0) == hc.HC_ERR_DIM
+    assert head_rc(lib, eps=math.nan) == hc.HC_ERR_DIM
+    assert head_rc(lib, s=9) == hc.HC_ERR_DIM
+    assert head_rc(lib, path=5) == hc.HC_ERR_DIM
+    assert head_rc(lib, x=0) == hc.HC_ERR_NULL
+    assert head_rc(lib, y=0) == hc.HC_ERR_NULL
+    assert head_rc(lib, fn_w=A + 8) == hc.HC_ERR_ALIGN
+    assert head_rc(lib, gates=A + 41 * MB + 2) == hc.HC_ERR_ALIGN
+    assert head_rc(lib, d=4094) == hc.HC_ERR_ALIGN
+    assert head_rc(lib, y=A + 256) == hc.HC_ERR_ALIAS                 # y inside x
+    assert head_rc(lib, gates=A + 42 * MB + 4) == hc.HC_ERR_ALIAS     # gates inside y
+    assert head_rc(lib, ws=0) == hc.HC_ERR_WORKSPACE
+    assert head_rc(lib, ws_bytes=16) == hc.HC_ERR_WORKSPACE
+    assert head_rc(lib, ws=A + 42 * MB) == hc.HC_ERR_ALIAS            # workspace over y
+    assert head_rc(lib, T=0, x=0) == hc.HC_OK                         # empty batch
