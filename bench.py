@@ -341,6 +341,8 @@ def run_gpu(args):
             "kernels": kernels, "gpu_launches": (pre_launches + 1) * K, "clocks": clocks,
             "kernel_sources": src_hash}
 
+    if not args.no_head:
+        line["exit_head"] = measure_head(w, dv, ws, stream, peak)
     if not args.no_e2e:
         line["e2e"] = measure_e2e(w, dv, ws, out, x_out, stream, K, pre, post)
     if not args.no_decode:
@@ -388,6 +390,40 @@ def measure_e2e(w, dv, ws, out, x_out, stream, K, pre, post):
     sec = e0.elapsed_time(e1) / 1e3
     return {"value": w.T * K / sec, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": 1e3 * sec / K}
+
+
+def measure_head(w, dv, ws, stream, peak, reps: int = 20):
+    """The gated-head trunk exit (hc_head) on the step's stream state, outside the
+    timed step: mean of `reps` event-timed launches after 3 warm-up launches."""
+    import torch
+    from mhc_hyper_connection_hc_gb300 import hc
+    T, s, d = w.T, w.s, w.d
+    hw, hs, hb = synth.head_params(w.cid, s, d)
+    with torch.cuda.stream(stream):
+        hw, hs, hb = (torch.from_numpy(a).to(dv["x"].device) for a in (hw, hs, hb))
+        gates = torch.empty(T, s, device=dv["x"].device)
+        y = torch.empty(T, d, device=dv["x"].device)
+
+    def head():
+        hc.hc_head(dv["x"], hw, hs, hb, w.eps, y, ws, gates=gates, stream=stream)
+
+    for _ in range(3):
+        head()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    for e0, e1 in ev:
+        e0.record(stream)
+        head()
+        e1.record(stream)
+    stream.synchronize()
+    if hc.hc_workspace_status(ws, stream) != 0:
+        raise RuntimeError("the head kernel flagged an error")
+    us = statistics.mean(e0.elapsed_time(e1) for e0, e1 in ev) * 1e3
+    nbytes = T * s * d * 4 + T * d * 4   # x read once, y written
+    gbs = nbytes / us / 1e3
+    path = hc.HC_PATH_CLUSTER if hc.hc_pre_auto_path(T, s, d) == hc.HC_PATH_CLUSTER else hc.HC_PATH_GENERIC
+    return {"us": us, "algorithmic_bytes": nbytes, "GB/s": gbs, "frac_hbm": gbs / peak,
+            "path": "cluster" if path == hc.HC_PATH_CLUSTER else "generic",
+            "note": "gated-head trunk exit on the same state, timed separately from the step"}
 
 
 def measure_decode(dev, iters=None, n_sites: int = 300):
@@ -470,6 +506,7 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-head", action="store_true", help="skip the gated-head exit measurement")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
