@@ -177,6 +177,37 @@ int hc_post(const float *x, const float *f, const float *post, const float *comb
             float *x_out, int T, int s, int d, void *stream);
 
 /*
+ * hc_post_pre_fused -- the boundary between two sites in one call: site i's
+ * hc_post followed by site i+1's pre-chain on its result (hyper.rs module header:
+ * the post formula, then the next site's "mixes", "mixes *= rsqrt", "sinkhorn"
+ * and "y" lines; the pages' walk runs post_t1_ws -> pre_t1_ws back to back).
+ *   x_prev [T, s, d]      site i's input state (in)
+ *   f [T, d], post_prev [T, s], comb_prev [T, s, s]   site i's branch output and
+ *                          gates (in)
+ *   fn_w, scale, base     site i+1's trio, as for hc_pre_fused (in)
+ *   x_new [T, s, d]       post_prev . f + comb_prev^T x_prev, the new state (out)
+ *   pre, post, comb, y    site i+1's pre-chain outputs on x_new (out)
+ * x_new is bit-identical to hc_post's output, and pre/post/comb/y to
+ * hc_pre_fused on x_new, on the cluster path; there the new state is formed in
+ * shared memory from one read of x_prev, so it is not read back from memory.
+ * The cluster path takes the shapes hc_pre_fused's does with d <= 4096; other
+ * shapes run hc_post then the generic pre-chain.  Outputs must not overlap
+ * any input or each other; workspace as for hc_pre_fused.
+ */
+int hc_post_pre_fused(const float *x_prev, const float *f, const float *post_prev,
+                      const float *comb_prev, const float *fn_w, const float *scale,
+                      const float *base, int T, int s, int d, int iters, float eps,
+                      float *x_new, float *pre, float *post, float *comb, float *y,
+                      void *workspace, size_t ws_bytes, void *stream);
+
+/* hc_post_pre_fused with an explicit kernel path (enum hc_pre_path). */
+int hc_post_pre_fused_path(const float *x_prev, const float *f, const float *post_prev,
+                           const float *comb_prev, const float *fn_w, const float *scale,
+                           const float *base, int T, int s, int d, int iters, float eps,
+                           float *x_new, float *pre, float *post, float *comb, float *y,
+                           void *workspace, size_t ws_bytes, void *stream, int path);
+
+/*
  * hc_head -- gated-head trunk exit [T, s, d] -> [T, d] (hyper.rs `collapse`, case
  * HcCollapse::GatedHead: the head trio of HyperHead::load -- fn_w with rows equal
  * to the streams, base [s] and ONE scale -- then rowsq_scale, hc_head_pre and

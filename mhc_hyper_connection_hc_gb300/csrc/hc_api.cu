@@ -228,6 +228,75 @@ int hc_pre_fused_path(const float *x, const float *fn_w, const float *scale, con
                                           comb, y, workspace, st));
 }
 
+int hc_post_pre_fused_path(const float *x_prev, const float *f, const float *post_prev,
+                           const float *comb_prev, const float *fn_w, const float *scale,
+                           const float *base, int T, int s, int d, int iters, float eps, float *x_new,
+                           float *pre, float *post, float *comb, float *y, void *workspace,
+                           size_t ws_bytes, void *stream, int path)
+{
+    if (!dims_ok(T, s, d) || iters < 1 || !(eps > 0.f) || !std::isfinite(eps))
+        return HC_ERR_DIM;
+    if (path != HC_PATH_AUTO && path != HC_PATH_GENERIC && path != HC_PATH_CLUSTER)
+        return HC_ERR_DIM;
+    if (T == 0)
+        return HC_OK;
+    if (!x_prev || !f || !post_prev || !comb_prev || !fn_w || !scale || !base || !x_new || !pre ||
+        !post || !comb || !y)
+        return HC_ERR_NULL;
+    if (d % 4 || !aligned(x_prev, 16) || !aligned(f, 16) || !aligned(x_new, 16) || !aligned(fn_w, 16) ||
+        !aligned(y, 16) || !aligned(post_prev, 4) || !aligned(comb_prev, 4) || !aligned(scale, 4) ||
+        !aligned(base, 4) || !aligned(pre, 4) || !aligned(post, 4) || !aligned(comb, 4))
+        return HC_ERR_ALIGN;
+    const int R = (2 + s) * s;
+    const size_t xb = (size_t)T * s * d * 4, fb = (size_t)T * d * 4, wb = (size_t)R * s * d * 4;
+    const size_t gb = (size_t)T * s * 4, cb = (size_t)T * s * s * 4;
+    const void *ins[7] = {x_prev, f, post_prev, comb_prev, fn_w, scale, base};
+    const size_t in_b[7] = {xb, fb, gb, cb, wb, 12, (size_t)R * 4};
+    const void *outs[5] = {x_new, pre, post, comb, y};
+    const size_t out_b[5] = {xb, gb, gb, cb, fb};
+    for (int o = 0; o < 5; ++o) {
+        for (int i = 0; i < 7; ++i)
+            if (overlap(outs[o], out_b[o], ins[i], in_b[i]))
+                return HC_ERR_ALIAS;
+        for (int o2 = o + 1; o2 < 5; ++o2)
+            if (overlap(outs[o], out_b[o], outs[o2], out_b[o2]))
+                return HC_ERR_ALIAS;
+    }
+    if (!workspace || !aligned(workspace, 16) || ws_bytes < hc_pre_workspace_bytes(T, s, d))
+        return HC_ERR_WORKSPACE;
+    for (int o = 0; o < 5; ++o)
+        if (overlap(outs[o], out_b[o], workspace, ws_bytes))
+            return HC_ERR_ALIAS;
+    for (int i = 0; i < 7; ++i)
+        if (overlap(ins[i], in_b[i], workspace, ws_bytes))
+            return HC_ERR_ALIAS;
+
+    if (path == HC_PATH_AUTO)
+        path = hc::cluster_fused_supported(s, d) ? HC_PATH_CLUSTER : HC_PATH_GENERIC;
+    cudaStream_t st = as_stream(stream);
+    if (path == HC_PATH_CLUSTER) {
+        if (!hc::cluster_fused_supported(s, d))
+            return HC_ERR_UNSUPPORTED;
+        return cuda_rc(hc::launch_post_pre_cluster(x_prev, f, post_prev, comb_prev, fn_w, scale, base, T, s, d,
+                                                   iters, eps, x_new, pre, post, comb, y, workspace, st));
+    }
+    // Shapes the fused kernel does not take: hc_post, then the generic pre-chain on its output.
+    const cudaError_t e = hc::launch_post(x_prev, f, post_prev, comb_prev, x_new, T, s, d, st);
+    if (e != cudaSuccess)
+        return HC_ERR_CUDA;
+    return cuda_rc(hc::launch_pre_generic(x_new, fn_w, scale, base, T, s, d, iters, eps, pre, post, comb, y,
+                                          workspace, st));
+}
+
+int hc_post_pre_fused(const float *x_prev, const float *f, const float *post_prev, const float *comb_prev,
+                      const float *fn_w, const float *scale, const float *base, int T, int s, int d,
+                      int iters, float eps, float *x_new, float *pre, float *post, float *comb, float *y,
+                      void *workspace, size_t ws_bytes, void *stream)
+{
+    return hc_post_pre_fused_path(x_prev, f, post_prev, comb_prev, fn_w, scale, base, T, s, d, iters, eps,
+                                  x_new, pre, post, comb, y, workspace, ws_bytes, stream, HC_PATH_AUTO);
+}
+
 int hc_head_path(const float *x, const float *fn_w, const float *scale, const float *base, int T,
                  int s, int d, float eps, float *gates, float *y, void *workspace, size_t ws_bytes,
                  void *stream, int path)

@@ -67,10 +67,19 @@ cudaError_t launch_pre_generic(const float *x, const float *fn_w, const float *s
 bool cluster_shape_ok(int s, int d);
 bool cluster_supported(int s, int d);
 bool cluster_supported(int s, int d, bool head);
+bool cluster_fused_supported(int s, int d);   // fused post -> pre: also d / 16 <= 256
 cudaError_t launch_pre_cluster(const float *x, const float *fn_w, const float *scale,
                                const float *base, int T, int s, int d, int iters, float eps,
                                float *pre, float *post, float *comb, float *y,
                                void *workspace, cudaStream_t st);
+
+// Fused post -> pre: x_new = post_prev . f + comb_prev^T x_prev, then the pre-chain of
+// the next site on x_new, in one launch of the cluster kernel.
+cudaError_t launch_post_pre_cluster(const float *x_prev, const float *f, const float *post_prev,
+                                    const float *comb_prev, const float *fn_w, const float *scale,
+                                    const float *base, int T, int s, int d, int iters, float eps,
+                                    float *x_new, float *pre, float *post, float *comb, float *y,
+                                    void *workspace, cudaStream_t st);
 
 // Gated-head trunk exit: rows = streams, one scale, gates (optional output) + collapse.
 cudaError_t launch_head_cluster(const float *x, const float *fn_w, const float *scale,

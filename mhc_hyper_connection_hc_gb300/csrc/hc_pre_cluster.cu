@@ -87,6 +87,7 @@ constexpr int kSinkLag = 8;          // a finisher waits for the Sinkhorn of the
 constexpr int kComputeThreads = kNCW * 32;
 constexpr int kNstPersist = 3;
 constexpr int kMaxLK = 1024;         // s*d/16 <= 1024: three 64 KiB stages fit in shared memory
+constexpr int kMaxFusedHs = 256;     // fused post -> pre: f slice of <= 256 columns (16 KiB a tile)
 constexpr uint32_t kTmemCols = 512;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 constexpr unsigned kFull = 0xffffffffu;
@@ -97,7 +98,8 @@ constexpr unsigned kFull = 0xffffffffu;
 // collapse of tile it released, so three slots would do; four leave a margin.
 constexpr int kNQ = 4;
 constexpr int kBarXFull = 0, kBarRecv = 3, kBarPre = kBarRecv + kNQ, kBarSink = kBarPre + kNQ,
-              kBarWFull = kBarSink + 1, kBarSinkDone = kBarWFull + 1, kNumBars = kBarSinkDone + 1;
+              kBarWFull = kBarSink + 1, kBarSinkDone = kBarWFull + 1, kBarFFull = kBarSinkDone + 1,
+              kNumBars = kBarFFull + 1;
 enum WaitSite : unsigned { kSiteWFull = 1, kSiteXFull, kSiteRecv, kSitePre, kSiteSink, kSiteDrain, kSiteSinkDone };
 
 // HEAD: the gated-head trunk exit, whose rows equal its streams (pre gates only).
@@ -122,7 +124,7 @@ struct CT {
 };
 
 struct Lay {   // shared-memory layout in bytes
-    int stage_bytes, nst, off_w, off_recv, off_pre, off_sink, off_bar, off_misc, total;
+    int stage_bytes, nst, off_w, off_recv, off_pre, off_sink, off_coef, off_f, off_bar, off_misc, total;
 };
 
 template <int S, bool PERSIST, bool HEAD>
@@ -142,9 +144,13 @@ __host__ __device__ inline Lay make_lay(int LK)
     o += kNQ * kTMT * 4 * 4;
     L.off_sink = o;                  // [16 tokens][16]: the comb blocks this CTA scales
     o += kTMT * 16 * 4;
+    L.off_coef = o;                  // [16 tokens][s + s*s]: fused post -> pre, the tile's post/comb
+    o += (kTMT * (S + S * S) * 4 + 127) / 128 * 128;
+    L.off_f = o;                     // [16 tokens][hs <= 256]: fused post -> pre, the tile's slice of f
+    o += kTMT * kMaxFusedHs * 4;
     L.off_bar = o;
     o += kNumBars * 8;
-    L.off_misc = o;                  // TMEM address, abort flag, bulk-copy phases issued per stage
+    L.off_misc = o;                  // TMEM address, abort flag, TMA loads issued per stage, f loads
     o += 32;
     L.total = o;
     return L;
@@ -156,8 +162,14 @@ struct Params {
     // column slice of n rows and every box dimension stays within TMA's 256 limit.
     CUtensorMap tmap_x;   // x: rows = tokens, box n = tm_tile
     CUtensorMap tmap_w;   // fn_w: rows = R, box n = R
+    CUtensorMap tmap_f;   // fused post -> pre: f as [T][1][d], box (hc, hsc, 1, tm_tile)
     const float *x, *fn_w, *scale, *base;
     float *pre, *post, *comb, *y;
+    // Fused post -> pre (x_new != nullptr): x holds the previous site's input state,
+    // and each tile is first turned into x' = post_prev . f + comb_prev^T x (written
+    // to x_new), on which this site's pre-chain then runs.
+    const float *f, *post_prev, *comb_prev;
+    float *x_new;
     StatusBlock *status;
     int T, d, hs, hsc, LK, NJ, iters, tm_tile, ntiles;
     float eps, invK;   // invK = 1 / (s*d)
@@ -334,6 +346,9 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const __gri
     float *recv = reinterpret_cast<float *>(smem + L.off_recv);
     float *preb = reinterpret_cast<float *>(smem + L.off_pre);
     float *sinkbuf = reinterpret_cast<float *>(smem + L.off_sink);
+    float *coefs = reinterpret_cast<float *>(smem + L.off_coef);
+    float *fbuf = reinterpret_cast<float *>(smem + L.off_f);
+    volatile int *f_issued = reinterpret_cast<volatile int *>(smem + L.off_misc + 20);
     const uint32_t bar0 = ptx::smem_u32(smem + L.off_bar);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L.off_misc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L.off_misc + 4);
@@ -360,6 +375,14 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const __gri
                          t0, BAR(kBarXFull + s));
         issued[s] = issued[s] + 1;
     };
+    // Fused post -> pre: TMA-load tile it's slice of f into the f buffer (one thread).
+    auto load_f = [&](int it) {
+        int t0, tm;
+        tile_tokens(it, t0, tm);
+        ptx::mbar_arrive_expect_tx(BAR(kBarFFull), (uint32_t)p.tm_tile * hs_bytes);
+        ptx::tma_load_4d(ptx::smem_u32(fbuf), &p.tmap_f, 0, (int)rank * p.hsc, 0, t0, BAR(kBarFFull));
+        *f_issued = *f_issued + 1;
+    };
 
     // ------------------------------------------------------------------ set-up
     if (threadIdx.x == 0) {
@@ -367,6 +390,7 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const __gri
             ptx::mbar_init(BAR(kBarXFull + s), 1);
             issued[s] = 0;
         }
+        *f_issued = 0;
         for (int q = 0; q < kNQ; ++q) {
             ptx::mbar_init(BAR(kBarRecv + q), 1);   // armed by this CTA; data by remote stores
             ptx::mbar_init(BAR(kBarPre + q), 1);
@@ -374,6 +398,7 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const __gri
         ptx::mbar_init(BAR(kBarSink), 1);
         ptx::mbar_init(BAR(kBarWFull), 1);
         ptx::mbar_init(BAR(kBarSinkDone), 1);
+        ptx::mbar_init(BAR(kBarFFull), 1);
         *abort_flag = 0;
         ptx::fence_mbar_init_cluster();
     }
@@ -415,6 +440,8 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const __gri
             ptx::tma_load_4d(ptx::smem_u32(wdst), &p.tmap_w, 0, (int)rank * p.hsc, 0, 0,
                              BAR(kBarWFull));
             load_tile(0);   // every cluster has at least one tile
+            if (p.x_new)
+                load_f(0);
         }
         bool ok = ptx::named_bar_and(
             1, kComputeThreads, threadIdx.x != 0 || wait_bar<false>(BAR(kBarWFull), 0, abort_flag, sb, kSiteWFull));
@@ -479,26 +506,108 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const __gri
         // Persistent variant: the two column halves (warpgroups) wait for tiles on
         // their own barriers, and half 1 starts once half 0 has done its first dots,
         // so one half reduces and ships while the other runs its FMAs.  The decode
-        // variant keeps all eight warps together (its collapse needs them all).
-        const uint32_t tbar = PERSIST ? kNbHalf0 + (uint32_t)half : kNbCompute;
-        const uint32_t tthreads = PERSIST ? kComputeThreads / 2 : kComputeThreads;
-        const int tpoll = PERSIST ? half * (kComputeThreads / 2) : 0;   // the thread that polls
-        bool arrived = !(PERSIST && half == 0);
-        if (PERSIST && half == 1)
+        // variant keeps all eight warps together (its collapse needs them all), and
+        // so does the fused post -> pre mode, whose tile transform needs them all.
+        const bool fused = p.x_new != nullptr;
+        const bool split = PERSIST && !fused;
+        const uint32_t tbar = split ? kNbHalf0 + (uint32_t)half : kNbCompute;
+        const uint32_t tthreads = split ? kComputeThreads / 2 : kComputeThreads;
+        const int tpoll = split ? half * (kComputeThreads / 2) : 0;   // the thread that polls
+        bool arrived = !(split && half == 0);
+        if (split && half == 1)
             ptx::named_bar_sync(kNbStagger, kComputeThreads);
         const int lk4 = p.LK * 4;
+        // Fused post -> pre: this thread's share of the next tile's post/comb (at most
+        // 16 tokens x (s + s*s) values over the 256 compute threads).
+        constexpr int NC = S + S * S;
+        constexpr int kCoefPerThread = (kTMT * NC + kComputeThreads - 1) / kComputeThreads;
+        float cpre[kCoefPerThread];
+        auto load_coefs = [&](int itn, float (&c)[kCoefPerThread]) {
+            int t0n, tmn;
+            tile_tokens(itn, t0n, tmn);
+#pragma unroll
+            for (int m = 0; m < kCoefPerThread; ++m) {
+                const int e = threadIdx.x + m * kComputeThreads;
+                c[m] = 0.f;
+                if (e < tmn * NC) {
+                    const int t = e / NC, cc = e - (e / NC) * NC;
+                    c[m] = cc < S ? __ldg(p.post_prev + (size_t)(t0n + t) * S + cc)
+                                  : __ldg(p.comb_prev + (size_t)(t0n + t) * S * S + (cc - S));
+                }
+            }
+        };
         int it = 0;
         for (; ok; ++it) {
             if (!tile_exists(it))
                 break;
             const int s = it % L.nst, u = it / L.nst;
-            ok = ptx::named_bar_and(tbar, tthreads,
-                                    (int)threadIdx.x != tpoll ||
-                                        wait_bar<false>(BAR(kBarXFull + s), u & 1, abort_flag, sb, kSiteXFull));
+            ok = ptx::named_bar_and(
+                tbar, tthreads,
+                (int)threadIdx.x != tpoll ||
+                    (wait_bar<false>(BAR(kBarXFull + s), u & 1, abort_flag, sb, kSiteXFull) &&
+                     (!fused || wait_bar<false>(BAR(kBarFFull), it & 1, abort_flag, sb, kSiteXFull))));
             if (!ok)
                 break;
             int t0, tm;
             tile_tokens(it, t0, tm);
+            if (fused) {
+                // The previous site's hc_post on this tile, in place: thread e owns the
+                // 4 columns h4 of token t in every stream, reads x_prev, writes x' (the
+                // same operations, in the same order, as hc_post_kernel).  The tile's
+                // post/comb came into registers during the previous tile (cpre), its f
+                // slice by TMA.
+                if (it == 0)
+                    load_coefs(it, cpre);
+#pragma unroll
+                for (int m = 0; m < kCoefPerThread; ++m) {
+                    const int e = threadIdx.x + m * kComputeThreads;
+                    if (e < tm * NC)
+                        coefs[e] = cpre[m];
+                }
+                ptx::named_bar_sync(kNbCompute, kComputeThreads);
+                // Thread -> (token t = tid / 16, columns h4 = tid % 16 + 16 m): one token's
+                // coefficients per thread, loaded once.
+                float *xs = stages + s * stage_floats;
+                const int h4n = p.hs / 4;
+                const int t = threadIdx.x >> 4;
+                if (t < tm) {
+                    float cf[NC];
+#pragma unroll
+                    for (int c = 0; c < NC; ++c)
+                        cf[c] = coefs[t * NC + c];
+                    for (int h4 = threadIdx.x & 15; h4 < h4n; h4 += 16) {
+                        float4 *xt = reinterpret_cast<float4 *>(xs + t * p.LK + 4 * h4);
+                        const float4 fv = *reinterpret_cast<const float4 *>(fbuf + t * p.hs + 4 * h4);
+                        float4 xv[S];
+#pragma unroll
+                        for (int j = 0; j < S; ++j)
+                            xv[j] = xt[j * h4n];
+#pragma unroll
+                        for (int k = 0; k < S; ++k) {
+                            const float pk = cf[k];
+                            float4 o = make_float4(pk * fv.x, pk * fv.y, pk * fv.z, pk * fv.w);
+#pragma unroll
+                            for (int j = 0; j < S; ++j) {
+                                const float cc = cf[S + j * S + k];
+                                o.x = fmaf(cc, xv[j].x, o.x);
+                                o.y = fmaf(cc, xv[j].y, o.y);
+                                o.z = fmaf(cc, xv[j].z, o.z);
+                                o.w = fmaf(cc, xv[j].w, o.w);
+                            }
+                            xt[k * h4n] = o;
+                            *reinterpret_cast<float4 *>(p.x_new + ((size_t)(t0 + t) * S + k) * p.d +
+                                                        (size_t)rank * p.hs + 4 * h4) = o;
+                        }
+                    }
+                }
+                ptx::fence_proxy_async_smem();   // the stage and the f buffer are refilled by TMA
+                ptx::named_bar_sync(kNbCompute, kComputeThreads);
+                if (tile_exists(it + 1)) {
+                    if (threadIdx.x == 0)
+                        load_f(it + 1);
+                    load_coefs(it + 1, cpre);
+                }
+            }
             const int ntok = min(NT, max(0, tm - NT * tg));
             // Byte address of token slot 0 of this half-warp, at this lane's first column group.
             const uint32_t xs_addr = ptx::smem_u32(stages + s * stage_floats + (tg * NT) * p.LK) + 16u * kg;
@@ -779,6 +888,8 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const __gri
         for (int s = 0; s < L.nst; ++s)
             if (issued[s] > 0)
                 wait_bar<false>(BAR(kBarXFull + s), (issued[s] - 1) & 1, abort_flag, sb, kSiteDrain, false);
+        if (*f_issued > 0)
+            wait_bar<false>(BAR(kBarFFull), (*f_issued - 1) & 1, abort_flag, sb, kSiteDrain, false);
     }
     __syncwarp();
     if (PERSIST) {
@@ -863,6 +974,12 @@ bool supported_s(int device)
            max_clusters_for<S, false, 8, HEAD>(device) > 0;
 }
 
+// The previous site's hc_post inputs and output, for the fused post -> pre mode.
+struct FusedPost {
+    const float *f, *post_prev, *comb_prev;
+    float *x_new;
+};
+
 // cuTensorMapEncodeTiled through the runtime's driver entry point (no libcuda link).
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
 {
@@ -910,9 +1027,15 @@ bool encode_slab_map(CUtensorMap *m, const float *base, int rows, int s, int d, 
 template <int S, bool HEAD>
 cudaError_t run_s(const float *x, const float *fn_w, const float *scale, const float *base, int T,
                   int d, int iters, float eps, float *pre, float *post, float *comb, float *y,
-                  void *workspace, cudaStream_t st, int device)
+                  void *workspace, cudaStream_t st, int device, const FusedPost *fp = nullptr)
 {
     Params p = {};
+    if (fp) {
+        p.f = fp->f;
+        p.post_prev = fp->post_prev;
+        p.comb_prev = fp->comb_prev;
+        p.x_new = fp->x_new;
+    }
     p.x = x;
     p.fn_w = fn_w;
     p.scale = scale;
@@ -941,6 +1064,8 @@ cudaError_t run_s(const float *x, const float *fn_w, const float *scale, const f
     // at once; prefill: 16-token tiles on persistent clusters.
     p.tm_tile = decode ? (T + nc_decode - 1) / nc_decode : kTMT;
     p.ntiles = (T + p.tm_tile - 1) / p.tm_tile;
+    if (p.x_new && !encode_slab_map(&p.tmap_f, p.f, T, 1, d, p.hs, p.hsc, p.tm_tile))
+        return cudaErrorInvalidValue;
     if (!encode_slab_map(&p.tmap_x, x, T, S, d, p.hs, p.hsc, p.tm_tile) ||
         !encode_slab_map(&p.tmap_w, fn_w, CG<S, HEAD>::R, S, d, p.hs, p.hsc, CG<S, HEAD>::R))
         return cudaErrorInvalidValue;
@@ -985,6 +1110,8 @@ bool cluster_supported(int s, int d, bool head)
 
 bool cluster_supported(int s, int d) { return cluster_supported(s, d, false); }
 
+bool cluster_fused_supported(int s, int d) { return d / kCS <= kMaxFusedHs && cluster_supported(s, d, false); }
+
 cudaError_t launch_pre_cluster(const float *x, const float *fn_w, const float *scale,
                                const float *base, int T, int s, int d, int iters, float eps,
                                float *pre, float *post, float *comb, float *y, void *workspace,
@@ -998,6 +1125,27 @@ cudaError_t launch_pre_cluster(const float *x, const float *fn_w, const float *s
     case S:                                                                                         \
         return run_s<S, false>(x, fn_w, scale, base, T, d, iters, eps, pre, post, comb, y, workspace, st, \
                                di.device);
+        HC_CASE(1) HC_CASE(2) HC_CASE(3) HC_CASE(4)
+#undef HC_CASE
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t launch_post_pre_cluster(const float *x_prev, const float *f, const float *post_prev,
+                                    const float *comb_prev, const float *fn_w, const float *scale,
+                                    const float *base, int T, int s, int d, int iters, float eps,
+                                    float *x_new, float *pre, float *post, float *comb, float *y,
+                                    void *workspace, cudaStream_t st)
+{
+    DeviceInfo di;
+    if (!device_info(di))
+        return cudaErrorNoDevice;
+    const FusedPost fp{f, post_prev, comb_prev, x_new};
+    switch (s) {
+#define HC_CASE(S)                                                                                  \
+    case S:                                                                                         \
+        return run_s<S, false>(x_prev, fn_w, scale, base, T, d, iters, eps, pre, post, comb, y, workspace, \
+                               st, di.device, &fp);
         HC_CASE(1) HC_CASE(2) HC_CASE(3) HC_CASE(4)
 #undef HC_CASE
     default: return cudaErrorInvalidValue;

@@ -26,7 +26,8 @@ HC_PATH_AUTO, HC_PATH_GENERIC, HC_PATH_CLUSTER = 0, 1, 2
 
 EXPORTED = ("hc_status_string", "hc_expand", "hc_pre_workspace_bytes", "hc_workspace_init",
             "hc_workspace_status", "hc_pre_fused", "hc_pre_fused_path", "hc_pre_auto_path",
-            "hc_post", "hc_mean", "hc_pre_fused_noalloc", "hc_head", "hc_head_path")
+            "hc_post", "hc_mean", "hc_pre_fused_noalloc", "hc_head", "hc_head_path",
+            "hc_post_pre_fused", "hc_post_pre_fused_path")
 
 
 class HcError(RuntimeError):
@@ -62,6 +63,9 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     head_args = [vp, vp, vp, vp, i, i, i, f, vp, vp, vp, sz, vp]
     lib.hc_head.argtypes = head_args
     lib.hc_head_path.argtypes = head_args + [i]
+    fused_args = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, vp, vp, vp, vp, vp, vp, sz, vp]
+    lib.hc_post_pre_fused.argtypes = fused_args
+    lib.hc_post_pre_fused_path.argtypes = fused_args + [i]
     for name in EXPORTED[1:]:
         if name != "hc_pre_workspace_bytes":
             getattr(lib, name).restype = i
@@ -161,6 +165,22 @@ def hc_pre_fused_noalloc(x, fn_w, scale, base, iters: int, eps: float, pre, post
         _ptr(x, "x"), _ptr(fn_w, "fn_w"), _ptr(scale, "scale"), _ptr(base, "base"), T, s, d,
         int(iters), float(eps), _ptr(pre, "pre"), _ptr(post, "post"), _ptr(comb, "comb"),
         _ptr(y, "y"), _stream(stream)))
+
+
+def hc_post_pre_fused(x_prev, f, post_prev, comb_prev, fn_w, scale, base, iters: int, eps: float,
+                      x_new, pre, post, comb, y, workspace, stream=None, path: int | None = None) -> None:
+    """Site i's hc_post and site i+1's pre-chain in one call: x_new = post_prev . f +
+    comb_prev^T x_prev, then pre/post/comb/y of the next site on x_new."""
+    T, s, d = _shape(x_prev)
+    args = (_ptr(x_prev, "x_prev"), _ptr(f, "f"), _ptr(post_prev, "post_prev"),
+            _ptr(comb_prev, "comb_prev"), _ptr(fn_w, "fn_w"), _ptr(scale, "scale"), _ptr(base, "base"),
+            T, s, d, int(iters), float(eps), _ptr(x_new, "x_new"), _ptr(pre, "pre"), _ptr(post, "post"),
+            _ptr(comb, "comb"), _ptr(y, "y"), _ptr(workspace, "workspace", torch.uint8),
+            workspace.numel(), _stream(stream))
+    if path is None:
+        _check("hc_post_pre_fused", load().hc_post_pre_fused(*args))
+    else:
+        _check("hc_post_pre_fused_path", load().hc_post_pre_fused_path(*args, int(path)))
 
 
 def hc_head(x, fn_w, scale, base, eps: float, y, workspace, gates=None, stream=None,

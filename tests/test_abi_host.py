@@ -139,3 +139,31 @@ def test_head_validation(lib):
     assert head_rc(lib, ws_bytes=16) == hc.HC_ERR_WORKSPACE
     assert head_rc(lib, ws=A + 42 * MB) == hc.HC_ERR_ALIAS            # workspace over y
     assert head_rc(lib, T=0, x=0) == hc.HC_OK                         # empty batch
+
+
+def fused_rc(lib, T=2, s=4, d=4096, iters=20, eps=1e-6, path=0, **over):
+    p = dict(x_prev=A, f=A + 8 * MB, post_prev=A + 9 * MB, comb_prev=A + 9 * MB + 4096,
+             fn_w=A + 10 * MB, scale=A + 12 * MB, base=A + 12 * MB + 64, x_new=A + 13 * MB,
+             pre=A + 14 * MB, post=A + 14 * MB + 4096, comb=A + 14 * MB + 8192, y=A + 15 * MB,
+             ws=A + 64 * MB)
+    p.update(over)
+    ws_bytes = p.pop("ws_bytes", 16 * MB)
+    return lib.hc_post_pre_fused_path(p["x_prev"], p["f"], p["post_prev"], p["comb_prev"], p["fn_w"],
+                                      p["scale"], p["base"], T, s, d, iters, eps, p["x_new"], p["pre"],
+                                      p["post"], p["comb"], p["y"], p["ws"], ws_bytes, None, path)
+
+
+def test_post_pre_fused_validation(lib):
+    assert fused_rc(lib, iters=0) == hc.HC_ERR_DIM
+    assert fused_rc(lib, eps=0.0) == hc.HC_ERR_DIM
+    assert fused_rc(lib, path=9) == hc.HC_ERR_DIM
+    assert fused_rc(lib, f=0) == hc.HC_ERR_NULL
+    assert fused_rc(lib, x_new=0) == hc.HC_ERR_NULL
+    assert fused_rc(lib, f=A + 8 * MB + 4) == hc.HC_ERR_ALIGN
+    assert fused_rc(lib, comb_prev=A + 9 * MB + 4098) == hc.HC_ERR_ALIGN
+    assert fused_rc(lib, x_new=A) == hc.HC_ERR_ALIAS                   # in place refused
+    assert fused_rc(lib, y=A + 8 * MB) == hc.HC_ERR_ALIAS              # y over f
+    assert fused_rc(lib, pre=A + 13 * MB + 64) == hc.HC_ERR_ALIAS      # pre inside x_new
+    assert fused_rc(lib, ws_bytes=16) == hc.HC_ERR_WORKSPACE
+    assert fused_rc(lib, ws=A + 13 * MB) == hc.HC_ERR_ALIAS            # workspace over x_new
+    assert fused_rc(lib, T=0, x_prev=0) == hc.HC_OK
