@@ -270,6 +270,21 @@ def run_gpu(args):
     stream.synchronize()
     path = hc.hc_pre_auto_path(T, s, d)
     pre_launches = 1 if path == hc.HC_PATH_CLUSTER else 2
+    fused = args.pipeline == "fused"
+    fused_cluster = path == hc.HC_PATH_CLUSTER and d // 16 <= 256   # else hc_post + generic pre
+    if fused:
+        # The previous site's gates (this trio on this state, computed once) and the
+        # new state: a step is site i's hc_post fused with site i+1's pre-chain.
+        with torch.cuda.stream(stream):
+            hc.hc_pre_fused(dv["x"], dv["fn_w"], dv["scale"], dv["base"], iters, w.eps, out["pre"],
+                            out["post"], out["comb"], out["y"], ws, stream)
+            post_prev, comb_prev = out["post"].clone(), out["comb"].clone()
+        stream.synchronize()
+
+    def boundary():
+        hc.hc_post_pre_fused(dv["x"], dv["f"], post_prev, comb_prev, dv["fn_w"], dv["scale"], dv["base"],
+                             iters, w.eps, x_out, out["pre"], out["post"], out["comb"], out["y"], ws,
+                             stream)
 
     def pre():
         hc.hc_pre_fused(dv["x"], dv["fn_w"], dv["scale"], dv["base"], iters, w.eps, out["pre"],
@@ -287,22 +302,44 @@ def run_gpu(args):
 
     K = args.steps
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    if fused:
+        for _ in range(args.warmup):
+            boundary()
+        stream.synchronize()
     barrier()
     torch.cuda.synchronize(dev)
     with ClockSampler(dev.index if dev.index is not None else 0) as clk:
         for k in range(K):
             ev[k][0].record(stream)
-            pre()
-            ev[k][1].record(stream)
-            post()
+            if fused:
+                boundary()
+                ev[k][1].record(stream)
+            else:
+                pre()
+                ev[k][1].record(stream)
+                post()
             ev[k][2].record(stream)
         stream.synchronize()
     torch.cuda.synchronize(dev)
     barrier()
     clocks = clk.summary()
     total_s = ev[0][0].elapsed_time(ev[-1][2]) / 1e3
-    pre_ms = [ev[k][0].elapsed_time(ev[k][1]) for k in range(K)]
-    post_ms = [ev[k][1].elapsed_time(ev[k][2]) for k in range(K)]
+    if fused:
+        fused_ms = [ev[k][0].elapsed_time(ev[k][1]) for k in range(K)]
+        # the two separate launches, timed after the step loop for context
+        ev2 = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+        for k in range(K):
+            ev2[k][0].record(stream)
+            pre()
+            ev2[k][1].record(stream)
+            post()
+            ev2[k][2].record(stream)
+        stream.synchronize()
+        pre_ms = [ev2[k][0].elapsed_time(ev2[k][1]) for k in range(K)]
+        post_ms = [ev2[k][1].elapsed_time(ev2[k][2]) for k in range(K)]
+    else:
+        pre_ms = [ev[k][0].elapsed_time(ev[k][1]) for k in range(K)]
+        post_ms = [ev[k][1].elapsed_time(ev[k][2]) for k in range(K)]
     if hc.hc_workspace_status(ws, stream) != 0:
         raise RuntimeError("a kernel flagged an error in the timed region")
     max_s, all_tokens = aggregate(total_s, float(T * K))
@@ -327,7 +364,21 @@ def run_gpu(args):
                     "GB/s": post_bytes / post_avg / 1e9, "frac_hbm": post_bytes / post_avg / 1e9 / peak,
                     "launches_per_step": 1},
     }
-    dom = max(kernels, key=lambda k: kernels[k]["us"])
+    if fused:
+        fz_avg = statistics.mean(fused_ms) / 1e3
+        fz_bytes = T * s * d * 4 * 2 + T * d * 4 * 2   # x_prev and f read; x_new and y written
+        kernels["hc_post_pre_fused"] = {
+            "us": fz_avg * 1e6, "algorithmic_bytes": fz_bytes, "GB/s": fz_bytes / fz_avg / 1e9,
+            "frac_hbm": fz_bytes / fz_avg / 1e9 / peak,
+            "TFLOP/s": (pre_flops + 2 * (s + 1) * s * d * T) / fz_avg / 1e12,
+            "frac_fp32": (pre_flops + 2 * (s + 1) * s * d * T) / fz_avg / 1e12 / fp32_peak,
+            "launches_per_step": 1 if fused_cluster else 1 + pre_launches,
+            "path": "cluster" if fused_cluster else "generic (hc_post, then the generic pre-chain)"}
+        kernels["hc_pre_fused"]["launches_per_step"] = 0
+        kernels["hc_post"]["launches_per_step"] = 0
+        dom = "hc_post_pre_fused"
+    else:
+        dom = max(kernels, key=lambda k: kernels[k]["us"])
     kd = kernels[dom]
     roofline = {"bound": "hbm", "kernel": dom, "achieved": kd["GB/s"], "peak": peak, "unit": "GB/s",
                 "frac": kd["GB/s"] / peak, "peak_note": note,
@@ -337,14 +388,26 @@ def run_gpu(args):
     line = {"metric": METRIC, "value": all_tokens / max_s, "unit": "tokens/s", "n_gpus": world,
             "steps": K, "warmup": args.warmup, "ms_per_step": 1e3 * max_s / K,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-            "data": "synthetic", "config": workload_config(w), "roofline": roofline,
-            "kernels": kernels, "gpu_launches": (pre_launches + 1) * K, "clocks": clocks,
+            "data": "synthetic", "config": dict(workload_config(w), pipeline=args.pipeline, step=(
+                "site boundary: the previous site's hc_post fused with this site's pre-chain "
+                "(hc_post_pre_fused, one launch; the same work as hc_pre_fused + hc_post)"
+                if fused else "hc_pre_fused then hc_post")), "roofline": roofline,
+            "kernels": kernels,
+            "gpu_launches": ((1 if fused_cluster else pre_launches + 1) if fused else pre_launches + 1) * K,
+            "clocks": clocks,
             "kernel_sources": src_hash}
 
     if not args.no_head:
         line["exit_head"] = measure_head(w, dv, ws, stream, peak)
     if not args.no_e2e:
-        line["e2e"] = measure_e2e(w, dv, ws, out, x_out, stream, K, pre, post)
+        if fused:
+            line["e2e"] = measure_e2e(w, {"x": dv["x"], "f": dv["f"], "post_prev": post_prev,
+                                          "comb_prev": comb_prev}, dict(out, x_new=x_out), stream, K, boundary)
+        else:
+            def site():
+                pre()
+                post()
+            line["e2e"] = measure_e2e(w, {"x": dv["x"], "f": dv["f"]}, dict(out, x_out=x_out), stream, K, site)
     if not args.no_decode:
         line["decode_t1"] = measure_decode(dev, args.iters)
     if rank == 0 and world == 1 and not args.no_cpu:
@@ -357,24 +420,21 @@ def run_gpu(args):
     return 0
 
 
-def measure_e2e(w, dv, ws, out, x_out, stream, K, pre, post):
+def measure_e2e(w, dev_in, dev_out, stream, K, run):
     """The same step through the C ABI with HOST buffers: pinned host -> device
-    copies of x and f, the site, and the device -> host read of every output."""
+    copies of the step's inputs (dev_in), the step (run), and the device -> host
+    read of every output (dev_out)."""
     import torch
-    host_in = {k: dv[k].cpu().pin_memory() for k in ("x", "f")}
-    host_out = {"x_out": torch.empty_like(x_out, device="cpu").pin_memory()}
-    for k, v in out.items():
-        host_out[k] = torch.empty_like(v, device="cpu").pin_memory()
-    h2d = sum(t.numel() * 4 for t in host_in.values())
-    d2h = sum(t.numel() * 4 for t in host_out.values())
+    host_in = {k: v.cpu().pin_memory() for k, v in dev_in.items()}
+    host_out = {k: torch.empty_like(v, device="cpu").pin_memory() for k, v in dev_out.items()}
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = sum(t.numel() * t.element_size() for t in host_out.values())
 
     def step():
-        dv["x"].copy_(host_in["x"], non_blocking=True)
-        dv["f"].copy_(host_in["f"], non_blocking=True)
-        pre()
-        post()
-        host_out["x_out"].copy_(x_out, non_blocking=True)
-        for k, v in out.items():
+        for k, v in dev_in.items():
+            v.copy_(host_in[k], non_blocking=True)
+        run()
+        for k, v in dev_out.items():
             host_out[k].copy_(v, non_blocking=True)
 
     with torch.cuda.stream(stream):
@@ -501,6 +561,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=("gb300", "reference"), default="gb300")
     ap.add_argument("--workload", choices=tuple(WORKLOAD_IDS), default="prefill")
     ap.add_argument("--iters", type=int, default=None, help="override the workload's Sinkhorn iterations")
+    ap.add_argument("--pipeline", choices=("fused", "separate"), default="fused",
+                    help="a step is one site boundary: hc_post_pre_fused (fused) or hc_pre_fused + hc_post")
     ap.add_argument("--cpu-tokens", type=int, default=4096, help="tokens of the CPU-oracle sample")
     ap.add_argument("--ref-tokens", type=int, default=256, help="tokens per reference-arm step")
     ap.add_argument("--no-e2e", action="store_true")
