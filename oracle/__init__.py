@@ -34,7 +34,11 @@ def _load():
         lib.hco_mean.argtypes = [dp, dp, ctypes.c_long, ctypes.c_int, ctypes.c_long]
         lib.hco_head.argtypes = [dp, dp, dp, dp, ctypes.c_long, ctypes.c_int, ctypes.c_long,
                                  ctypes.c_double, dp, dp, ctypes.c_int]
-        for fn in (lib.hco_pre, lib.hco_post, lib.hco_expand, lib.hco_mean, lib.hco_head):
+        lib.hco_rms_norm.argtypes = [dp, dp, ctypes.c_long, ctypes.c_long, ctypes.c_double, dp]
+        fp = ctypes.POINTER(ctypes.c_float)
+        lib.hco_q8_blocks_f32.argtypes = [fp, ctypes.c_long, ctypes.POINTER(ctypes.c_byte), fp]
+        for fn in (lib.hco_pre, lib.hco_post, lib.hco_expand, lib.hco_mean, lib.hco_head, lib.hco_rms_norm,
+                   lib.hco_q8_blocks_f32):
             fn.restype = ctypes.c_int
         lib.hco_max_threads.restype = ctypes.c_int
         _lib = lib
@@ -108,6 +112,32 @@ def head(x, fn_w, scale, base, eps: float, threads: int | None = None):
     if rc != 0:
         raise ValueError(f"hco_head failed with code {rc}")
     return out
+
+
+def rms_norm(y, norm_w, eps_norm: float) -> np.ndarray:
+    """Branch-input norm: y [T, d], norm_w [d] -> z [T, d] (float64)."""
+    y = _f64(y)
+    T, d = y.shape
+    nw = _f64(norm_w).reshape(d)
+    z = np.empty((T, d))
+    if _load().hco_rms_norm(_p(y), _p(nw), T, d, float(eps_norm), _p(z)) != 0:
+        raise ValueError("hco_rms_norm failed")
+    return z
+
+
+def q8_blocks(z32):
+    """Q8_0 blocks of 32 along the last axis, decided in float32: z [..., n] float32 ->
+    (q int8 [..., n], scale float32 [..., n/32])."""
+    z32 = np.ascontiguousarray(np.asarray(z32), dtype=np.float32)
+    n = z32.size
+    q = np.empty(z32.shape, dtype=np.int8)
+    sc = np.empty(z32.shape[:-1] + (z32.shape[-1] // 32,), dtype=np.float32)
+    rc = _load().hco_q8_blocks_f32(z32.ctypes.data_as(ctypes.POINTER(ctypes.c_float)), n,
+                                   q.ctypes.data_as(ctypes.POINTER(ctypes.c_byte)),
+                                   sc.ctypes.data_as(ctypes.POINTER(ctypes.c_float)))
+    if rc != 0:
+        raise ValueError("hco_q8_blocks_f32 failed (the last axis must be a multiple of 32)")
+    return q, sc
 
 
 def expand(emb, s: int) -> np.ndarray:

@@ -250,6 +250,64 @@ int hco_head(const double *x, const double *fn_w, const double *scale, const dou
     return HCO_OK;
 }
 
+/*
+ * Branch-input norm of the collapse (hyper.rs module header: f = branch(rms_norm(y));
+ * the pages' fused v4z variant of the pre kernel also emits it, with an int8 pair):
+ *   z[t, i] = y[t, i] * rsqrt(mean_i(y[t, :]^2) + eps_norm) * norm_w[i]     (float64)
+ * y [T, d], norm_w [d] -> z [T, d].
+ */
+int hco_rms_norm(const double *y, const double *norm_w, long T, long d, double eps_norm, double *z)
+{
+    if (T < 0 || d < 1 || !(eps_norm >= 0.0))
+        return HCO_EINVAL;
+    for (long t = 0; t < T; ++t) {
+        const double *yt = y + t * d;
+        double ss = 0.0;
+        for (long i = 0; i < d; ++i)
+            ss += yt[i] * yt[i];
+        const double r = 1.0 / sqrt(ss / (double)d + eps_norm);
+        for (long i = 0; i < d; ++i)
+            z[t * d + i] = yt[i] * r * norm_w[i];
+    }
+    return HCO_OK;
+}
+
+/*
+ * The int8 pair of that norm, read as GGML's Q8_0 blocks of 32 values (the pages
+ * allocate an int8 [d] and a float [d/32] for it): per block, amax = max |z|,
+ * scale = amax / 127, q = round(z * (1 / scale)) (0 when scale is 0), rounding half
+ * away from zero.  These steps decide integers, so they run in float32, on float32
+ * z, in exactly this order: a float64 restatement could round a code differently.
+ * z [n] float32 (n % 32 == 0) -> q [n] int8, scale [n / 32] float32.
+ */
+int hco_q8_blocks_f32(const float *z, long n, signed char *q, float *scale)
+{
+    if (n < 0 || n % 32)
+        return HCO_EINVAL;
+    for (long b = 0; b < n / 32; ++b) {
+        const float *zb = z + b * 32;
+        float amax = 0.0f;
+        for (int i = 0; i < 32; ++i) {
+            const float a = fabsf(zb[i]);
+            if (a > amax)
+                amax = a;
+        }
+        const float sc = amax / 127.0f;
+        const float inv = sc != 0.0f ? 1.0f / sc : 0.0f;
+        scale[b] = sc;
+        for (int i = 0; i < 32; ++i) {
+            const float v = zb[i] * inv;
+            float r = roundf(v);
+            if (r > 127.0f)
+                r = 127.0f;
+            if (r < -127.0f)
+                r = -127.0f;
+            q[b * 32 + i] = (signed char)r;
+        }
+    }
+    return HCO_OK;
+}
+
 /* hc_expand (hyper.rs `expand`): every stream starts as the token's embedding. */
 int hco_expand(const double *emb, double *x, long T, int s, long d)
 {

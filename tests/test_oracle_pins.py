@@ -317,3 +317,65 @@ def test_head_rejects_bad_arguments():
         oracle.head(np.zeros((1, 2, 4)), np.zeros((2, 8)), [1.0], np.zeros(2), -1.0)
     r = oracle.head(np.zeros((0, 2, 4)), np.zeros((2, 8)), [1.0], np.zeros(2), 1e-6)
     assert r["y"].shape == (0, 4)
+
+
+# ----------------------------------------------------------------------------- branch-input norm + q8
+
+
+def test_rms_norm_closed_forms():
+    """Row [3, 4]: mean of squares 12.5, so z = [3, 4] / sqrt(12.5 + eps) * w.  A mean over the
+    wrong count, a missing sqrt or eps outside it changes these numbers."""
+    y = np.array([[3.0, 4.0], [-1.0, 1.0]])
+    w = np.array([0.5, 2.0])
+    z = oracle.rms_norm(y, w, 0.25)
+    np.testing.assert_allclose(z[0], np.array([3.0, 4.0]) / math.sqrt(12.5 + 0.25) * w, rtol=1e-15)
+    np.testing.assert_allclose(z[1], np.array([-1.0, 1.0]) / math.sqrt(1.0 + 0.25) * w, rtol=1e-15)
+
+
+def test_rms_norm_scale_invariance():
+    y = synth.branch_output(940, 0, 3, 64).astype(np.float64)
+    w = 1.0 + 0.1 * synth.branch_output(941, 0, 1, 64)[0].astype(np.float64)
+    np.testing.assert_allclose(oracle.rms_norm(7.5 * y, w, 0.0), oracle.rms_norm(y, w, 0.0), rtol=1e-14)
+    # unit mean square after the norm when w = 1 and eps = 0
+    z = oracle.rms_norm(y, np.ones(64), 0.0)
+    np.testing.assert_allclose((z ** 2).mean(axis=1), 1.0, rtol=1e-14)
+
+
+def test_q8_hand_computed_block():
+    """amax 127 gives scale 1: the codes are z rounded half away from zero."""
+    z = np.zeros(32, dtype=np.float32)
+    z[:6] = [127.0, -63.5, 0.5, -0.5, 1.5, -2.5]
+    q, sc = oracle.q8_blocks(z)
+    assert sc[0] == np.float32(1.0)
+    assert list(q[:6]) == [127, -64, 1, -1, 2, -3]
+    assert np.all(q[6:] == 0)
+
+
+def test_q8_zero_block_and_extremes():
+    z = np.zeros(64, dtype=np.float32)
+    z[32:] = synth.branch_output(942, 0, 1, 32)[0]
+    q, sc = oracle.q8_blocks(z)
+    assert sc[0] == 0 and np.all(q[:32] == 0)
+    i = int(np.argmax(np.abs(z[32:])))
+    assert abs(int(q[32 + i])) == 127 and np.all(np.abs(q) <= 127)
+
+
+def _q8_restated(z32):
+    """Independent restatement: numpy float32 for the scale and the product, exact float64
+    arithmetic for rounding half away from zero."""
+    z32 = np.asarray(z32, dtype=np.float32).reshape(-1, 32)
+    amax = np.abs(z32).max(axis=1)
+    sc = (amax / np.float32(127)).astype(np.float32)
+    inv = np.where(sc != 0, np.float32(1) / np.where(sc != 0, sc, np.float32(1)), np.float32(0)).astype(np.float32)
+    v = (z32 * inv[:, None]).astype(np.float32).astype(np.float64)
+    r = np.where(v >= 0, np.floor(v + 0.5), -np.floor(-v + 0.5))
+    return np.clip(r, -127, 127).astype(np.int8).reshape(-1), sc
+
+
+def test_q8_matches_restatement_and_bounds():
+    z = (3.0 * synth.branch_output(943, 0, 1, 4096)[0]).astype(np.float32)
+    q, sc = oracle.q8_blocks(z)
+    q2, sc2 = _q8_restated(z)
+    assert np.array_equal(sc, sc2) and np.array_equal(q, q2)
+    err = np.abs(q.astype(np.float64) * np.repeat(sc, 32) - z)
+    assert np.all(err <= 0.5 * np.repeat(sc, 32) * (1 + 1e-6) + 1e-12)
