@@ -177,6 +177,36 @@ int hc_post(const float *x, const float *f, const float *post, const float *comb
             float *x_out, int T, int s, int d, void *stream);
 
 /*
+ * hc_rms_norm_q8 -- the branch input of a site (hyper.rs module header:
+ * f = branch(rms_norm(y))), with the int8 pair the pages' fused v4z pre kernel
+ * emits beside it:
+ *   z[t, i] = y[t, i] * rsqrt(mean_i(y[t, :]^2) + eps_norm) * norm_w[i]
+ *   per block of 32 consecutive z of a token (GGML Q8_0 layout; the pages give
+ *   only the buffer shapes int8 [d] and float [d/32]):
+ *     q_scale = amax / 127,  q = round-half-away(z * (1 / q_scale)), 0 if q_scale = 0
+ *   y [T, d] (in), norm_w [d] (in), z [T, d] (out), q [T, d] int8 (out, optional),
+ *   q_scale [T, d/32] (out, optional: q and q_scale are both given or both NULL).
+ *   d % 4 == 0, and d % 32 == 0 when q is given; eps_norm >= 0 and finite.
+ *   The int8 codes are decided in IEEE float32 (divide, reciprocal, multiply,
+ *   round half away from zero) from the float32 z.
+ */
+int hc_rms_norm_q8(const float *y, const float *norm_w, int T, int d, float eps_norm,
+                   float *z, signed char *q, float *q_scale, void *stream);
+
+/*
+ * hc_pre_fused_norm -- hc_pre_fused, then hc_rms_norm_q8 on its y (two launches;
+ * the pages' v4z does both in one).  Arguments as for those two calls; z, q and
+ * q_scale must not overlap any other argument.  Everything is validated before
+ * the first launch.
+ */
+int hc_pre_fused_norm(const float *x, const float *fn_w, const float *scale, const float *base,
+                      int T, int s, int d, int iters, float eps,
+                      const float *norm_w, float eps_norm,
+                      float *pre, float *post, float *comb, float *y,
+                      float *z, signed char *q, float *q_scale,
+                      void *workspace, size_t ws_bytes, void *stream);
+
+/*
  * hc_post_pre_fused -- the boundary between two sites in one call: site i's
  * hc_post followed by site i+1's pre-chain on its result (hyper.rs module header:
  * the post formula, then the next site's "mixes", "mixes *= rsqrt", "sinkhorn"

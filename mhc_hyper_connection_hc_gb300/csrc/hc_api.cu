@@ -228,6 +228,74 @@ int hc_pre_fused_path(const float *x, const float *fn_w, const float *scale, con
                                           comb, y, workspace, st));
 }
 
+int hc_rms_norm_q8(const float *y, const float *norm_w, int T, int d, float eps_norm, float *z,
+                   signed char *q, float *q_scale, void *stream)
+{
+    if (T < 0 || d < 4 || !(eps_norm >= 0.f) || !std::isfinite(eps_norm) || (int64_t)T * d >= ((int64_t)1 << 31))
+        return HC_ERR_DIM;
+    if (T == 0)
+        return HC_OK;
+    if (!y || !norm_w || !z || (!q) != (!q_scale))
+        return HC_ERR_NULL;
+    if (d % 4 || (q && d % 32) || !aligned(y, 16) || !aligned(norm_w, 16) || !aligned(z, 16) ||
+        (q && (!aligned(q, 4) || !aligned(q_scale, 4))))
+        return HC_ERR_ALIGN;
+    const size_t yb = (size_t)T * d * 4, qb = q ? (size_t)T * d : 0, sb = q ? (size_t)T * (d / 32) * 4 : 0;
+    const void *ins[2] = {y, norm_w};
+    const size_t in_b[2] = {yb, (size_t)d * 4};
+    const void *outs[3] = {z, q, q_scale};
+    const size_t out_b[3] = {yb, qb, sb};
+    for (int o = 0; o < 3; ++o) {
+        for (int i = 0; i < 2; ++i)
+            if (overlap(outs[o], out_b[o], ins[i], in_b[i]))
+                return HC_ERR_ALIAS;
+        for (int o2 = o + 1; o2 < 3; ++o2)
+            if (overlap(outs[o], out_b[o], outs[o2], out_b[o2]))
+                return HC_ERR_ALIAS;
+    }
+    return cuda_rc(hc::launch_rms_norm_q8(y, norm_w, T, d, eps_norm, z, q, q_scale, as_stream(stream)));
+}
+
+int hc_pre_fused_norm(const float *x, const float *fn_w, const float *scale, const float *base, int T, int s,
+                      int d, int iters, float eps, const float *norm_w, float eps_norm, float *pre, float *post,
+                      float *comb, float *y, float *z, signed char *q, float *q_scale, void *workspace,
+                      size_t ws_bytes, void *stream)
+{
+    // Every argument is checked before either launch.
+    if (!(eps_norm >= 0.f) || !std::isfinite(eps_norm))
+        return HC_ERR_DIM;
+    if (T > 0) {
+        if (!norm_w || !z || (!q) != (!q_scale))
+            return HC_ERR_NULL;
+        if ((q && d % 32) || !aligned(norm_w, 16) || !aligned(z, 16) ||
+            (q && (!aligned(q, 4) || !aligned(q_scale, 4))))
+            return HC_ERR_ALIGN;
+        const int R = (2 + s) * s;
+        const size_t xb = (size_t)T * s * d * 4, yb = (size_t)T * d * 4;
+        const size_t qb = q ? (size_t)T * d : 0, sb = q ? (size_t)T * (d / 32) * 4 : 0;
+        const void *others[9] = {x, fn_w, scale, base, pre, post, comb, y, workspace};
+        const size_t other_b[9] = {xb, (size_t)R * s * d * 4, 12, (size_t)R * 4, (size_t)T * s * 4,
+                                   (size_t)T * s * 4, (size_t)T * s * s * 4, yb, ws_bytes};
+        const void *outs[3] = {z, q, q_scale};
+        const size_t out_b[3] = {yb, qb, sb};
+        for (int o = 0; o < 3; ++o) {
+            for (int i = 0; i < 9; ++i)
+                if (overlap(outs[o], out_b[o], others[i], other_b[i]))
+                    return HC_ERR_ALIAS;
+            if (overlap(outs[o], out_b[o], norm_w, (size_t)d * 4))
+                return HC_ERR_ALIAS;
+            for (int o2 = o + 1; o2 < 3; ++o2)
+                if (overlap(outs[o], out_b[o], outs[o2], out_b[o2]))
+                    return HC_ERR_ALIAS;
+        }
+    }
+    const int rc = hc_pre_fused(x, fn_w, scale, base, T, s, d, iters, eps, pre, post, comb, y, workspace, ws_bytes,
+                                stream);
+    if (rc != HC_OK || T == 0)
+        return rc;
+    return hc_rms_norm_q8(y, norm_w, T, d, eps_norm, z, q, q_scale, stream);
+}
+
 int hc_post_pre_fused_path(const float *x_prev, const float *f, const float *post_prev,
                            const float *comb_prev, const float *fn_w, const float *scale,
                            const float *base, int T, int s, int d, int iters, float eps, float *x_new,

@@ -54,6 +54,10 @@ cudaError_t launch_post(const float *x, const float *f, const float *post, const
                         float *x_out, int T, int s, int d, cudaStream_t st);
 cudaError_t launch_expand(const float *emb, float *x, int T, int s, int d, cudaStream_t st);
 cudaError_t launch_mean(const float *x, float *out, int T, int s, int d, cudaStream_t st);
+// Branch-input norm z = y * rsqrt(mean(y^2) + eps_norm) * norm_w, and optionally its
+// Q8_0 pair (q [T, d] int8, q_scale [T, d/32]); q == nullptr skips the pair.
+cudaError_t launch_rms_norm_q8(const float *y, const float *norm_w, int T, int d, float eps_norm, float *z,
+                               signed char *q, float *q_scale, cudaStream_t st);
 
 // Generic pre path: split-K mixes partials, then a per-token finish + collapse.
 size_t generic_workspace_bytes(int T, int s, int d);

@@ -27,7 +27,7 @@ HC_PATH_AUTO, HC_PATH_GENERIC, HC_PATH_CLUSTER = 0, 1, 2
 EXPORTED = ("hc_status_string", "hc_expand", "hc_pre_workspace_bytes", "hc_workspace_init",
             "hc_workspace_status", "hc_pre_fused", "hc_pre_fused_path", "hc_pre_auto_path",
             "hc_post", "hc_mean", "hc_pre_fused_noalloc", "hc_head", "hc_head_path",
-            "hc_post_pre_fused", "hc_post_pre_fused_path")
+            "hc_post_pre_fused", "hc_post_pre_fused_path", "hc_rms_norm_q8", "hc_pre_fused_norm")
 
 
 class HcError(RuntimeError):
@@ -66,6 +66,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     fused_args = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, vp, vp, vp, vp, vp, vp, sz, vp]
     lib.hc_post_pre_fused.argtypes = fused_args
     lib.hc_post_pre_fused_path.argtypes = fused_args + [i]
+    lib.hc_rms_norm_q8.argtypes = [vp, vp, i, i, f, vp, vp, vp, vp]
+    lib.hc_pre_fused_norm.argtypes = [vp, vp, vp, vp, i, i, i, i, f, vp, f, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     for name in EXPORTED[1:]:
         if name != "hc_pre_workspace_bytes":
             getattr(lib, name).restype = i
@@ -165,6 +167,28 @@ def hc_pre_fused_noalloc(x, fn_w, scale, base, iters: int, eps: float, pre, post
         _ptr(x, "x"), _ptr(fn_w, "fn_w"), _ptr(scale, "scale"), _ptr(base, "base"), T, s, d,
         int(iters), float(eps), _ptr(pre, "pre"), _ptr(post, "post"), _ptr(comb, "comb"),
         _ptr(y, "y"), _stream(stream)))
+
+
+def hc_rms_norm_q8(y, norm_w, eps_norm: float, z, q=None, q_scale=None, stream=None) -> None:
+    """Branch-input norm z = y * rsqrt(mean(y^2) + eps_norm) * norm_w, and optionally its
+    Q8_0 pair q (int8 [T, d]) and q_scale ([T, d/32])."""
+    if y.dim() != 2:
+        raise ValueError("y must be [T, d]")
+    T, d = int(y.shape[0]), int(y.shape[1])
+    _check("hc_rms_norm_q8", load().hc_rms_norm_q8(
+        _ptr(y, "y"), _ptr(norm_w, "norm_w"), T, d, float(eps_norm), _ptr(z, "z"),
+        _ptr(q, "q", torch.int8), _ptr(q_scale, "q_scale"), _stream(stream)))
+
+
+def hc_pre_fused_norm(x, fn_w, scale, base, iters: int, eps: float, norm_w, eps_norm: float, pre, post,
+                      comb, y, z, workspace, q=None, q_scale=None, stream=None) -> None:
+    """hc_pre_fused, then hc_rms_norm_q8 on its y."""
+    T, s, d = _shape(x)
+    _check("hc_pre_fused_norm", load().hc_pre_fused_norm(
+        _ptr(x, "x"), _ptr(fn_w, "fn_w"), _ptr(scale, "scale"), _ptr(base, "base"), T, s, d, int(iters),
+        float(eps), _ptr(norm_w, "norm_w"), float(eps_norm), _ptr(pre, "pre"), _ptr(post, "post"),
+        _ptr(comb, "comb"), _ptr(y, "y"), _ptr(z, "z"), _ptr(q, "q", torch.int8), _ptr(q_scale, "q_scale"),
+        _ptr(workspace, "workspace", torch.uint8), workspace.numel(), _stream(stream)))
 
 
 def hc_post_pre_fused(x_prev, f, post_prev, comb_prev, fn_w, scale, base, iters: int, eps: float,

@@ -167,3 +167,20 @@ def test_post_pre_fused_validation(lib):
     assert fused_rc(lib, ws_bytes=16) == hc.HC_ERR_WORKSPACE
     assert fused_rc(lib, ws=A + 13 * MB) == hc.HC_ERR_ALIAS            # workspace over x_new
     assert fused_rc(lib, T=0, x_prev=0) == hc.HC_OK
+
+
+def norm_rc(lib, y=A, w=A + 8 * MB, z=A + 9 * MB, q=A + 10 * MB, qs=A + 11 * MB, T=2, d=4096, eps=1e-5):
+    return lib.hc_rms_norm_q8(y, w, T, d, eps, z, q, qs, None)
+
+
+def test_rms_norm_q8_validation(lib):
+    assert norm_rc(lib, T=-1) == hc.HC_ERR_DIM
+    assert norm_rc(lib, eps=-1.0) == hc.HC_ERR_DIM
+    assert norm_rc(lib, eps=math.inf) == hc.HC_ERR_DIM
+    assert norm_rc(lib, y=0) == hc.HC_ERR_NULL
+    assert norm_rc(lib, q=0) == hc.HC_ERR_NULL                      # q without its scales
+    assert norm_rc(lib, d=4100) == hc.HC_ERR_ALIGN                  # q needs d % 32 == 0
+    assert norm_rc(lib, z=A + 9 * MB + 8) == hc.HC_ERR_ALIGN
+    assert norm_rc(lib, z=A + 64) == hc.HC_ERR_ALIAS                # z over y
+    assert norm_rc(lib, qs=A + 10 * MB + 16) == hc.HC_ERR_ALIAS     # scales over q
+    assert norm_rc(lib, T=0, y=0) == hc.HC_OK

@@ -1,0 +1,80 @@
+"""The branch-input norm and its int8 pair (hc_rms_norm_q8, hc_pre_fused_norm) against
+the oracle: z within 1e-4 of the float64 norm; the int8 codes and block scales bit for
+bit against the float32 quantiser applied to the GPU's own z (they decide integers, so
+both sides decide in the same precision)."""
+
+import numpy as np
+import pytest
+
+import oracle
+from hc_testutil import TOL, eps32, rel_err, to_np
+from mhc_hyper_connection_hc_gb300 import synth
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+def _up(a):
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).cuda()
+
+
+def _norm_w(cid, d):
+    return (1.0 + 0.25 * synth.branch_output(cid, 7, 1, d)[0]).astype(np.float32)
+
+
+@pytest.mark.parametrize("T,d", [(1, 4096), (37, 4096), (300, 7168), (5, 32), (3, 96)])
+def test_norm_q8_parity(T, d):
+    from mhc_hyper_connection_hc_gb300 import hc
+    y = (2.0 * synth.branch_output(950 + T, 0, T, d)).astype(np.float32)
+    y[0, : min(d, 64)] = 0.0                     # a zero block: scale 0, codes 0
+    w = _norm_w(950, d)
+    z = torch.empty(T, d, device="cuda")
+    q = torch.empty(T, d, dtype=torch.int8, device="cuda")
+    qs = torch.empty(T, d // 32, device="cuda")
+    hc.hc_rms_norm_q8(_up(y), _up(w), 1e-5, z, q, qs)
+    torch.cuda.synchronize()
+    want = oracle.rms_norm(y, w, eps32(1e-5))
+    assert rel_err(to_np(z), want) <= TOL
+    zq = z.cpu().numpy()
+    q_want, s_want = oracle.q8_blocks(zq)
+    assert np.array_equal(q.cpu().numpy(), q_want)
+    assert np.array_equal(qs.cpu().numpy().view(np.uint32), s_want.view(np.uint32))
+    # z alone (no pair), and reruns give the same bits
+    z2 = torch.empty_like(z)
+    hc.hc_rms_norm_q8(_up(y), _up(w), 1e-5, z2)
+    assert torch.equal(z2.view(torch.int32), z.view(torch.int32))
+
+
+@pytest.mark.parametrize("T,s,d", [(1, 4, 4096), (37, 4, 4096), (200, 4, 4096), (17, 3, 4096), (9, 8, 7168)])
+def test_pre_fused_norm_parity(T, s, d):
+    from mhc_hyper_connection_hc_gb300 import hc
+    inp = synth.site_inputs(960 + T, T, s, d, "normal" if s == 8 else "uniform")
+    w = _norm_w(960, d)
+    want = oracle.pre(inp["x"], inp["fn_w"], inp["scale"], inp["base"], 20, eps32(1e-6))
+    z_want = oracle.rms_norm(want["y"], w, eps32(1e-5))
+    ws = hc.new_workspace(T, s, d)
+    out = hc.new_pre_outputs(T, s, d)
+    z = torch.empty(T, d, device="cuda")
+    q = torch.empty(T, d, dtype=torch.int8, device="cuda")
+    qs = torch.empty(T, d // 32, device="cuda")
+    dv = {k: _up(v) for k, v in inp.items()}
+    hc.hc_pre_fused_norm(dv["x"], dv["fn_w"], dv["scale"], dv["base"], 20, 1e-6, _up(w), 1e-5, out["pre"],
+                         out["post"], out["comb"], out["y"], z, ws, q=q, q_scale=qs)
+    assert hc.hc_workspace_status(ws) == 0
+    for k in ("pre", "post", "comb", "y"):
+        assert rel_err(to_np(out[k]), want[k]) <= TOL, k
+    assert rel_err(to_np(z), z_want) <= TOL
+    q_want, s_want = oracle.q8_blocks(z.cpu().numpy())
+    assert np.array_equal(q.cpu().numpy(), q_want)
+    assert np.array_equal(qs.cpu().numpy().view(np.uint32), s_want.view(np.uint32))
+
+
+def test_norm_rejects_pair_with_ragged_blocks():
+    from mhc_hyper_connection_hc_gb300 import hc
+    y = torch.zeros(2, 36, device="cuda")
+    w = torch.ones(36, device="cuda")
+    z = torch.empty(2, 36, device="cuda")
+    hc.hc_rms_norm_q8(y, w, 1e-5, z)                                    # z alone: fine
+    with pytest.raises(hc.HcError):
+        hc.hc_rms_norm_q8(y, w, 1e-5, z, torch.empty(2, 36, dtype=torch.int8, device="cuda"),
+                          torch.empty(2, 1, device="cuda"))
