@@ -99,8 +99,10 @@ constexpr unsigned kFull = 0xffffffffu;
 constexpr int kNQ = 4;
 constexpr int kBarXFull = 0, kBarRecv = 3, kBarPre = kBarRecv + kNQ, kBarSink = kBarPre + kNQ,
               kBarWFull = kBarSink + 1, kBarSinkDone = kBarWFull + 1, kBarFFull = kBarSinkDone + 1,
-              kNumBars = kBarFFull + 1;
-enum WaitSite : unsigned { kSiteWFull = 1, kSiteXFull, kSiteRecv, kSitePre, kSiteSink, kSiteDrain, kSiteSinkDone };
+              kBarStored = kBarFFull + 1, kNumBars = kBarStored + 3;   // kBarStored: per stage
+enum WaitSite : unsigned {
+    kSiteWFull = 1, kSiteXFull, kSiteRecv, kSitePre, kSiteSink, kSiteDrain, kSiteSinkDone, kSiteStored
+};
 
 // HEAD: the gated-head trunk exit, whose rows equal its streams (pre gates only).
 template <int S, bool HEAD = false>
@@ -163,6 +165,7 @@ struct Params {
     CUtensorMap tmap_x;   // x: rows = tokens, box n = tm_tile
     CUtensorMap tmap_w;   // fn_w: rows = R, box n = R
     CUtensorMap tmap_f;   // fused post -> pre: f as [T][1][d], box (hc, hsc, 1, tm_tile)
+    CUtensorMap tmap_xnew;   // fused post -> pre: x_new, boxes as for x
     const float *x, *fn_w, *scale, *base;
     float *pre, *post, *comb, *y;
     // Fused post -> pre (x_new != nullptr): x holds the previous site's input state,
@@ -399,6 +402,8 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const __gri
         ptx::mbar_init(BAR(kBarWFull), 1);
         ptx::mbar_init(BAR(kBarSinkDone), 1);
         ptx::mbar_init(BAR(kBarFFull), 1);
+        for (int s = 0; s < kNstPersist; ++s)
+            ptx::mbar_init(BAR(kBarStored + s), 1);   // fused: the stage's x' store has read it
         *abort_flag = 0;
         ptx::fence_mbar_init_cluster();
     }
@@ -595,13 +600,15 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const __gri
                                 o.w = fmaf(cc, xv[j].w, o.w);
                             }
                             xt[k * h4n] = o;
-                            *reinterpret_cast<float4 *>(p.x_new + ((size_t)(t0 + t) * S + k) * p.d +
-                                                        (size_t)rank * p.hs + 4 * h4) = o;
                         }
                     }
                 }
-                ptx::fence_proxy_async_smem();   // the stage and the f buffer are refilled by TMA
+                ptx::fence_proxy_async_smem();   // TMA reads the stage (store) and refills it later
                 ptx::named_bar_sync(kNbCompute, kComputeThreads);
+                if (threadIdx.x == 0) {   // x' of this tile -> the new state, one TMA store
+                    ptx::tma_store_4d(&p.tmap_xnew, 0, (int)rank * p.hsc, 0, t0, ptx::smem_u32(xs));
+                    ptx::bulk_commit();
+                }
                 if (tile_exists(it + 1)) {
                     if (threadIdx.x == 0)
                         load_f(it + 1);
@@ -656,6 +663,10 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const __gri
                 ptx::named_bar_arrive(kNbStagger, kComputeThreads);
                 arrived = true;
             }
+            if (fused && threadIdx.x == 0) {   // the x' store has had the dots to read the stage
+                ptx::bulk_wait_read_all();
+                ptx::mbar_arrive(BAR(kBarStored + s));
+            }
 
             // Half-warp sums over the 16 K-groups.
             float v[C::NVP];
@@ -704,6 +715,8 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const __gri
         }
         if (!arrived)
             ptx::named_bar_arrive(kNbStagger, kComputeThreads);
+        if (fused && threadIdx.x == 0)
+            ptx::bulk_wait_all();   // every x' store complete before the CTA can exit
     } else {
         ptx::setmaxnreg_dec<kRegsAux>();
         if (warp < kSinkWarp) {
@@ -871,7 +884,9 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const __gri
                     }
                 }
                 ptx::named_bar_sync(kNbCollapse, kCollapseThreads);
-                if (ct == 0 && tile_exists(it + L.nst))
+                if (ct == 0 && tile_exists(it + L.nst) &&
+                    (!p.x_new || wait_bar<false>(BAR(kBarStored + it % L.nst), (it / L.nst) & 1, abort_flag, sb,
+                                                 kSiteStored)))
                     load_tile(it + L.nst);
             }
         }
@@ -1064,7 +1079,8 @@ cudaError_t run_s(const float *x, const float *fn_w, const float *scale, const f
     // at once; prefill: 16-token tiles on persistent clusters.
     p.tm_tile = decode ? (T + nc_decode - 1) / nc_decode : kTMT;
     p.ntiles = (T + p.tm_tile - 1) / p.tm_tile;
-    if (p.x_new && !encode_slab_map(&p.tmap_f, p.f, T, 1, d, p.hs, p.hsc, p.tm_tile))
+    if (p.x_new && (!encode_slab_map(&p.tmap_f, p.f, T, 1, d, p.hs, p.hsc, p.tm_tile) ||
+                    !encode_slab_map(&p.tmap_xnew, p.x_new, T, S, d, p.hs, p.hsc, p.tm_tile)))
         return cudaErrorInvalidValue;
     if (!encode_slab_map(&p.tmap_x, x, T, S, d, p.hs, p.hsc, p.tm_tile) ||
         !encode_slab_map(&p.tmap_w, fn_w, CG<S, HEAD>::R, S, d, p.hs, p.hsc, CG<S, HEAD>::R))

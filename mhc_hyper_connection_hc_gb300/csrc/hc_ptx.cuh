@@ -116,6 +116,21 @@ __device__ __forceinline__ float lds32(uint32_t addr)
     return v;
 }
 
+// 4-D tiled TMA store: this CTA's shared memory at `src` -> the box of `tmap` at
+// (c0, c1, c2, c3), in the thread's bulk async-group (commit / wait below).  Parts
+// of the box outside the tensor are not written.
+__device__ __forceinline__ void tma_store_4d(const void *tmap, int c0, int c1, int c2, int c3, uint32_t src)
+{
+    asm volatile("cp.async.bulk.tensor.4d.global.shared::cta.bulk_group [%0, {%1, %2, %3, %4}], [%5];" ::"l"(tmap),
+                 "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Wait until this thread's committed bulk stores have read their shared memory.
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// Wait until this thread's committed bulk stores are complete.
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 // 4-D tiled TMA load: the box of the tensor map `tmap` (a __grid_constant__
 // kernel parameter) at coordinates (c0, c1, c2, c3), innermost first, into this
 // CTA's shared memory at `dst`; completion counted in bytes on `bar`.
