@@ -19,26 +19,28 @@
 //    it processes: in tensor memory (TMEM, tcgen05.ld into registers) for the
 //    persistent prefill variant, in shared memory for the one-tile decode
 //    variant.  It is read from L2/HBM once per CTA.
-//  * Eight compute warps run the contraction.  Warp w owns rows
-//    [B*(w%4), B*(w%4)+B) (B = 6 for s = 4) and half of the column groups
-//    (w/4); in a warp, lanes 0-15 take the tile's first token slots and lanes
-//    16-31 the rest, and lane&15 is the K-group owning float4 columns kg,
-//    kg+16, ...  Operands: x from shared memory, fn_w from TMEM; packed
+//  * Eight compute warps run the contraction.  Persistent variant: warp w owns
+//    rows [B*(w&1), B*(w&1)+B) (B = 12 for s = 4), column half (w>>1)&1 and
+//    token slots [8*(w/4), 8*(w/4)+8), so every x value of a stage is read by
+//    two warps; decode variant: rows [B*(w%4), ..) (B = 6), column half w/4,
+//    every token slot.  In a warp, lanes 0-15 take the first of its token slots
+//    and lanes 16-31 the rest, and lane&15 is the K-group owning float4 columns
+//    kg, kg+16, ...  Operands: x from shared memory, fn_w from TMEM; packed
 //    float32 FMAs on CUDA cores (no TF32: the 24-row contraction is too skinny
 //    for tensor cores and must stay in f32).  A 16-lane xor reduce-scatter
 //    sums the K-groups, and each lane stores its partial dots and sums of
 //    squares straight into the owner CTA's receive buffer (token t of a tile
 //    belongs to CTA t) with st.async, which counts the bytes on the owner's
 //    mbarrier.  Then they go on to the next tile: they never wait for gates.
-//  * Persistent variant: the two column halves of the compute warps wait for
-//    tiles on their own barriers, half 1 starting a tile later than half 0,
-//    so one half reduces and ships while the other runs its FMAs.  Four
+//  * Persistent variant: the two warpgroups of compute warps wait for tiles on
+//    their own barriers, warpgroup 1 starting a tile later than warpgroup 0, so
+//    one reduces and ships while the other runs its FMAs.  Four
 //    collapse warps (one per SM sub-partition) wait for each tile's pre gates,
 //    write y for the CTA's hidden columns from the tile's stage and refill the
 //    stage, so the stage ring alone couples them to the compute warps.  The
 //    decode variant's single tile is collapsed by the compute warps.  The
 //    sixteen warps launch at 128 registers; the two compute warpgroups raise
-//    theirs to 184 with setmaxnreg while the other two drop to 72.
+//    theirs to 200 with setmaxnreg while the other two drop to 56.
 //  * Two finisher warps (even/odd tiles) of each owner sum the 2 x 16
 //    partials in a fixed tree, apply the rsqrt rescale, form the gates,
 //    broadcast pre to all 16 CTAs and write pre/post; exp(comb logits) go to
@@ -66,7 +68,6 @@ namespace {
 
 constexpr int kCS = 16;              // CTAs per cluster (non-portable cluster size)
 constexpr int kTMT = 16;             // max tokens per tile = one owner CTA per token
-constexpr int kRG = 4;               // row groups (compute warps w and w+4 share one)
 constexpr int kNCW = 8;              // compute warps: two per SM sub-partition
 constexpr int kFinisherWarp = 8;     // warps 8 and 9 take even and odd tiles
 constexpr int kSinkWarp = 10;        // the Sinkhorn of the tiles this CTA normalises
@@ -74,11 +75,11 @@ constexpr int kCollapseWarp0 = 12;   // persistent variant: warps 12-15 collapse
 constexpr int kCollapseThreads = 4 * 32;
 constexpr int kThreads = 16 * 32;    // four warpgroups, launched at 128 registers a thread
 // The two compute warpgroups take registers from the other two (whose warps wait
-// or stream shared memory): 2 x 128 x 184 + 2 x 128 x 72 = 512 x 128.  The split
+// or stream shared memory): 2 x 128 x 200 + 2 x 128 x 56 = 512 x 128.  The split
 // is made once, at the role dispatch, and kept until exit: a warpgroup that gave
 // registers back and then asked for them again could take them before the compute
 // warpgroups had theirs, and those would then wait for registers forever.
-constexpr int kRegsCompute = 184, kRegsAux = 72;
+constexpr int kRegsCompute = 200, kRegsAux = 56;
 static_assert(2 * 128 * kRegsCompute + 2 * 128 * kRegsAux == kThreads * 128, "register split");
 // Named barriers: 1 all compute warps, 2 collapse warps, 3 + h column half h of the
 // persistent variant, 5 the halves' one-off start stagger.
@@ -104,22 +105,34 @@ enum WaitSite : unsigned {
     kSiteWFull = 1, kSiteXFull, kSiteRecv, kSitePre, kSiteSink, kSiteDrain, kSiteSinkDone, kSiteStored
 };
 
+// Compute-warp map.  Warp w runs on SM sub-partition w%4, whose TMEM lane quarter it
+// reads.  Persistent variant: sub-partition q takes row group q&1 and column half q>>1,
+// and warpgroup w/4 half of the tile's token slots, so each x value of a stage is
+// read by two warps.  Decode variant (fn_w in shared memory, mostly one-token tiles):
+// four row groups (w%4) by two column halves (w/4), every warp on all token slots.
+template <bool PERSIST>
+struct WM {
+    static constexpr int RG = PERSIST ? 2 : 4;   // row groups
+    static constexpr int TW = PERSIST ? 2 : 1;   // warp token groups
+};
+
 // HEAD: the gated-head trunk exit, whose rows equal its streams (pre gates only).
-template <int S, bool HEAD = false>
+template <int S, bool HEAD = false, int RG = 4>
 struct CG {
     static constexpr int R = HEAD ? S : (2 + S) * S;
-    static constexpr int RP = (R + kRG - 1) / kRG * kRG;   // rows padded to the 4 row groups
-    static constexpr int B = RP / kRG;                      // rows per compute warp
+    static constexpr int RP = (R + RG - 1) / RG * RG;      // rows padded to the row groups
+    static constexpr int B = RP / RG;                       // rows per compute warp
     static constexpr int RV = (R + 1 + 3) / 4 * 4;          // exchange stride: R dots + sum of squares
     static constexpr int WQ = 4 * B;                        // fn_w floats per thread per column group
 };
 
-// NT = token slots per half-warp (a tile holds up to 2*NT tokens, one owner CTA each).
-// The warps of row group g sum the squares of slots g, g+4, ...: NSS values per thread.
-template <int S, int NT, bool HEAD = false>
+// NT = token slots per half-warp (a tile holds up to 2*TW*NT tokens, one owner CTA
+// each).  The warps of row group g sum the squares of slots g, g+RG, ...: NSS values
+// per thread.
+template <int S, int NT, bool HEAD = false, int RG = 4>
 struct CT {
-    static constexpr int B = CG<S, HEAD>::B;
-    static constexpr int NSS = (NT + kRG - 1) / kRG;
+    static constexpr int B = CG<S, HEAD, RG>::B;
+    static constexpr int NSS = (NT + RG - 1) / RG;
     static constexpr int NV = NT * B + NSS;                 // per-thread values before the reduce-scatter
     static constexpr int NVP = (NV + 15) / 16 * 16;
     static constexpr int VPL = NVP / 16;                    // per-lane values after it
@@ -132,7 +145,7 @@ struct Lay {   // shared-memory layout in bytes
 template <int S, bool PERSIST, bool HEAD>
 __host__ __device__ inline Lay make_lay(int LK)
 {
-    using G = CG<S, HEAD>;
+    using G = CG<S, HEAD, WM<PERSIST>::RG>;
     Lay L;
     L.stage_bytes = kTMT * LK * 4;
     L.nst = PERSIST ? kNstPersist : 1;
@@ -292,19 +305,31 @@ __device__ __forceinline__ void sinkhorn_regs(float *c, int iters, float eps)
     }
 }
 
-// One column group of the dots: 4 columns of the NT token slots of this half-warp,
-// times this warp's B rows, as packed float32 FMAs (acc = (even-column sum,
-// odd-column sum)); plus the sums of squares of this warp's NSS slots.
-template <int B, int NT, int NSS>
-__device__ __forceinline__ void dots_step(float2 (&acc)[NT][B], float2 (&ssa)[NSS],
-                                          const float (&w)[4 * B], uint32_t xs_addr,
-                                          uint32_t xq_addr, uint32_t cofs, int lk4)
+// The sums of squares of the token slots this warp owns (slot i with i % RG == rg),
+// from the x registers of slots i0 .. i0+NH-1 that the dots just loaded: lo then hi.
+template <int RG, int NSS, int NH>
+__device__ __forceinline__ void squares_step(float2 (&ssa)[NSS], const float4 (&xv)[NH], int i0, int rg)
+{
+#pragma unroll
+    for (int i = 0; i < NH; ++i) {
+        if ((i0 + i) % RG == rg) {
+            const int m = (i0 + i) / RG;
+            const float2 lo = make_float2(xv[i].x, xv[i].y), hi = make_float2(xv[i].z, xv[i].w);
+            ssa[m] = ptx::ffma2(lo, lo, ssa[m]);
+            ssa[m] = ptx::ffma2(hi, hi, ssa[m]);
+        }
+    }
+}
+
+// One column group of the dots, fn_w from shared memory (decode variant): 4 columns
+// of the NT token slots of this half-warp, times this warp's B rows, as packed float32
+// FMAs (acc = (even-column sum, odd-column sum)); plus this warp's sums of squares.
+template <int B, int NT, int RG, int NSS>
+__device__ __forceinline__ void dots_step_smem(float2 (&acc)[NT][B], float2 (&ssa)[NSS],
+                                               const float (&w)[4 * B], uint32_t xs_addr, uint32_t cofs,
+                                               int lk4, int rg)
 {
     constexpr int NH = NT > 4 ? 4 : NT;   // token slots per half (fewer live x registers)
-    float4 xq[NSS];
-#pragma unroll
-    for (int m = 0; m < NSS; ++m)
-        xq[m] = ptx::lds128(xq_addr + (uint32_t)(m * kRG * lk4) + cofs);
 #pragma unroll
     for (int i0 = 0; i0 < NT; i0 += NH) {
         float4 xv[NH];
@@ -325,20 +350,46 @@ __device__ __forceinline__ void dots_step(float2 (&acc)[NT][B], float2 (&ssa)[NS
             for (int r = 0; r < B; ++r)
                 acc[i0 + i][r] = ptx::ffma2(make_float2(xv[i].z, xv[i].w), make_float2(w[4 * r + 2], w[4 * r + 3]),
                                             acc[i0 + i][r]);
+        squares_step<RG, NSS, NH>(ssa, xv, i0, rg);
     }
+}
+
+// The same column group with fn_w from TMEM (persistent variant).  The thread's
+// 4*B values of the group sit at columns taddr .. taddr+4B: first columns 0-1 of its
+// B rows as (row r col 0, row r col 1) pairs, then columns 2-3; each pair block is one
+// TMEM load of 2*B registers.  Same FMA order per accumulator as dots_step_smem.
+template <int B, int NT, int RG, int NSS>
+__device__ __forceinline__ void dots_step_tmem(float2 (&acc)[NT][B], float2 (&ssa)[NSS], uint32_t taddr,
+                                               uint32_t xs_addr, uint32_t cofs, int lk4, int rg)
+{
+    float2 xp[NT];
+    float w[2 * B];
 #pragma unroll
-    for (int m = 0; m < NSS; ++m) {
-        const float2 lo = make_float2(xq[m].x, xq[m].y), hi = make_float2(xq[m].z, xq[m].w);
-        ssa[m] = ptx::ffma2(lo, lo, ssa[m]);
-        ssa[m] = ptx::ffma2(hi, hi, ssa[m]);
+    for (int p = 0; p < 2; ++p) {
+#pragma unroll
+        for (int i = 0; i < NT; ++i)
+            xp[i] = ptx::lds64(xs_addr + (uint32_t)(i * lk4) + cofs + 8u * (uint32_t)p);
+        ptx::tmem_ld_issue<2 * B>(taddr + (uint32_t)(2 * B * p), w);
+        ptx::tmem_ld_wait_regs<2 * B>(w);
+#pragma unroll
+        for (int i = 0; i < NT; ++i)
+#pragma unroll
+            for (int r = 0; r < B; ++r)
+                acc[i][r] = ptx::ffma2(xp[i], make_float2(w[2 * r], w[2 * r + 1]), acc[i][r]);
+#pragma unroll
+        for (int i = 0; i < NT; ++i)
+            if (i % RG == rg)
+                ssa[i / RG] = ptx::ffma2(xp[i], xp[i], ssa[i / RG]);
     }
 }
 
 template <int S, bool PERSIST, int NT, bool HEAD>
 __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const __grid_constant__ Params p)
 {
-    using G = CG<S, HEAD>;
-    using C = CT<S, NT, HEAD>;
+    constexpr int RG = WM<PERSIST>::RG;
+    using G = CG<S, HEAD, RG>;
+    using C = CT<S, NT, HEAD, RG>;
+    static_assert(2 * WM<PERSIST>::TW * NT <= kTMT, "token slots");
     extern __shared__ __align__(128) unsigned char smem[];
     const Lay L = make_lay<S, PERSIST, HEAD>(p.LK);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -430,11 +481,13 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const __gri
         // hands its answer (and, by the barrier's ordering, what it acquired) to all
         // eight warps, so they always meet the same barriers.
         const int tg = lane >> 4, kg = lane & 15;
-        const int rg = warp & (kRG - 1), half = warp / kRG;
+        const int sp = warp & 3, wg = warp >> 2;   // sub-partition, warpgroup
+        const int rg = PERSIST ? (sp & 1) : sp, half = PERSIST ? (sp >> 1) : wg;
+        const int tw = PERSIST ? wg : 0;           // warp token group
         const int j0 = half * njh, nj = half ? p.NJ - njh : njh;
-        // TMEM: warp w reads lanes 32*(w%4).. of its sub-partition; the two warps of
-        // a sub-partition (the two column halves) use disjoint column ranges.
-        const uint32_t trow = tmem_base + ((uint32_t)(32 * rg) << 16) + (uint32_t)(half * njh * G::WQ);
+        // TMEM: warp w reads lanes 32*(w%4).. of its sub-partition; both warps of a
+        // sub-partition (the two token groups) read the same fn_w values there.
+        const uint32_t trow = tmem_base + ((uint32_t)(32 * sp) << 16);
         if (threadIdx.x == 0) {
             // fn_w slice (the persistent variant stages it in stages 1-2, so tile 0
             // can land in stage 0 meanwhile), then the first tile.
@@ -451,22 +504,34 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const __gri
         bool ok = ptx::named_bar_and(
             1, kComputeThreads, threadIdx.x != 0 || wait_bar<false>(BAR(kBarWFull), 0, abort_flag, sb, kSiteWFull));
         if (PERSIST && ok) {
-            // This thread's fixed fn_w values -> its TMEM lane, column jj*WQ + 4r + e.
+            // This thread's fixed fn_w values -> its TMEM lane (written by token group 0,
+            // read by both): column group jj at columns jj*WQ .., row r's columns 0-1 at
+            // 2r, 2r+1 and its columns 2-3 at 2B+2r, 2B+2r+1 (the layout dots_step_tmem reads).
             const float *wstage = stages + stage_floats;
-            for (int jj = 0; jj < nj; ++jj) {
-                const int c = 4 * (kg + 16 * (j0 + jj));
+            if (tw == 0) {
+                for (int jj = 0; jj < nj; ++jj) {
+                    const int c = 4 * (kg + 16 * (j0 + jj));
+                    float a[G::WQ];
 #pragma unroll
-                for (int r = 0; r < G::B; ++r) {
-                    const int row = rg * G::B + r;
-                    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-                    if (row < G::R)
-                        v = *reinterpret_cast<const float4 *>(wstage + row * p.LK + c);
-                    const float a[4] = {v.x, v.y, v.z, v.w};
-                    ptx::tmem_st4(trow + (uint32_t)(jj * G::WQ + 4 * r), a);
+                    for (int r = 0; r < G::B; ++r) {
+                        const int row = rg * G::B + r;
+                        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+                        if (row < G::R)
+                            v = *reinterpret_cast<const float4 *>(wstage + row * p.LK + c);
+                        a[2 * r] = v.x;
+                        a[2 * r + 1] = v.y;
+                        a[2 * G::B + 2 * r] = v.z;
+                        a[2 * G::B + 2 * r + 1] = v.w;
+                    }
+#pragma unroll
+                    for (int m = 0; m < G::B; ++m)
+                        ptx::tmem_st4(trow + (uint32_t)(jj * G::WQ + 4 * m), a + 4 * m);
                 }
+                ptx::tmem_wait_st();
             }
-            ptx::tmem_wait_st();
+            ptx::tmem_fence_before_sync();
             ptx::named_bar_sync(1, kComputeThreads);
+            ptx::tmem_fence_after_sync();
             // Stages 1 and 2 are free now.
             if (threadIdx.x == 0)
                 for (int it = 1; it < L.nst && tile_exists(it); ++it)
@@ -508,18 +573,18 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const __gri
             return true;
         };
 
-        // Persistent variant: the two column halves (warpgroups) wait for tiles on
-        // their own barriers, and half 1 starts once half 0 has done its first dots,
-        // so one half reduces and ships while the other runs its FMAs.  The decode
-        // variant keeps all eight warps together (its collapse needs them all), and
-        // so does the fused post -> pre mode, whose tile transform needs them all.
+        // Persistent variant: the two warpgroups (token groups) wait for tiles on
+        // their own barriers, and warpgroup 1 starts once warpgroup 0 has done its
+        // first dots, so one reduces and ships while the other runs its FMAs.  The
+        // decode variant keeps all eight warps together (its collapse needs them all),
+        // and so does the fused post -> pre mode, whose tile transform needs them all.
         const bool fused = p.x_new != nullptr;
         const bool split = PERSIST && !fused;
-        const uint32_t tbar = split ? kNbHalf0 + (uint32_t)half : kNbCompute;
+        const uint32_t tbar = split ? kNbHalf0 + (uint32_t)wg : kNbCompute;
         const uint32_t tthreads = split ? kComputeThreads / 2 : kComputeThreads;
-        const int tpoll = split ? half * (kComputeThreads / 2) : 0;   // the thread that polls
-        bool arrived = !(split && half == 0);
-        if (split && half == 1)
+        const int tpoll = split ? wg * (kComputeThreads / 2) : 0;   // the thread that polls
+        bool arrived = !(split && wg == 0);
+        if (split && wg == 1)
             ptx::named_bar_sync(kNbStagger, kComputeThreads);
         const int lk4 = p.LK * 4;
         // Fused post -> pre: this thread's share of the next tile's post/comb (at most
@@ -615,12 +680,11 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const __gri
                     load_coefs(it + 1, cpre);
                 }
             }
-            const int ntok = min(NT, max(0, tm - NT * tg));
+            const int slot0 = (2 * tw + tg) * NT;   // this half-warp's first token slot
+            const int ntok = min(NT, max(0, tm - slot0));
             // Byte address of token slot 0 of this half-warp, at this lane's first column group.
-            const uint32_t xs_addr = ptx::smem_u32(stages + s * stage_floats + (tg * NT) * p.LK) + 16u * kg;
+            const uint32_t xs_addr = ptx::smem_u32(stages + s * stage_floats + slot0 * p.LK) + 16u * kg;
             const uint32_t ws_addr = ptx::smem_u32(wsm + (rg * G::B) * p.LK) + 16u * kg;
-            // Slots rg, rg+4, ... of this half-warp: the ones whose squares this warp sums.
-            const uint32_t xq_addr = xs_addr + (uint32_t)(rg * lk4);
 
             // Every slot is computed (rows of a stage past the tile's last token hold stale
             // but harmless data, never sent), so the loop has no data-dependent branch.
@@ -638,12 +702,9 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const __gri
             if (PERSIST) {
                 // fn_w from TMEM, one column group at a time; the other compute warp
                 // of this sub-partition runs its FMAs while this one waits for a load.
-                for (int jj = 0; jj < nj; ++jj) {
-                    float w[G::WQ];
-                    ptx::tmem_ld_issue<G::WQ>(trow + (uint32_t)(jj * G::WQ), w);
-                    ptx::tmem_ld_wait_regs<G::WQ>(w);
-                    dots_step<G::B, NT, C::NSS>(acc, ssa, w, xs_addr, xq_addr, 256u * (uint32_t)(j0 + jj), lk4);
-                }
+                for (int jj = 0; jj < nj; ++jj)
+                    dots_step_tmem<G::B, NT, RG, C::NSS>(acc, ssa, trow + (uint32_t)(jj * G::WQ), xs_addr,
+                                                         256u * (uint32_t)(j0 + jj), lk4, rg);
             } else {
                 for (int jj = 0; jj < nj; ++jj) {
                     const uint32_t cofs = 256u * (uint32_t)(j0 + jj);
@@ -656,7 +717,7 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const __gri
                         w[4 * r + 2] = v.z;
                         w[4 * r + 3] = v.w;
                     }
-                    dots_step<G::B, NT, C::NSS>(acc, ssa, w, xs_addr, xq_addr, cofs, lk4);
+                    dots_step_smem<G::B, NT, RG, C::NSS>(acc, ssa, w, xs_addr, cofs, lk4, rg);
                 }
             }
             if (!arrived) {
@@ -697,11 +758,11 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const __gri
                     const int row = rg * G::B + (o - i * G::B);
                     vid = row < G::R ? row : -1;
                 } else if (o < C::NV) {
-                    i = rg + kRG * (o - NT * G::B);
+                    i = rg + RG * (o - NT * G::B);
                     vid = G::R;
                 }
                 if (vid >= 0 && i < ntok) {
-                    const uint32_t t = (uint32_t)(tg * NT + i);
+                    const uint32_t t = (uint32_t)(slot0 + i);
                     ptx::st_async_f32(ptx::mapa(recv_slot + 4u * (uint32_t)vid, t), v[q],
                                       ptx::mapa(BAR(kBarRecv + qb), t));
                 }
@@ -984,7 +1045,7 @@ cudaError_t launch_variant(const Params &p, int nclusters, cudaStream_t st)
 template <int S, bool HEAD>
 bool supported_s(int device)
 {
-    return max_clusters_for<S, true, 8, HEAD>(device) > 0 && max_clusters_for<S, false, 1, HEAD>(device) > 0 &&
+    return max_clusters_for<S, true, 4, HEAD>(device) > 0 && max_clusters_for<S, false, 1, HEAD>(device) > 0 &&
            max_clusters_for<S, false, 2, HEAD>(device) > 0 && max_clusters_for<S, false, 4, HEAD>(device) > 0 &&
            max_clusters_for<S, false, 8, HEAD>(device) > 0;
 }
@@ -1071,7 +1132,7 @@ cudaError_t run_s(const float *x, const float *fn_w, const float *scale, const f
     p.invK = 1.0f / (float)(S * d);
     // Every decode instantiation has the same footprint; NT = 8 bounds the others.
     const int nc_decode = max_clusters_for<S, false, 8, HEAD>(device);
-    const int nc_persist = max_clusters_for<S, true, 8, HEAD>(device);
+    const int nc_persist = max_clusters_for<S, true, 4, HEAD>(device);
     if (nc_decode < 1 || nc_persist < 1)
         return cudaErrorNotSupported;
     const bool decode = T <= nc_decode * kTMT;
@@ -1095,7 +1156,7 @@ cudaError_t run_s(const float *x, const float *fn_w, const float *scale, const f
             return launch_variant<S, false, 4, HEAD>(p, p.ntiles, st);
         return launch_variant<S, false, 8, HEAD>(p, p.ntiles, st);
     }
-    return launch_variant<S, true, 8, HEAD>(p, min(p.ntiles, nc_persist), st);
+    return launch_variant<S, true, 4, HEAD>(p, min(p.ntiles, nc_persist), st);
 }
 
 }  // namespace

@@ -101,6 +101,12 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t
 }
 
 // ---------------------------------------------------------------- shared memory loads
+__device__ __forceinline__ float2 lds64(uint32_t addr)
+{
+    float2 v;
+    asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr));
+    return v;
+}
 __device__ __forceinline__ float4 lds128(uint32_t addr)
 {
     float4 v;
@@ -293,6 +299,20 @@ template <int N>
 __device__ __forceinline__ void tmem_ld_issue(uint32_t taddr, float *v);
 template <int N>
 __device__ __forceinline__ void tmem_ld_wait_regs(float *v);
+
+template <>
+__device__ __forceinline__ void tmem_ld_issue<2>(uint32_t taddr, float *v)
+{
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x2.b32 {%0, %1}, [%2];\n"
+                 : "=f"(v[0]), "=f"(v[1])
+                 : "r"(taddr)
+                 : "memory");
+}
+template <>
+__device__ __forceinline__ void tmem_ld_wait_regs<2>(float *v)
+{
+    asm volatile("tcgen05.wait::ld.sync.aligned;" : "+f"(v[0]), "+f"(v[1]) :: "memory");
+}
 
 template <>
 __device__ __forceinline__ void tmem_ld_issue<4>(uint32_t taddr, float *v)
