@@ -895,7 +895,10 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const __gri
             // compute warps never wait for gates; only the stage ring links them to these.
             const int ct = threadIdx.x - kCollapseWarp0 * 32;
             const int h4n = p.hs / 4;
+            // Thread -> token t = ct / 8 (its pre gates loaded once) and float4 columns
+            // h4 = ct % 8 + 8 m: eight threads cover 128 contiguous bytes of a row.
             constexpr int U = 2;   // outputs per thread in flight
+            const int t = ct >> 3, hb = ct & 7;
             for (int it = 0; tile_exists(it); ++it) {
                 const int q = it % kNQ;
                 int t0, tm;
@@ -907,41 +910,36 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const __gri
                 }
                 if (!ptx::named_bar_and(kNbCollapse, kCollapseThreads, got))
                     break;
-                const uint32_t xs_base = ptx::smem_u32(stages + (it % L.nst) * stage_floats);
-                const uint32_t pre_base = ptx::smem_u32(preb + q * kTMT * 4);
-                const int n = tm * h4n;
-                for (int e0 = ct; e0 < n; e0 += U * kCollapseThreads) {
-                    float4 xv[U][S];
-                    float pr[U][4];
+                if (t < tm) {
+                    const float4 pv = ptx::lds128(ptx::smem_u32(preb + (q * kTMT + t) * 4));
+                    const float pr[4] = {pv.x, pv.y, pv.z, pv.w};
+                    const uint32_t xrow = ptx::smem_u32(stages + (it % L.nst) * stage_floats + t * p.LK);
+                    float *yrow = p.y + (size_t)(t0 + t) * p.d + (size_t)rank * p.hs;
+                    for (int h0 = hb; h0 < h4n; h0 += 8 * U) {
+                        float4 xv[U][S];
     #pragma unroll
-                    for (int u = 0; u < U; ++u) {
-                        const int e = min(e0 + kCollapseThreads * u, n - 1);
-                        const int t = e / h4n, h4 = e - t * h4n;
-                        const float4 pv = ptx::lds128(pre_base + 16u * (uint32_t)t);
-                        pr[u][0] = pv.x;
-                        pr[u][1] = pv.y;
-                        pr[u][2] = pv.z;
-                        pr[u][3] = pv.w;
+                        for (int u = 0; u < U; ++u) {
+                            const int h4 = min(h0 + 8 * u, h4n - 1);
     #pragma unroll
-                        for (int k = 0; k < S; ++k)
-                            xv[u][k] = ptx::lds128(xs_base + 4u * (uint32_t)(t * p.LK + k * p.hs + 4 * h4));
-                    }
-    #pragma unroll
-                    for (int u = 0; u < U; ++u) {
-                        const int e = e0 + kCollapseThreads * u;
-                        if (e >= n)
-                            break;
-                        const int t = e / h4n, h4 = e - t * h4n;
-                        float4 a = make_float4(pr[u][0] * xv[u][0].x, pr[u][0] * xv[u][0].y, pr[u][0] * xv[u][0].z,
-                                               pr[u][0] * xv[u][0].w);
-    #pragma unroll
-                        for (int k = 1; k < S; ++k) {
-                            a.x = fmaf(pr[u][k], xv[u][k].x, a.x);
-                            a.y = fmaf(pr[u][k], xv[u][k].y, a.y);
-                            a.z = fmaf(pr[u][k], xv[u][k].z, a.z);
-                            a.w = fmaf(pr[u][k], xv[u][k].w, a.w);
+                            for (int k = 0; k < S; ++k)
+                                xv[u][k] = ptx::lds128(xrow + 4u * (uint32_t)(k * p.hs + 4 * h4));
                         }
-                        *reinterpret_cast<float4 *>(p.y + (size_t)(t0 + t) * p.d + (size_t)rank * p.hs + 4 * h4) = a;
+    #pragma unroll
+                        for (int u = 0; u < U; ++u) {
+                            const int h4 = h0 + 8 * u;
+                            if (h4 >= h4n)
+                                break;
+                            float4 a = make_float4(pr[0] * xv[u][0].x, pr[0] * xv[u][0].y, pr[0] * xv[u][0].z,
+                                                   pr[0] * xv[u][0].w);
+    #pragma unroll
+                            for (int k = 1; k < S; ++k) {
+                                a.x = fmaf(pr[k], xv[u][k].x, a.x);
+                                a.y = fmaf(pr[k], xv[u][k].y, a.y);
+                                a.z = fmaf(pr[k], xv[u][k].z, a.z);
+                                a.w = fmaf(pr[k], xv[u][k].w, a.w);
+                            }
+                            *reinterpret_cast<float4 *>(yrow + 4 * h4) = a;
+                        }
                     }
                 }
                 ptx::named_bar_sync(kNbCollapse, kCollapseThreads);
