@@ -830,7 +830,10 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const __gri
                     const float ss = __shfl_sync(kFull, val, G::R);
                     const float rinv = rsqrtf(ss * p.invK + p.eps);
                     const float logit = lane < G::R ? val * rinv * my_scale + my_base : 0.f;
-                    const float sg = __frcp_rn(1.f + expf(-logit));
+                    // Hardware exp2-based exponential and fast divide (a few ulp each): the
+                    // gates sit on the path from the partials to the collapse, and this warp
+                    // shares its sub-partition with two FMA-bound compute warps.
+                    const float sg = __fdividef(1.f, 1.f + __expf(-logit));
                     const float pre_v = sg + p.eps;
                     // pre gates of this token -> every CTA of the cluster (16 bytes each);
                     // exp(comb logits) -> the Sinkhorn CTA, one value per lane.
@@ -845,7 +848,7 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const __gri
                     }
                     if (!HEAD && lane >= 2 * S && lane < G::R) {
                         const uint32_t dst = ptx::smem_u32(sinkbuf + (int)rank * 16 + (lane - 2 * S));
-                        ptx::st_async_f32(ptx::mapa(dst, sc), expf(logit), ptx::mapa(BAR(kBarSink), sc));
+                        ptx::st_async_f32(ptx::mapa(dst, sc), __expf(logit), ptx::mapa(BAR(kBarSink), sc));
                     }
                     const size_t tok = (size_t)t0 + rank;
                     if (lane < S) {
