@@ -24,8 +24,9 @@
 //    token slots [8*(w/4), 8*(w/4)+8), so every x value of a stage is read by
 //    two warps; decode variant: rows [B*(w%4), ..) (B = 6), column half w/4,
 //    every token slot.  In a warp, lanes 0-15 take the first of its token slots
-//    and lanes 16-31 the rest, and lane&15 is the K-group owning float4 columns
-//    kg, kg+16, ...  Operands: x from shared memory, fn_w from TMEM; packed
+//    and lanes 16-31 the rest, and lane&15 is the K-group kg owning columns
+//    2kg, 2kg+1, 32+2kg, 33+2kg of every 64-column group (so each half-warp
+//    load is 128 contiguous bytes).  Operands: x from shared memory, fn_w from TMEM; packed
 //    float32 FMAs on CUDA cores (no TF32: the 24-row contraction is too skinny
 //    for tensor cores and must stay in f32).  A 16-lane xor reduce-scatter
 //    sums the K-groups, and each lane stores its partial dots and sums of
@@ -321,9 +322,11 @@ __device__ __forceinline__ void squares_step(float2 (&ssa)[NSS], const float4 (&
     }
 }
 
-// One column group of the dots, fn_w from shared memory (decode variant): 4 columns
-// of the NT token slots of this half-warp, times this warp's B rows, as packed float32
-// FMAs (acc = (even-column sum, odd-column sum)); plus this warp's sums of squares.
+// One 64-column group of the dots, fn_w from shared memory (decode variant): lane kg's
+// two column pairs (2kg, 2kg+1 and 32+2kg, 33+2kg: each half-warp load is 128
+// contiguous bytes) of the NT token slots of this half-warp, times this warp's B rows,
+// as packed float32 FMAs (acc = (even-column sum, odd-column sum)); plus this warp's
+// sums of squares.
 template <int B, int NT, int RG, int NSS>
 __device__ __forceinline__ void dots_step_smem(float2 (&acc)[NT][B], float2 (&ssa)[NSS],
                                                const float (&w)[4 * B], uint32_t xs_addr, uint32_t cofs,
@@ -334,8 +337,11 @@ __device__ __forceinline__ void dots_step_smem(float2 (&acc)[NT][B], float2 (&ss
     for (int i0 = 0; i0 < NT; i0 += NH) {
         float4 xv[NH];
 #pragma unroll
-        for (int i = 0; i < NH; ++i)
-            xv[i] = ptx::lds128(xs_addr + (uint32_t)((i0 + i) * lk4) + cofs);
+        for (int i = 0; i < NH; ++i) {
+            const float2 a = ptx::lds64(xs_addr + (uint32_t)((i0 + i) * lk4) + cofs);
+            const float2 b = ptx::lds64(xs_addr + (uint32_t)((i0 + i) * lk4) + cofs + 128u);
+            xv[i] = make_float4(a.x, a.y, b.x, b.y);
+        }
         // Even-column halves first, then odd-column halves: consecutive packed FMAs
         // never depend on each other.
 #pragma unroll
@@ -355,9 +361,9 @@ __device__ __forceinline__ void dots_step_smem(float2 (&acc)[NT][B], float2 (&ss
 }
 
 // The same column group with fn_w from TMEM (persistent variant).  The thread's
-// 4*B values of the group sit at columns taddr .. taddr+4B: first columns 0-1 of its
-// B rows as (row r col 0, row r col 1) pairs, then columns 2-3; each pair block is one
-// TMEM load of 2*B registers.  Same FMA order per accumulator as dots_step_smem.
+// 4*B values of the group sit at columns taddr .. taddr+4B: its first column pair for
+// each of its B rows, then its second; each pair block is one TMEM load of 2*B
+// registers.  Same FMA order per accumulator as dots_step_smem.
 template <int B, int NT, int RG, int NSS>
 __device__ __forceinline__ void dots_step_tmem(float2 (&acc)[NT][B], float2 (&ssa)[NSS], uint32_t taddr,
                                                uint32_t xs_addr, uint32_t cofs, int lk4, int rg)
@@ -368,7 +374,7 @@ __device__ __forceinline__ void dots_step_tmem(float2 (&acc)[NT][B], float2 (&ss
     for (int p = 0; p < 2; ++p) {
 #pragma unroll
         for (int i = 0; i < NT; ++i)
-            xp[i] = ptx::lds64(xs_addr + (uint32_t)(i * lk4) + cofs + 8u * (uint32_t)p);
+            xp[i] = ptx::lds64(xs_addr + (uint32_t)(i * lk4) + cofs + 128u * (uint32_t)p);
         ptx::tmem_ld_issue<2 * B>(taddr + (uint32_t)(2 * B * p), w);
         ptx::tmem_ld_wait_regs<2 * B>(w);
 #pragma unroll
@@ -505,23 +511,26 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const __gri
             1, kComputeThreads, threadIdx.x != 0 || wait_bar<false>(BAR(kBarWFull), 0, abort_flag, sb, kSiteWFull));
         if (PERSIST && ok) {
             // This thread's fixed fn_w values -> its TMEM lane (written by token group 0,
-            // read by both): column group jj at columns jj*WQ .., row r's columns 0-1 at
-            // 2r, 2r+1 and its columns 2-3 at 2B+2r, 2B+2r+1 (the layout dots_step_tmem reads).
+            // read by both): column group jj at columns jj*WQ .., row r's first column
+            // pair (2kg, 2kg+1 of the group) at 2r, 2r+1 and its second (32+2kg, 33+2kg)
+            // at 2B+2r, 2B+2r+1 (the layout dots_step_tmem reads).
             const float *wstage = stages + stage_floats;
             if (tw == 0) {
                 for (int jj = 0; jj < nj; ++jj) {
-                    const int c = 4 * (kg + 16 * (j0 + jj));
+                    const int c = 64 * (j0 + jj) + 2 * kg;
                     float a[G::WQ];
 #pragma unroll
                     for (int r = 0; r < G::B; ++r) {
                         const int row = rg * G::B + r;
-                        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-                        if (row < G::R)
-                            v = *reinterpret_cast<const float4 *>(wstage + row * p.LK + c);
-                        a[2 * r] = v.x;
-                        a[2 * r + 1] = v.y;
-                        a[2 * G::B + 2 * r] = v.z;
-                        a[2 * G::B + 2 * r + 1] = v.w;
+                        float2 v0 = make_float2(0.f, 0.f), v1 = make_float2(0.f, 0.f);
+                        if (row < G::R) {
+                            v0 = *reinterpret_cast<const float2 *>(wstage + row * p.LK + c);
+                            v1 = *reinterpret_cast<const float2 *>(wstage + row * p.LK + c + 32);
+                        }
+                        a[2 * r] = v0.x;
+                        a[2 * r + 1] = v0.y;
+                        a[2 * G::B + 2 * r] = v1.x;
+                        a[2 * G::B + 2 * r + 1] = v1.y;
                     }
 #pragma unroll
                     for (int m = 0; m < G::B; ++m)
@@ -683,8 +692,8 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const __gri
             const int slot0 = (2 * tw + tg) * NT;   // this half-warp's first token slot
             const int ntok = min(NT, max(0, tm - slot0));
             // Byte address of token slot 0 of this half-warp, at this lane's first column group.
-            const uint32_t xs_addr = ptx::smem_u32(stages + s * stage_floats + slot0 * p.LK) + 16u * kg;
-            const uint32_t ws_addr = ptx::smem_u32(wsm + (rg * G::B) * p.LK) + 16u * kg;
+            const uint32_t xs_addr = ptx::smem_u32(stages + s * stage_floats + slot0 * p.LK) + 8u * kg;
+            const uint32_t ws_addr = ptx::smem_u32(wsm + (rg * G::B) * p.LK) + 8u * kg;
 
             // Every slot is computed (rows of a stage past the tile's last token hold stale
             // but harmless data, never sent), so the loop has no data-dependent branch.
@@ -711,11 +720,12 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const __gri
                     float w[G::WQ];
 #pragma unroll
                     for (int r = 0; r < G::B; ++r) {
-                        const float4 v = ptx::lds128(ws_addr + (uint32_t)(r * lk4) + cofs);
-                        w[4 * r] = v.x;
-                        w[4 * r + 1] = v.y;
-                        w[4 * r + 2] = v.z;
-                        w[4 * r + 3] = v.w;
+                        const float2 v0 = ptx::lds64(ws_addr + (uint32_t)(r * lk4) + cofs);
+                        const float2 v1 = ptx::lds64(ws_addr + (uint32_t)(r * lk4) + cofs + 128u);
+                        w[4 * r] = v0.x;
+                        w[4 * r + 1] = v0.y;
+                        w[4 * r + 2] = v1.x;
+                        w[4 * r + 3] = v1.y;
                     }
                     dots_step_smem<G::B, NT, RG, C::NSS>(acc, ssa, w, xs_addr, cofs, lk4, rg);
                 }
