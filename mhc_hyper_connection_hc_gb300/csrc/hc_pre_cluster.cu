@@ -38,10 +38,14 @@
 //    one reduces and ships while the other runs its FMAs.  Four
 //    collapse warps (one per SM sub-partition) wait for each tile's pre gates,
 //    write y for the CTA's hidden columns from the tile's stage and refill the
-//    stage, so the stage ring alone couples them to the compute warps.  The
-//    decode variant's single tile is collapsed by the compute warps.  The
+//    stage, so the stage ring alone couples them to the compute warps.  In the
+//    fused post -> pre mode they also apply the previous site's hc_post to each
+//    landed tile in place (x -> x', two tiles ahead of their collapse), store x'
+//    by TMA and release the stage to the compute warps.  The decode variant's
+//    single tile is transformed and collapsed by the compute warps.  The
 //    sixteen warps launch at 128 registers; the two compute warpgroups raise
-//    theirs to 200 with setmaxnreg while the other two drop to 56.
+//    theirs to 192 with setmaxnreg while the finisher warpgroup drops to 48 and
+//    the collapse warpgroup to 80.
 //  * Two finisher warps (even/odd tiles) of each owner sum the 2 x 16
 //    partials in a fixed tree, apply the rsqrt rescale, form the gates,
 //    broadcast pre to all 16 CTAs and write pre/post; exp(comb logits) go to
@@ -76,12 +80,13 @@ constexpr int kCollapseWarp0 = 12;   // persistent variant: warps 12-15 collapse
 constexpr int kCollapseThreads = 4 * 32;
 constexpr int kThreads = 16 * 32;    // four warpgroups, launched at 128 registers a thread
 // The two compute warpgroups take registers from the other two (whose warps wait
-// or stream shared memory): 2 x 128 x 200 + 2 x 128 x 56 = 512 x 128.  The split
+// or stream shared memory): 2 x 128 x 192 + 128 x 48 (finisher / Sinkhorn warps)
+// + 128 x 80 (collapse warps, which also run the fused mode's tile transform) = 512 x 128.  The split
 // is made once, at the role dispatch, and kept until exit: a warpgroup that gave
 // registers back and then asked for them again could take them before the compute
 // warpgroups had theirs, and those would then wait for registers forever.
-constexpr int kRegsCompute = 200, kRegsAux = 56;
-static_assert(2 * 128 * kRegsCompute + 2 * 128 * kRegsAux == kThreads * 128, "register split");
+constexpr int kRegsCompute = 192, kRegsFinish = 48, kRegsCollapse = 80;
+static_assert(2 * 128 * kRegsCompute + 128 * kRegsFinish + 128 * kRegsCollapse == kThreads * 128, "register split");
 // Named barriers: 1 all compute warps, 2 collapse warps, 3 + h column half h of the
 // persistent variant, 5 the halves' one-off start stagger.
 constexpr uint32_t kNbCompute = 1, kNbCollapse = 2, kNbHalf0 = 3, kNbStagger = 5;
@@ -101,7 +106,8 @@ constexpr unsigned kFull = 0xffffffffu;
 constexpr int kNQ = 4;
 constexpr int kBarXFull = 0, kBarRecv = 3, kBarPre = kBarRecv + kNQ, kBarSink = kBarPre + kNQ,
               kBarWFull = kBarSink + 1, kBarSinkDone = kBarWFull + 1, kBarFFull = kBarSinkDone + 1,
-              kBarStored = kBarFFull + 1, kNumBars = kBarStored + 3;   // kBarStored: per stage
+              kBarStored = kBarFFull + 1, kBarXReady = kBarStored + 3, kNumBars = kBarXReady + 3;
+              // kBarStored, kBarXReady: per stage
 enum WaitSite : unsigned {
     kSiteWFull = 1, kSiteXFull, kSiteRecv, kSitePre, kSiteSink, kSiteDrain, kSiteSinkDone, kSiteStored
 };
@@ -459,8 +465,10 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const __gri
         ptx::mbar_init(BAR(kBarWFull), 1);
         ptx::mbar_init(BAR(kBarSinkDone), 1);
         ptx::mbar_init(BAR(kBarFFull), 1);
-        for (int s = 0; s < kNstPersist; ++s)
-            ptx::mbar_init(BAR(kBarStored + s), 1);   // fused: the stage's x' store has read it
+        for (int s = 0; s < kNstPersist; ++s) {
+            ptx::mbar_init(BAR(kBarStored + s), 1);   // fused decode: the stage's x' store has read it
+            ptx::mbar_init(BAR(kBarXReady + s), 1);   // fused persistent: the stage holds x'
+        }
         *abort_flag = 0;
         ptx::fence_mbar_init_cluster();
     }
@@ -504,7 +512,7 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const __gri
             ptx::tma_load_4d(ptx::smem_u32(wdst), &p.tmap_w, 0, (int)rank * p.hsc, 0, 0,
                              BAR(kBarWFull));
             load_tile(0);   // every cluster has at least one tile
-            if (p.x_new)
+            if (p.x_new && !PERSIST)   // the persistent variant's collapse warps load f
                 load_f(0);
         }
         bool ok = ptx::named_bar_and(
@@ -584,11 +592,14 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const __gri
 
         // Persistent variant: the two warpgroups (token groups) wait for tiles on
         // their own barriers, and warpgroup 1 starts once warpgroup 0 has done its
-        // first dots, so one reduces and ships while the other runs its FMAs.  The
-        // decode variant keeps all eight warps together (its collapse needs them all),
-        // and so does the fused post -> pre mode, whose tile transform needs them all.
+        // first dots, so one reduces and ships while the other runs its FMAs.  In its
+        // fused post -> pre mode the collapse warps transform each tile (x -> x') and
+        // the compute warps wait for that instead of the load.  The decode variant
+        // keeps all eight warps together: its collapse, and in fused mode its tile
+        // transform, need them all.
         const bool fused = p.x_new != nullptr;
-        const bool split = PERSIST && !fused;
+        const bool tf_here = fused && !PERSIST;   // these warps transform the tile
+        const bool split = PERSIST;
         const uint32_t tbar = split ? kNbHalf0 + (uint32_t)wg : kNbCompute;
         const uint32_t tthreads = split ? kComputeThreads / 2 : kComputeThreads;
         const int tpoll = split ? wg * (kComputeThreads / 2) : 0;   // the thread that polls
@@ -620,16 +631,17 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const __gri
             if (!tile_exists(it))
                 break;
             const int s = it % L.nst, u = it / L.nst;
+            const int xbar = (PERSIST && fused) ? kBarXReady + s : kBarXFull + s;
             ok = ptx::named_bar_and(
                 tbar, tthreads,
                 (int)threadIdx.x != tpoll ||
-                    (wait_bar<false>(BAR(kBarXFull + s), u & 1, abort_flag, sb, kSiteXFull) &&
-                     (!fused || wait_bar<false>(BAR(kBarFFull), it & 1, abort_flag, sb, kSiteXFull))));
+                    (wait_bar<false>(BAR(xbar), u & 1, abort_flag, sb, kSiteXFull) &&
+                     (!tf_here || wait_bar<false>(BAR(kBarFFull), it & 1, abort_flag, sb, kSiteXFull))));
             if (!ok)
                 break;
             int t0, tm;
             tile_tokens(it, t0, tm);
-            if (fused) {
+            if (tf_here) {
                 // The previous site's hc_post on this tile, in place: thread e owns the
                 // 4 columns h4 of token t in every stream, reads x_prev, writes x' (the
                 // same operations, in the same order, as hc_post_kernel).  The tile's
@@ -734,7 +746,7 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const __gri
                 ptx::named_bar_arrive(kNbStagger, kComputeThreads);
                 arrived = true;
             }
-            if (fused && threadIdx.x == 0) {   // the x' store has had the dots to read the stage
+            if (tf_here && threadIdx.x == 0) {   // the x' store has had the dots to read the stage
                 ptx::bulk_wait_read_all();
                 ptx::mbar_arrive(BAR(kBarStored + s));
             }
@@ -786,10 +798,13 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const __gri
         }
         if (!arrived)
             ptx::named_bar_arrive(kNbStagger, kComputeThreads);
-        if (fused && threadIdx.x == 0)
+        if (tf_here && threadIdx.x == 0)
             ptx::bulk_wait_all();   // every x' store complete before the CTA can exit
     } else {
-        ptx::setmaxnreg_dec<kRegsAux>();
+        if (warp >= kCollapseWarp0)
+            ptx::setmaxnreg_dec<kRegsCollapse>();
+        else
+            ptx::setmaxnreg_dec<kRegsFinish>();
         if (warp < kSinkWarp) {
             // -------------------------------------------------------------- finisher warps
             // Tile it's token t is owned by CTA t: its finisher (warp 8 + it % 2) sums the
@@ -906,13 +921,88 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const __gri
             // Tile by tile: wait for the owners' pre gates, write y for this CTA's hidden
             // columns from the tile's stage, then refill the stage with tile it + nst.  The
             // compute warps never wait for gates; only the stage ring links them to these.
+            // Fused post -> pre mode: these warps also turn each landed tile into x' in
+            // place (the previous site's hc_post), store x' by TMA and release the stage
+            // to the compute warps, two tiles ahead of their collapse.
             const int ct = threadIdx.x - kCollapseWarp0 * 32;
             const int h4n = p.hs / 4;
-            // Thread -> token t = ct / 8 (its pre gates loaded once) and float4 columns
-            // h4 = ct % 8 + 8 m: eight threads cover 128 contiguous bytes of a row.
+            // Thread -> token t = ct / 8 (its gates or coefficients loaded once) and float4
+            // columns h4 = ct % 8 + 8 m: eight threads cover 128 contiguous bytes of a row.
             constexpr int U = 2;   // outputs per thread in flight
             const int t = ct >> 3, hb = ct & 7;
-            for (int it = 0; tile_exists(it); ++it) {
+            const bool fused = p.x_new != nullptr;
+            constexpr int NC = S + S * S;
+            // x -> x' for tile k (the same operations, in the same order, as hc_post_kernel).
+            auto transform = [&](int k) -> bool {
+                const int s = k % L.nst;
+                int t0, tm;
+                tile_tokens(k, t0, tm);
+                for (int e = ct; e < tm * NC; e += kCollapseThreads) {   // the tile's post / comb
+                    const int tt = e / NC, cc = e - tt * NC;
+                    coefs[e] = cc < S ? __ldg(p.post_prev + (size_t)(t0 + tt) * S + cc)
+                                      : __ldg(p.comb_prev + (size_t)(t0 + tt) * S * S + (cc - S));
+                }
+                bool got = true;
+                if (ct == 0)
+                    got = wait_bar<false>(BAR(kBarXFull + s), (k / L.nst) & 1, abort_flag, sb, kSiteXFull) &&
+                          wait_bar<false>(BAR(kBarFFull), k & 1, abort_flag, sb, kSiteXFull);
+                if (!ptx::named_bar_and(kNbCollapse, kCollapseThreads, got))
+                    return false;
+                if (t < tm) {
+                    float cf[NC];
+    #pragma unroll
+                    for (int c = 0; c < NC; ++c)
+                        cf[c] = coefs[t * NC + c];
+                    float *xr = stages + s * stage_floats + t * p.LK;
+                    const float *fr = fbuf + t * p.hs;
+                    for (int h4 = hb; h4 < h4n; h4 += 8) {
+                        float4 *xt = reinterpret_cast<float4 *>(xr + 4 * h4);
+                        const float4 fv = *reinterpret_cast<const float4 *>(fr + 4 * h4);
+                        float4 xv[S];
+    #pragma unroll
+                        for (int j = 0; j < S; ++j)
+                            xv[j] = xt[j * h4n];
+    #pragma unroll
+                        for (int kk = 0; kk < S; ++kk) {
+                            const float pk = cf[kk];
+                            float4 o = make_float4(pk * fv.x, pk * fv.y, pk * fv.z, pk * fv.w);
+    #pragma unroll
+                            for (int j = 0; j < S; ++j) {
+                                const float cc = cf[S + j * S + kk];
+                                o.x = fmaf(cc, xv[j].x, o.x);
+                                o.y = fmaf(cc, xv[j].y, o.y);
+                                o.z = fmaf(cc, xv[j].z, o.z);
+                                o.w = fmaf(cc, xv[j].w, o.w);
+                            }
+                            xt[kk * h4n] = o;
+                        }
+                    }
+                }
+                ptx::fence_proxy_async_smem();   // the TMA store reads the stage, a TMA load refills it
+                ptx::named_bar_sync(kNbCollapse, kCollapseThreads);
+                if (ct == 0) {
+                    ptx::tma_store_4d(&p.tmap_xnew, 0, (int)rank * p.hsc, 0, t0, ptx::smem_u32(stages + s * stage_floats));
+                    ptx::bulk_commit();
+                    ptx::mbar_arrive(BAR(kBarXReady + s));   // the compute warps may read x'
+                    if (tile_exists(k + 1))
+                        load_f(k + 1);
+                }
+                return true;
+            };
+            int nt = 0;   // the next tile to transform
+            bool tok = true;
+            if (fused) {
+                if (ct == 0)
+                    load_f(0);
+                for (; tok && nt < 2 && tile_exists(nt); ++nt)
+                    tok = transform(nt);
+            }
+            for (int it = 0; tok && tile_exists(it); ++it) {
+                if (fused && tile_exists(nt)) {   // nt = it + 2
+                    if (!(tok = transform(nt)))
+                        break;
+                    ++nt;
+                }
                 const int q = it % kNQ;
                 int t0, tm;
                 tile_tokens(it, t0, tm);
@@ -956,11 +1046,16 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const __gri
                     }
                 }
                 ptx::named_bar_sync(kNbCollapse, kCollapseThreads);
-                if (ct == 0 && tile_exists(it + L.nst) &&
-                    (!p.x_new || wait_bar<false>(BAR(kBarStored + it % L.nst), (it / L.nst) & 1, abort_flag, sb,
-                                                 kSiteStored)))
+                if (ct == 0 && tile_exists(it + L.nst)) {
+                    // Fused: tile it's x' store has read the stage (only the stores of
+                    // tiles it + 1 and it + 2 may still be pending).
+                    if (fused)
+                        ptx::bulk_wait_read<2>();
                     load_tile(it + L.nst);
+                }
             }
+            if (fused && ct == 0)
+                ptx::bulk_wait_all();   // every x' store complete before the CTA can exit
         }
     }
 
