@@ -106,10 +106,9 @@ constexpr unsigned kFull = 0xffffffffu;
 constexpr int kNQ = 4;
 constexpr int kBarXFull = 0, kBarRecv = 3, kBarPre = kBarRecv + kNQ, kBarSink = kBarPre + kNQ,
               kBarWFull = kBarSink + 1, kBarSinkDone = kBarWFull + 1, kBarFFull = kBarSinkDone + 1,
-              kBarStored = kBarFFull + 1, kBarXReady = kBarStored + 3, kNumBars = kBarXReady + 3;
-              // kBarStored, kBarXReady: per stage
+              kBarXReady = kBarFFull + 1, kNumBars = kBarXReady + 3;   // kBarXReady: per stage
 enum WaitSite : unsigned {
-    kSiteWFull = 1, kSiteXFull, kSiteRecv, kSitePre, kSiteSink, kSiteDrain, kSiteSinkDone, kSiteStored
+    kSiteWFull = 1, kSiteXFull, kSiteRecv, kSitePre, kSiteSink, kSiteDrain, kSiteSinkDone
 };
 
 // Compute-warp map.  Warp w runs on SM sub-partition w%4, whose TMEM lane quarter it
@@ -465,10 +464,8 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const __gri
         ptx::mbar_init(BAR(kBarWFull), 1);
         ptx::mbar_init(BAR(kBarSinkDone), 1);
         ptx::mbar_init(BAR(kBarFFull), 1);
-        for (int s = 0; s < kNstPersist; ++s) {
-            ptx::mbar_init(BAR(kBarStored + s), 1);   // fused decode: the stage's x' store has read it
+        for (int s = 0; s < kNstPersist; ++s)
             ptx::mbar_init(BAR(kBarXReady + s), 1);   // fused persistent: the stage holds x'
-        }
         *abort_flag = 0;
         ptx::fence_mbar_init_cluster();
     }
@@ -745,10 +742,6 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const __gri
             if (!arrived) {
                 ptx::named_bar_arrive(kNbStagger, kComputeThreads);
                 arrived = true;
-            }
-            if (tf_here && threadIdx.x == 0) {   // the x' store has had the dots to read the stage
-                ptx::bulk_wait_read_all();
-                ptx::mbar_arrive(BAR(kBarStored + s));
             }
 
             // Half-warp sums over the 16 K-groups.

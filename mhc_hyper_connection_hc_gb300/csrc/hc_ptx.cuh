@@ -132,8 +132,6 @@ __device__ __forceinline__ void tma_store_4d(const void *tmap, int c0, int c1, i
                  : "memory");
 }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-// Wait until this thread's committed bulk stores have read their shared memory.
-__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 // Wait until all but this thread's N most recent committed bulk-store groups have
 // read their shared memory.
 template <int N>
