@@ -116,15 +116,19 @@ def profiled_traffic(kernel: str, workload: str):
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 200 ms in the background."""
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi clocks and throttle reasons sampled every 100 ms in the background,
+    each sample with its timestamp; mark() brackets the timed region, and the summary
+    is taken over the samples that fall inside it (all samples if none does)."""
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    STAMP = "%Y/%m/%d %H:%M:%S.%f"
 
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.proc = None
         self.path = None
+        self.t0 = self.t1 = None
 
     def __enter__(self):
         fd, self.path = tempfile.mkstemp(suffix=".csv")
@@ -132,15 +136,25 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except (OSError, ValueError):
             self.proc = None
         time.sleep(0.25)
         return self
 
+    def mark(self, which: str):
+        """Host wall time at the start ("start") or end ("end") of the timed region."""
+        import datetime
+        now = datetime.datetime.now()
+        if which == "start":
+            self.t0 = now
+        else:
+            self.t1 = now
+
     def __exit__(self, *exc):
         if self.proc is not None:
+            time.sleep(0.15)   # one more sample after the region
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
@@ -148,27 +162,28 @@ class ClockSampler:
                 self.proc.kill()
 
     def summary(self):
+        import datetime
         if self.proc is None or not self.path or not os.path.exists(self.path):
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        sm, smax, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        rows = []
         for line in open(self.path):
             parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 9:
+            if len(parts) < 10:
                 continue
             try:
-                sm.append(float(parts[1]))
-                smax.append(float(parts[2]))
+                rows.append((datetime.datetime.strptime(parts[0], self.STAMP), float(parts[2]), float(parts[3]),
+                             parts[6:10]))
             except ValueError:
                 continue
-            for name, val in zip(names, parts[5:9]):
-                if val.lower() == "active":
-                    reasons.add(name)
         os.unlink(self.path)
-        if not sm:
+        if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
-                "samples": len(sm)}
+        inside = [r for r in rows if self.t0 and self.t1 and self.t0 <= r[0] <= self.t1]
+        use = inside or rows
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = {n for r in use for n, v in zip(names, r[3]) if v.lower() == "active"}
+        return {"sm_mhz": statistics.median(r[1] for r in use), "sm_max_mhz": max(r[2] for r in use),
+                "reasons": sorted(reasons), "samples": len(rows), "samples_in_timed_region": len(inside)}
 
 
 # ----------------------------------------------------------------------------- CPU oracle timing
@@ -197,19 +212,34 @@ def time_oracle(w: synth.Workload, max_tokens: int, budget_s: float, max_reps: i
 
 
 def run_reference(args):
+    """The oracle as it stands, on the host cores: each step is one float64 pre-chain +
+    hc_post over a fixed sample of the workload's tokens (inputs made and widened once,
+    outside the timed loop)."""
+    import oracle
     rank, world, _ = dist_env()
     if rank != 0:
         return 0
     w = selected_workload(args)
     sample = min(w.T, args.ref_tokens)
+    inp = synth.workload_inputs(w, T=sample)
+    x = inp["x"].astype(np.float64)
+    f = inp["f"].astype(np.float64)
+    threads = oracle.default_threads()
+    eps = float(np.float32(w.eps))
+
+    def step():
+        oracle.site(x, inp["fn_w"], inp["scale"], inp["base"], f, w.iters, eps, threads=threads)
+
     for _ in range(args.warmup):
-        time_oracle(w, max_tokens=min(sample, 64), budget_s=0.0, max_reps=1)
+        step()
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        cb = time_oracle(w, max_tokens=sample, budget_s=0.0, max_reps=1)
+        step()
     elapsed = time.perf_counter() - t0
     value = sample * args.steps / elapsed
-    cb["value"] = value
+    cb = {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+          "sample": f"{sample} of {w.T} tokens of the {w.name} workload (s={w.s}, d={w.d}, "
+                    f"iters={w.iters}) per step, pre-chain + hc_post in float64, {args.steps} steps"}
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1e3 * elapsed / args.steps, "higher_is_better": True,
@@ -309,6 +339,7 @@ def run_gpu(args):
     barrier()
     torch.cuda.synchronize(dev)
     with ClockSampler(dev.index if dev.index is not None else 0) as clk:
+        clk.mark("start")
         for k in range(K):
             ev[k][0].record(stream)
             if fused:
@@ -320,6 +351,7 @@ def run_gpu(args):
                 post()
             ev[k][2].record(stream)
         stream.synchronize()
+        clk.mark("end")
     torch.cuda.synchronize(dev)
     barrier()
     clocks = clk.summary()
@@ -584,7 +616,7 @@ def measure_decode(dev, iters=None, n_sites: int = 300):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("gb300", "reference"), default="gb300")
     ap.add_argument("--workload", choices=tuple(WORKLOAD_IDS), default="prefill")
