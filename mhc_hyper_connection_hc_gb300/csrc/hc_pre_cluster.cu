@@ -87,9 +87,9 @@ constexpr int kThreads = 16 * 32;    // four warpgroups, launched at 128 registe
 // warpgroups had theirs, and those would then wait for registers forever.
 constexpr int kRegsCompute = 192, kRegsFinish = 48, kRegsCollapse = 80;
 static_assert(2 * 128 * kRegsCompute + 128 * kRegsFinish + 128 * kRegsCollapse == kThreads * 128, "register split");
-// Named barriers: 1 all compute warps, 2 collapse warps, 3 + h column half h of the
-// persistent variant, 5 the halves' one-off start stagger.
-constexpr uint32_t kNbCompute = 1, kNbCollapse = 2, kNbHalf0 = 3, kNbStagger = 5;
+// Named barriers: 1 all compute warps, 2 collapse warps, 3 + g compute warpgroup g of the
+// persistent variant (its tile barrier), 5 the warpgroups' one-off start stagger.
+constexpr uint32_t kNbCompute = 1, kNbCollapse = 2, kNbGroup0 = 3, kNbStagger = 5;
 constexpr int kSinkLag = 8;          // a finisher waits for the Sinkhorn of the tile 8 before its own
 constexpr int kComputeThreads = kNCW * 32;
 constexpr int kNstPersist = 3;
@@ -347,8 +347,8 @@ __device__ __forceinline__ void dots_step_smem(float2 (&acc)[NT][B], float2 (&ss
             const float2 b = ptx::lds64(xs_addr + (uint32_t)((i0 + i) * lk4) + cofs + 128u);
             xv[i] = make_float4(a.x, a.y, b.x, b.y);
         }
-        // Even-column halves first, then odd-column halves: consecutive packed FMAs
-        // never depend on each other.
+        // The first column pair of every slot and row, then the second: consecutive
+        // packed FMAs never depend on each other.
 #pragma unroll
         for (int i = 0; i < NH; ++i)
 #pragma unroll
@@ -597,7 +597,7 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const __gri
         const bool fused = p.x_new != nullptr;
         const bool tf_here = fused && !PERSIST;   // these warps transform the tile
         const bool split = PERSIST;
-        const uint32_t tbar = split ? kNbHalf0 + (uint32_t)wg : kNbCompute;
+        const uint32_t tbar = split ? kNbGroup0 + (uint32_t)wg : kNbCompute;
         const uint32_t tthreads = split ? kComputeThreads / 2 : kComputeThreads;
         const int tpoll = split ? wg * (kComputeThreads / 2) : 0;   // the thread that polls
         bool arrived = !(split && wg == 0);

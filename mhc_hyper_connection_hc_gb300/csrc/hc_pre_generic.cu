@@ -28,7 +28,8 @@ namespace {
 
 constexpr int kTM = 16;            // tokens per tile (2 token groups of 8)
 constexpr int kKC = 128;           // columns per K chunk staged in shared memory
-constexpr int kTargetCtas = 304;   // split-K sizing: two CTAs per SM of a 152-SM GB300
+constexpr int kTargetCtas = 304;   // split-K sizing: 2 x the 152 SMs of a GB300 (the s = 4 kernel
+                                   // holds 3 CTAs per SM, s >= 7 one)
 constexpr int kFinishThreads = 256;
 
 // HEAD: the gated-head trunk exit (rows = streams, pre-style gates only).
