@@ -97,3 +97,46 @@ def test_reference_arm_non_zero_rank_exits_quietly():
                         "--gpus", "2", "--steps", "1", "--warmup", "3"],
                        capture_output=True, text=True, timeout=120, cwd=ROOT, env=env)
     assert r.returncode == 0 and r.stdout.strip() == ""
+
+
+def test_clock_sampler_keeps_the_samples_inside_the_timed_region(tmp_path):
+    """bench.py's clock summary: the median SM clock and the throttle reasons of the
+    samples whose timestamps fall inside the timed region, with their count; all
+    samples when none does."""
+    import datetime
+    sys.path.insert(0, ROOT)
+    import bench
+    t0 = datetime.datetime(2026, 1, 2, 3, 4, 5)
+    rows = [  # seconds after t0, SM MHz, hw_slowdown, sw_power_cap
+        (-0.3, 1000, "Not Active", "Not Active"),
+        (0.1, 2070, "Not Active", "Active"),
+        (0.2, 2040, "Not Active", "Not Active"),
+        (0.3, 2070, "Not Active", "Not Active"),
+        (0.9, 500, "Active", "Not Active"),
+    ]
+    path = tmp_path / "clocks.csv"
+    with open(path, "w") as fh:
+        for dt, mhz, hw, cap in rows:
+            stamp = (t0 + datetime.timedelta(seconds=dt)).strftime(bench.ClockSampler.STAMP)[:-3]
+            fh.write(f"{stamp}, 0, {mhz}, 2070, 900.0, 0x0, {hw}, Not Active, Not Active, {cap}\n")
+
+    def summary(start, end):
+        cs = bench.ClockSampler(0)
+        cs.proc, cs.path = object(), str(path)
+        cs.t0 = t0 + datetime.timedelta(seconds=start)
+        cs.t1 = t0 + datetime.timedelta(seconds=end)
+        import shutil
+        keep = str(path) + ".keep"
+        shutil.copy(path, keep)
+        try:
+            return cs.summary()
+        finally:
+            shutil.move(keep, path)
+
+    s = summary(0.0, 0.5)
+    assert s["samples"] == 5 and s["samples_in_timed_region"] == 3
+    assert s["sm_mhz"] == 2070 and s["sm_max_mhz"] == 2070
+    assert s["reasons"] == ["sw_power_cap"]            # the hw_slowdown sample lies outside
+    s = summary(5.0, 6.0)                              # no sample inside: all of them
+    assert s["samples_in_timed_region"] == 0 and s["sm_mhz"] == 2040
+    assert s["reasons"] == ["hw_slowdown", "sw_power_cap"]
