@@ -16,7 +16,7 @@ pytestmark = pytest.mark.gpu
 
 SMALL = [  # (T, s, d)
     (1, 4, 4096), (37, 4, 4096), (200, 4, 4096), (150, 2, 2048), (133, 3, 3072), (19, 1, 1024),
-    (17, 3, 4100), (5, 8, 7168), (33, 6, 40),
+    (17, 3, 4100), (5, 8, 7168), (33, 6, 40), (130, 1, 1024), (300, 4, 2048),
 ]
 
 

@@ -16,7 +16,7 @@ pytestmark = pytest.mark.gpu
 
 SMALL = [  # (T, s, d)
     (1, 4, 4096), (37, 4, 4096), (200, 4, 4096), (19, 1, 1024), (150, 2, 2048), (133, 3, 3072),
-    (3, 2, 64), (17, 3, 4100), (33, 6, 40), (5, 8, 7168), (1, 8, 4),
+    (3, 2, 64), (17, 3, 4100), (33, 6, 40), (5, 8, 7168), (1, 8, 4), (130, 1, 1024), (300, 4, 2048),
 ]
 
 

@@ -21,7 +21,7 @@ pytestmark = pytest.mark.gpu
 SMALL = [  # (T, s, d)
     (1, 4, 4096), (8, 4, 4096), (37, 4, 4096), (16, 4, 1024), (19, 1, 1024), (3, 2, 64),
     (17, 3, 4100), (2, 5, 12), (33, 6, 40), (4, 7, 8), (1, 8, 4), (5, 8, 7168), (40, 2, 2048),
-    (21, 3, 3072), (200, 4, 4096), (150, 2, 2048), (130, 1, 1024), (133, 3, 3072),
+    (21, 3, 3072), (200, 4, 4096), (150, 2, 2048), (130, 1, 1024), (133, 3, 3072), (300, 4, 2048),
 ]
 
 
