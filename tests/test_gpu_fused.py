@@ -105,3 +105,27 @@ def test_fused_full_size_sampled_and_bit_identical():
         assert torch.equal(x_new.view(torch.int32), ref["x_new"].view(torch.int32))
         for k in ("pre", "post", "comb", "y"):
             assert torch.equal(o[k].view(torch.int32), ref[k].view(torch.int32)), k
+
+
+def test_fused_largest_state():
+    """T*s*d just under 2^31 elements (8 GiB of state in, 8 GiB out): 64-bit offsets and
+    tensor-map rows of the fused boundary, on sampled tokens at both ends and the middle."""
+    s, d = 4, 4096
+    T = (2 ** 31 - 1) // (s * d)
+    base_T = 64
+    inp = _inputs(43, base_T, s, d)
+    reps = (T + base_T - 1) // base_T
+    dv = {k: _up(v) for k, v in inp.items()}
+    for k in ("x", "f", "post_prev", "comb_prev"):
+        t = dv[k]
+        dv[k] = t.repeat(reps, *([1] * (t.dim() - 1)))[:T].contiguous()
+    fz = Fused(T, s, d)
+    x_new, o = fz.run(dv)
+    idx = np.array([0, 1, T // 2, T - 2, T - 1])
+    src = idx % base_T
+    x_new_want = oracle.post(inp["x"][src], inp["f"][src], inp["post_prev"][src], inp["comb_prev"][src])
+    want = oracle.pre(x_new_want, inp["fn_w"], inp["scale"], inp["base"], 20, eps32(1e-6))
+    assert rel_err(to_np(x_new[idx]), x_new_want) <= TOL
+    for k in ("pre", "post", "comb", "y"):
+        assert rel_err(to_np(o[k][idx]), want[k]) <= TOL, k
+    del dv, x_new
