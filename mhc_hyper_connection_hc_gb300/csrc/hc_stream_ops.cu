@@ -33,20 +33,23 @@ hc_post_kernel(const float4 *__restrict__ x, const float4 *__restrict__ f,
     __shared__ float coef[S + S * S];   // post[k] then comb[j][k]
     const int t = blockIdx.x / blocks_per_token;
     const int col = (blockIdx.x - t * blocks_per_token) * kThreads + threadIdx.x;
+    // The streaming loads go out first, so their latency covers the coefficients'.
+    const bool active = col < d4;
+    const size_t xbase = (size_t)t * S * d4 + col;
+    float4 xv[S], fv = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (active) {
+#pragma unroll
+        for (int j = 0; j < S; ++j)
+            xv[j] = ld_stream(x + xbase + (size_t)j * d4);
+        fv = ld_stream(f + (size_t)t * d4 + col);
+    }
     if (threadIdx.x < S)
         coef[threadIdx.x] = post[(size_t)t * S + threadIdx.x];
     else if (threadIdx.x < S + S * S)
         coef[threadIdx.x] = comb[(size_t)t * S * S + (threadIdx.x - S)];
     __syncthreads();
-    if (col >= d4)
+    if (!active)
         return;
-
-    const size_t xbase = (size_t)t * S * d4 + col;
-    float4 xv[S];
-#pragma unroll
-    for (int j = 0; j < S; ++j)
-        xv[j] = ld_stream(x + xbase + (size_t)j * d4);
-    const float4 fv = ld_stream(f + (size_t)t * d4 + col);
 
 #pragma unroll
     for (int k = 0; k < S; ++k) {
