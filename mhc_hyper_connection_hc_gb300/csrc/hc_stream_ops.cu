@@ -33,16 +33,21 @@ hc_post_kernel(const float4 *__restrict__ x, const float4 *__restrict__ f,
     __shared__ float coef[S + S * S];   // post[k] then comb[j][k]
     const int t = blockIdx.x / blocks_per_token;
     const int col = (blockIdx.x - t * blocks_per_token) * kThreads + threadIdx.x;
-    // The streaming loads go out first, so their latency covers the coefficients'.
+    // Up to six streams the streaming loads go out before the coefficient barrier, so
+    // their latency covers the coefficients'; with more, holding them across it would
+    // cost a resident block per SM (registers), and they follow it.
+    constexpr bool kEarly = S <= 6;
     const bool active = col < d4;
     const size_t xbase = (size_t)t * S * d4 + col;
     float4 xv[S], fv = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (active) {
+    auto load = [&]() {
 #pragma unroll
         for (int j = 0; j < S; ++j)
             xv[j] = ld_stream(x + xbase + (size_t)j * d4);
         fv = ld_stream(f + (size_t)t * d4 + col);
-    }
+    };
+    if (kEarly && active)
+        load();
     if (threadIdx.x < S)
         coef[threadIdx.x] = post[(size_t)t * S + threadIdx.x];
     else if (threadIdx.x < S + S * S)
@@ -50,6 +55,8 @@ hc_post_kernel(const float4 *__restrict__ x, const float4 *__restrict__ f,
     __syncthreads();
     if (!active)
         return;
+    if (!kEarly)
+        load();
 
 #pragma unroll
     for (int k = 0; k < S; ++k) {
