@@ -431,6 +431,7 @@ def run_gpu(args):
 
     if not args.no_head:
         line["exit_head"] = measure_head(w, dv, ws, stream, peak)
+        line["branch_norm"] = measure_norm(w, out["y"], stream, peak)
     if not args.no_e2e:
         if fused:
             def boundary_on(bi, bo):
@@ -510,6 +511,40 @@ def measure_e2e(w, dev_in, dev_out, stream, K, run):
     return {"value": w.T * K / sec, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": 1e3 * sec / K,
             "pipelining": "2 device buffer sets; copy-in, compute and copy-out streams"}
+
+
+def measure_norm(w, y, stream, peak, reps: int = 20):
+    """The branch-input norm with its Q8_0 pair (hc_rms_norm_q8) on the step's y,
+    outside the timed step: mean of `reps` event-timed launches after 3 warm-up
+    launches.  Algorithmic bytes: y read; z, q and the block scales written."""
+    import torch
+    from mhc_hyper_connection_hc_gb300 import hc
+    T, d = y.shape
+    if d % 32:
+        return {"note": "d is not a multiple of 32: no Q8_0 pair"}
+    with torch.cuda.stream(stream):
+        norm_w = torch.from_numpy((1.0 + 0.25 * synth.branch_output(w.cid, 7, 1, d)[0]).astype(np.float32))
+        norm_w = norm_w.to(y.device)   # 1 + 0.25 U[-1, 1), as the norm's parity tests
+        z = torch.empty_like(y)
+        q = torch.empty(T, d, dtype=torch.int8, device=y.device)
+        qs = torch.empty(T, d // 32, dtype=torch.float32, device=y.device)
+
+    def norm():
+        hc.hc_rms_norm_q8(y, norm_w, 1e-5, z, q, qs, stream=stream)
+
+    for _ in range(3):
+        norm()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    for e0, e1 in ev:
+        e0.record(stream)
+        norm()
+        e1.record(stream)
+    stream.synchronize()
+    us = statistics.mean(e0.elapsed_time(e1) for e0, e1 in ev) * 1e3
+    nbytes = T * d * 4 + T * d * 4 + T * d + T * (d // 32) * 4
+    gbs = nbytes / us / 1e3
+    return {"us": us, "algorithmic_bytes": nbytes, "GB/s": gbs, "frac_hbm": gbs / peak,
+            "note": "rms_norm of y (eps 1e-5) and its Q8_0 pair, timed separately from the step"}
 
 
 def measure_head(w, dv, ws, stream, peak, reps: int = 20):
