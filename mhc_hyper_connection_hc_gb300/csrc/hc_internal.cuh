@@ -48,6 +48,11 @@ struct DeviceInfo {
 // Cached per device; returns false if the CUDA runtime fails.
 bool device_info(DeviceInfo &out);
 
+// Unique id (cuCtxGetId) of the CUDA context current on the calling thread, 0 if none
+// is current yet.  Per-device set-up (function attributes, symbol addresses) is cached
+// under it, so a device reset, which replaces the context, makes the set-up run again.
+unsigned long long context_id();
+
 // ---------------------------------------------------------------- launchers (host)
 // All launchers assume validated arguments and return a cudaError_t.
 cudaError_t launch_post(const float *x, const float *f, const float *post, const float *comb,

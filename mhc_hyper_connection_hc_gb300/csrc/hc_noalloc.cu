@@ -14,7 +14,8 @@
 // of the library image, so every GPU that loads the library holds its
 // kNoallocScratchBytes until the process exits.  Its device address is looked
 // up with cudaGetSymbolAddress once per device, on the first call made with
-// that device current.
+// that device current (and again if the device's context has been replaced,
+// e.g. after cudaDeviceReset, which unloads the module and the buffer with it).
 #include <mutex>
 
 #include "hc_internal.cuh"
@@ -26,17 +27,20 @@ constexpr size_t kNoallocScratchBytes = (size_t)4 << 20;   // 4 MiB
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
 
-// Device address of g_noalloc_scratch on `device` (which must be current).
+// Device address of g_noalloc_scratch on `device` (which must be current), cached
+// per device under the id of the context it was looked up in.
 void *scratch_address(int device, cudaError_t *err)
 {
     static std::mutex mu;
     static void *addr[64] = {};
+    static unsigned long long ctx_of[64] = {};
     if (device < 0 || device >= 64) {
         *err = cudaErrorInvalidDevice;
         return nullptr;
     }
     std::lock_guard<std::mutex> lock(mu);
-    if (addr[device] == nullptr) {
+    const unsigned long long ctx = context_id();   // 0 before the runtime has made one current
+    if (addr[device] == nullptr || ctx == 0 || ctx != ctx_of[device]) {
         void *p = nullptr;
         const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
         if (e != cudaSuccess || p == nullptr) {
@@ -44,6 +48,7 @@ void *scratch_address(int device, cudaError_t *err)
             return nullptr;
         }
         addr[device] = p;
+        ctx_of[device] = context_id();   // the look-up has made the device's context current
     }
     return addr[device];
 }

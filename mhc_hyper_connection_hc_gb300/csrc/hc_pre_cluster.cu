@@ -1077,7 +1077,7 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const __gri
 // ---------------------------------------------------------------------- host side
 
 struct VariantInfo {
-    bool init = false;
+    unsigned long long ctx = 0;   // context the attributes were set in (0: not yet)
     int max_clusters = 0;
 };
 
@@ -1090,15 +1090,20 @@ int max_clusters_for(int device)
         return 0;
     std::lock_guard<std::mutex> lock(mu);
     VariantInfo &vi = info[device];
-    if (!vi.init) {
-        vi.init = true;
+    const unsigned long long ctx = context_id();
+    if (ctx == 0 || vi.ctx != ctx) {
+        // Function attributes belong to the context: set them again in a new one.
+        vi.ctx = ctx;
+        vi.max_clusters = 0;
         const Lay L = make_lay<S, PERSIST, HEAD>(kMaxLK);
         auto kern = hc_pre_cluster_kernel<S, PERSIST, NT, HEAD>;
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L.total) != cudaSuccess ||
             cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
             cudaGetLastError();
+            vi.ctx = 0;
             return 0;
         }
+        vi.ctx = context_id();
         cudaLaunchConfig_t cfg = {};
         cudaLaunchAttribute at[1];
         at[0].id = cudaLaunchAttributeClusterDimension;

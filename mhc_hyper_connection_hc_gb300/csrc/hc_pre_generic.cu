@@ -21,6 +21,8 @@
 // in a fixed order (lane order within a thread, an xor butterfly over the 16
 // K-groups, then ascending K-slice), and no floating-point atomics are used,
 // so repeated calls are bit-identical.
+#include <mutex>
+
 #include "hc_internal.cuh"
 
 namespace hc {
@@ -325,16 +327,23 @@ cudaError_t run_generic(const float *x, const float *fn_w, const float *scale, c
     using G = Geo<S, HEAD>;
     const Split sp = make_split(T, S, d);
     float *part = reinterpret_cast<float *>(static_cast<char *>(workspace) + kStatusBytes);
-    static bool smem_set[64] = {};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (G::SMEM > 48 * 1024 && dev < 64 && !smem_set[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(mixes_partial_kernel<S, HEAD>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)G::SMEM);
-        if (e != cudaSuccess)
-            return e;
-        smem_set[dev] = true;
+    if (G::SMEM > 48 * 1024) {
+        // The dynamic shared-memory limit is a per-context attribute: set once per
+        // device and context (a device reset replaces the context and drops it).
+        static std::mutex mu;
+        static unsigned long long set_in[64] = {};
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+            return cudaErrorInvalidDevice;
+        std::lock_guard<std::mutex> lock(mu);
+        const unsigned long long ctx = context_id();
+        if (ctx == 0 || set_in[dev] != ctx) {
+            cudaError_t e = cudaFuncSetAttribute(mixes_partial_kernel<S, HEAD>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)G::SMEM);
+            if (e != cudaSuccess)
+                return e;
+            set_in[dev] = context_id();
+        }
     }
     dim3 grid1(sp.nt, sp.nks);
     mixes_partial_kernel<S, HEAD><<<grid1, G::NT, G::SMEM, st>>>(x, fn_w, T, S * d, sp.nck, sp.ck_per, part);

@@ -1,15 +1,38 @@
 """CPU-only checks of the C ABI: the library loads, exports every function that
 include/hc.h declares, and refuses bad arguments on the host before any CUDA
-call (fake pointers are passed; none of these cases reaches a launch)."""
+call (fake pointers are passed; none of these cases reaches a launch).
+
+Fake device addresses must never reach a GPU: if a regression moved a host check
+after a launch, a kernel would dereference them.  So in a process that can see a
+GPU these tests do not run directly; test_host_checks_in_a_process_without_devices
+runs them (and the no-alloc size check) in a child process with no device visible,
+where such a regression fails with a CUDA error instead."""
 
 import ctypes
 import math
 import os
 import re
+import subprocess
+import sys
 
 import pytest
 
 from mhc_hyper_connection_hc_gb300 import hc
+
+
+def _device_visible() -> bool:
+    if os.environ.get("CUDA_VISIBLE_DEVICES") == "":
+        return False
+    try:
+        import torch
+        return bool(torch.cuda.is_available())
+    except Exception:
+        return False
+
+
+DEVICE_VISIBLE = _device_visible()
+fake_addresses = pytest.mark.skipif(
+    DEVICE_VISIBLE, reason="fake device addresses: run in a child process without devices")
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "hc.h")
@@ -31,6 +54,7 @@ def lib():
     return hc.load()
 
 
+@fake_addresses
 def test_every_declared_function_is_exported(lib):
     names = declared_functions()
     assert len(names) >= 10
@@ -39,6 +63,7 @@ def test_every_declared_function_is_exported(lib):
     assert set(names) >= set(hc.EXPORTED)
 
 
+@fake_addresses
 def test_status_strings(lib):
     for rc in range(0, 9):
         assert len(hc.status_string(rc)) >= 2
@@ -50,6 +75,7 @@ def post_rc(lib, x=A, f=A + 64 * MB, post=A + 96 * MB, comb=A + 97 * MB, out=A +
     return lib.hc_post(x, f, post, comb, out, T, s, d, None)
 
 
+@fake_addresses
 def test_post_validation(lib):
     assert post_rc(lib, x=0) == hc.HC_ERR_NULL
     assert post_rc(lib, out=0) == hc.HC_ERR_NULL
@@ -66,6 +92,7 @@ def test_post_validation(lib):
     assert post_rc(lib, T=0, x=0, f=0, out=0) == hc.HC_OK            # empty batch
 
 
+@fake_addresses
 def test_expand_mean_validation(lib):
     assert lib.hc_expand(A, A, 2, 4, 64, None) == hc.HC_ERR_ALIAS
     assert lib.hc_expand(0, A, 2, 4, 64, None) == hc.HC_ERR_NULL
@@ -86,6 +113,7 @@ def pre_rc(lib, T=3, s=4, d=4096, iters=20, eps=1e-6, ws_bytes=None, path=0, **o
     return lib.hc_pre_fused_path(*args)
 
 
+@fake_addresses
 def test_pre_validation(lib):
     assert pre_rc(lib, iters=0) == hc.HC_ERR_DIM                     # zero iterations refused
     assert pre_rc(lib, eps=0.0) == hc.HC_ERR_DIM                     # eps <= 0 refused
@@ -108,6 +136,7 @@ def test_pre_validation(lib):
     assert pre_rc(lib, T=0, x=0) == hc.HC_OK                          # empty batch
 
 
+@fake_addresses
 def test_workspace_sizes(lib):
     assert hc.hc_pre_workspace_bytes(0, 4, 4096) >= 256
     assert hc.hc_pre_workspace_bytes(1, 9, 4096) == 0
@@ -123,6 +152,7 @@ def head_rc(lib, x=A, fn_w=A + 32 * MB, scale=A + 40 * MB, base=A + 40 * MB + 64
     return lib.hc_head_path(x, fn_w, scale, base, T, s, d, eps, gates, y, ws, ws_bytes, None, path)
 
 
+@fake_addresses
 def test_head_validation(lib):
     assert head_rc(lib, eps=0.0) == hc.HC_ERR_DIM
     assert head_rc(lib, eps=math.nan) == hc.HC_ERR_DIM
@@ -153,6 +183,7 @@ def fused_rc(lib, T=2, s=4, d=4096, iters=20, eps=1e-6, path=0, **over):
                                       p["post"], p["comb"], p["y"], p["ws"], ws_bytes, None, path)
 
 
+@fake_addresses
 def test_post_pre_fused_validation(lib):
     assert fused_rc(lib, iters=0) == hc.HC_ERR_DIM
     assert fused_rc(lib, eps=0.0) == hc.HC_ERR_DIM
@@ -173,6 +204,7 @@ def norm_rc(lib, y=A, w=A + 8 * MB, z=A + 9 * MB, q=A + 10 * MB, qs=A + 11 * MB,
     return lib.hc_rms_norm_q8(y, w, T, d, eps, z, q, qs, None)
 
 
+@fake_addresses
 def test_rms_norm_q8_validation(lib):
     assert norm_rc(lib, T=-1) == hc.HC_ERR_DIM
     assert norm_rc(lib, eps=-1.0) == hc.HC_ERR_DIM
@@ -184,3 +216,19 @@ def test_rms_norm_q8_validation(lib):
     assert norm_rc(lib, z=A + 64) == hc.HC_ERR_ALIAS                # z over y
     assert norm_rc(lib, qs=A + 10 * MB + 16) == hc.HC_ERR_ALIAS     # scales over q
     assert norm_rc(lib, T=0, y=0) == hc.HC_OK
+
+
+@pytest.mark.gpu
+def test_host_checks_in_a_process_without_devices():
+    """On a machine with a GPU: the fake-address checks of this file and of the no-alloc
+    entry point, in a child process that sees no device."""
+    if not DEVICE_VISIBLE:
+        pytest.skip("no device visible here: the checks run directly in this process")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, CUDA_VISIBLE_DEVICES="")
+    r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-p", "no:cacheprovider", "-m", "not gpu",
+                        os.path.join(root, "tests", "test_abi_host.py"),
+                        os.path.join(root, "tests", "test_zz_no_alloc.py")],
+                       capture_output=True, text=True, timeout=600, cwd=root, env=env)
+    assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-2000:]
+    assert " passed" in r.stdout and " skipped" not in r.stdout.splitlines()[-1], r.stdout[-2000:]

@@ -219,6 +219,23 @@ def test_expand_then_mean_is_identity(s):
         np.testing.assert_allclose(m, e, rtol=4e-16, atol=0)
 
 
+@pytest.mark.parametrize("s", [1, 2, 3, 4, 8])
+def test_mean_of_distinct_streams(s):
+    """Stream c holds (c+1) v, so the unweighted mean is ((s+1)/2) v; and stream c holding
+    2^c v gives ((2^s - 1)/s) v.  Equal streams (the expand pin) cannot tell a stream-0-only
+    mean, a wrong stream stride or a wrong divisor from the right one; these can."""
+    T, d = 3, 40
+    v = synth.branch_output(912, 0, T, d).astype(np.float64)
+    x = np.stack([(c + 1) * v for c in range(s)], axis=1)
+    np.testing.assert_allclose(oracle.mean(x), 0.5 * (s + 1) * v, rtol=1e-15, atol=0)
+    x2 = np.stack([(2.0 ** c) * v for c in range(s)], axis=1)
+    np.testing.assert_allclose(oracle.mean(x2), (2.0 ** s - 1.0) / s * v, rtol=1e-15, atol=0)
+    # token-major layout: token t's streams are x[t, :, :], not interleaved across tokens
+    x3 = np.stack([(c + 1) * v for c in range(s)], axis=1) + 10.0 * np.arange(T)[:, None, None]
+    np.testing.assert_allclose(oracle.mean(x3), 0.5 * (s + 1) * v + 10.0 * np.arange(T)[:, None],
+                               rtol=1e-14, atol=1e-13)
+
+
 # ----------------------------------------------------------------------------- brute force
 
 

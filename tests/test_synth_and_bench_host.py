@@ -99,10 +99,11 @@ def test_reference_arm_non_zero_rank_exits_quietly():
     assert r.returncode == 0 and r.stdout.strip() == ""
 
 
-def test_clock_sampler_keeps_the_samples_inside_the_timed_region(tmp_path):
+def test_clock_sampler_keeps_the_samples_inside_the_measurement_region(tmp_path):
     """bench.py's clock summary: the median SM clock and the throttle reasons of the
-    samples whose timestamps fall inside the timed region, with their count; all
-    samples when none does."""
+    samples whose timestamps fall inside the measurement region (the timed steps and the
+    per-kernel rounds after them), with the counts in the timed and the measurement
+    region; sm_mhz is null when no sample falls inside."""
     import datetime
     sys.path.insert(0, ROOT)
     import bench
@@ -120,11 +121,12 @@ def test_clock_sampler_keeps_the_samples_inside_the_timed_region(tmp_path):
             stamp = (t0 + datetime.timedelta(seconds=dt)).strftime(bench.ClockSampler.STAMP)[:-3]
             fh.write(f"{stamp}, 0, {mhz}, 2070, 900.0, 0x0, {hw}, Not Active, Not Active, {cap}\n")
 
-    def summary(start, end):
+    def summary(start, end, region_end=None):
         cs = bench.ClockSampler(0)
         cs.proc, cs.path = object(), str(path)
         cs.t0 = t0 + datetime.timedelta(seconds=start)
         cs.t1 = t0 + datetime.timedelta(seconds=end)
+        cs.t2 = None if region_end is None else t0 + datetime.timedelta(seconds=region_end)
         import shutil
         keep = str(path) + ".keep"
         shutil.copy(path, keep)
@@ -133,10 +135,12 @@ def test_clock_sampler_keeps_the_samples_inside_the_timed_region(tmp_path):
         finally:
             shutil.move(keep, path)
 
-    s = summary(0.0, 0.5)
-    assert s["samples"] == 5 and s["samples_in_timed_region"] == 3
+    s = summary(0.0, 0.15, 0.5)
+    assert s["samples"] == 5 and s["samples_in_timed_region"] == 1
+    assert s["samples_in_measurement_region"] == 3
     assert s["sm_mhz"] == 2070 and s["sm_max_mhz"] == 2070
     assert s["reasons"] == ["sw_power_cap"]            # the hw_slowdown sample lies outside
-    s = summary(5.0, 6.0)                              # no sample inside: all of them
-    assert s["samples_in_timed_region"] == 0 and s["sm_mhz"] == 2040
-    assert s["reasons"] == ["hw_slowdown", "sw_power_cap"]
+    s = summary(0.0, 0.5)                              # no rounds: the timed region alone
+    assert s["samples_in_measurement_region"] == 3 and s["sm_mhz"] == 2070
+    s = summary(5.0, 6.0)                              # no sample inside: no clock reported
+    assert s["samples_in_timed_region"] == 0 and s["sm_mhz"] is None and s["reasons"] == []
