@@ -755,6 +755,127 @@ def measure_decode(dev, iters=None, n_sites: int = 300):
     return res
 
 
+STAMP_EVENTS = ("stage_ready", "dots_done", "shipped", "partials", "gates_sent", "pre_arrived", "collapsed",
+                "refilled", "xf_start", "xf_landed", "xf_done", "sink_done", "kernel_start")
+STAMP_TILES, STAMP_EV, STAMP_CTAS = 256, 16, 2
+
+
+def run_stamps(args):
+    """Per-phase timing of the fused pre kernel from its phase-stamp build (HC_STAMPS):
+    %globaltimer stamps of CTAs 0 and 8 of cluster 0 at every tile's phase boundaries,
+    for the pre-chain and the fused site boundary of the selected workload; medians
+    over the tiles (the first two skipped) of each phase, in microseconds."""
+    import torch
+    from mhc_hyper_connection_hc_gb300 import build as lib_build, hc
+    hc.load(lib_build.build(stamps=True))
+    dev = torch.device("cuda", 0)
+    w = selected_workload(args)
+    T, s, d = w.T, w.s, w.d
+    inp = synth.workload_inputs(w)
+    dv = {k: torch.from_numpy(v).to(dev) for k, v in inp.items()}
+    ws = hc.new_workspace(T, s, d, dev)
+    out = hc.new_pre_outputs(T, s, d, dev)
+    x_new = torch.empty(T, s, d, device=dev)
+    hc.hc_pre_fused(dv["x"], dv["fn_w"], dv["scale"], dv["base"], w.iters, w.eps, out["pre"], out["post"],
+                    out["comb"], out["y"], ws)
+    post_prev, comb_prev = out["post"].clone(), out["comb"].clone()
+    base = 256   # stamps follow the 256-byte status block
+
+    def read(fn):
+        for _ in range(3):
+            fn()
+        hc.hc_workspace_init(ws)
+        fn()
+        torch.cuda.synchronize()
+        if hc.hc_workspace_status(ws) != 0:
+            raise RuntimeError("a kernel flagged an error")
+        raw = ws[base:base + STAMP_CTAS * STAMP_TILES * STAMP_EV * 8].view(torch.int64)
+        return raw.view(STAMP_CTAS, STAMP_TILES, STAMP_EV).cpu().numpy().astype(np.float64) / 1e3   # µs
+
+    def med(vals):
+        vals = [v for v in vals if np.isfinite(v)]
+        return round(float(np.median(vals)), 3) if vals else None
+
+    def analyse(st):
+        E = {n: i for i, n in enumerate(STAMP_EVENTS)}
+        t0 = st[0, 0, E["kernel_start"]]
+        ntile = int(np.max(np.nonzero(st[0, :, E["stage_ready"]])[0])) + 1 if np.any(st[0, :, E["stage_ready"]]) else 0
+
+        def ev(c, it, name):
+            v = st[c, it, E[name]] if 0 <= it < STAMP_TILES else 0.0
+            return v if v > 0 else np.nan
+
+        rng = range(2, ntile) if ntile > 4 else range(0, ntile)
+        res = {"tiles_stamped": ntile, "cta": "cluster 0, CTA 0 (owner of token 0 of every tile); "
+                                              "compute phases are warpgroup 0's",
+               "kernel_us": round(float(np.nanmax(st[0, :ntile, :12]) - t0), 3) if ntile else None,
+               "first_stage_ready_us": round(float(ev(0, 0, "stage_ready") - t0), 3) if ntile else None}
+        res["dots"] = med(ev(0, i, "dots_done") - ev(0, i, "stage_ready") for i in rng)
+        res["reduce_and_ship"] = med(ev(0, i, "shipped") - ev(0, i, "dots_done") for i in rng)
+        res["tile_period"] = med(ev(0, i, "stage_ready") - ev(0, i - 1, "stage_ready") for i in rng)
+        res["wait_for_stage"] = med(ev(0, i, "stage_ready") - ev(0, i - 1, "shipped") for i in rng)
+        res["shipped_to_owner_partials"] = med(ev(0, i, "partials") - ev(0, i, "shipped") for i in rng)
+        res["owner_gates"] = med(ev(0, i, "gates_sent") - ev(0, i, "partials") for i in rng)
+        res["shipped_to_pre_arrived"] = med(ev(0, i, "pre_arrived") - ev(0, i, "shipped") for i in rng)
+        res["collapse"] = med(ev(0, i, "collapsed") - ev(0, i, "pre_arrived") for i in rng)
+        res["collapse_period"] = med(ev(0, i, "collapsed") - ev(0, i - 1, "collapsed") for i in rng)
+        res["refill_to_stage_ready"] = med(ev(0, i + 3, "stage_ready") - ev(0, i, "refilled") for i in rng)
+        res["sinkhorn_after_gates"] = med(ev(0, i, "sink_done") - ev(0, i, "gates_sent") for i in rng)
+        if np.any(st[0, :ntile, E["xf_done"]] > 0):
+            res["transform_wait"] = med(ev(0, i, "xf_landed") - ev(0, i, "xf_start") for i in rng)
+            res["transform"] = med(ev(0, i, "xf_done") - ev(0, i, "xf_landed") for i in rng)
+            res["transform_done_to_stage_ready"] = med(ev(0, i, "stage_ready") - ev(0, i, "xf_done") for i in rng)
+        return res
+
+    def pre():
+        hc.hc_pre_fused(dv["x"], dv["fn_w"], dv["scale"], dv["base"], w.iters, w.eps, out["pre"], out["post"],
+                        out["comb"], out["y"], ws)
+
+    def boundary():
+        hc.hc_post_pre_fused(dv["x"], dv["f"], post_prev, comb_prev, dv["fn_w"], dv["scale"], dv["base"], w.iters,
+                             w.eps, x_new, out["pre"], out["post"], out["comb"], out["y"], ws)
+
+    def analyse_wide(st):
+        """The wide-stream kernel's stamps: slot 0 CTA 0 (compute warp 0, publisher, collapse
+        warp); slot 1 group 0's sum and the finish of every tile, whichever CTA did them."""
+        E = {n: i for i, n in enumerate(STAMP_EVENTS)}
+        t0 = st[0, 0, E["kernel_start"]]
+        ntile = int(np.max(np.nonzero(st[0, :, E["stage_ready"]])[0])) + 1 if np.any(st[0, :, E["stage_ready"]]) else 0
+
+        def ev(c, it, name):
+            v = st[c, it, E[name]] if 0 <= it < STAMP_TILES else 0.0
+            return v if v > 0 else np.nan
+
+        rng = range(2, ntile) if ntile > 4 else range(0, ntile)
+        res = {"tiles_stamped": ntile,
+               "kernel_us": round(float(np.nanmax(st[0, :ntile, :12]) - t0), 3) if ntile else None,
+               "first_stage_ready_us": round(float(ev(0, 0, "stage_ready") - t0), 3) if ntile else None}
+        res["dots"] = med(ev(0, i, "dots_done") - ev(0, i, "stage_ready") for i in rng)
+        res["reduce_and_ship"] = med(ev(0, i, "shipped") - ev(0, i, "dots_done") for i in rng)
+        res["tile_period"] = med(ev(0, i, "stage_ready") - ev(0, i - 1, "stage_ready") for i in rng)
+        res["wait_for_stage"] = med(ev(0, i, "stage_ready") - ev(0, i - 1, "shipped") for i in rng)
+        res["shipped_to_published"] = med(ev(0, i, "partials") - ev(0, i, "shipped") for i in rng)
+        res["published_to_group0_counter"] = med(ev(1, i, "xf_start") - ev(0, i, "partials") for i in rng)
+        res["group0_sum"] = med(ev(1, i, "xf_done") - ev(1, i, "xf_start") for i in rng)
+        res["group0_sum_to_all_groups_in"] = med(ev(1, i, "xf_landed") - ev(1, i, "xf_done") for i in rng)
+        res["all_groups_in_to_flag_set"] = med(ev(1, i, "gates_sent") - ev(1, i, "xf_landed") for i in rng)
+        res["flag_set_to_seen_by_cta0"] = med(ev(0, i, "pre_arrived") - ev(1, i, "gates_sent") for i in rng)
+        res["shipped_to_flag_seen"] = med(ev(0, i, "pre_arrived") - ev(0, i, "shipped") for i in rng)
+        res["sinkhorn"] = med(ev(1, i, "sink_done") - ev(1, i, "gates_sent") for i in rng)
+        res["collapse"] = med(ev(0, i, "collapsed") - ev(0, i, "pre_arrived") for i in rng)
+        res["collapse_period"] = med(ev(0, i, "collapsed") - ev(0, i - 1, "collapsed") for i in rng)
+        res["refill_to_stage_ready"] = med(ev(0, i + 24, "stage_ready") - ev(0, i, "refilled") for i in rng)
+        return res
+
+    wide = hc.hc_pre_auto_path(T, s, d) == hc.HC_PATH_WIDE
+    an = analyse_wide if wide else analyse
+    line = {"stamps": {"workload": workload_config(w)["workload"],
+                       "unit": "µs, median over tiles", "path": "wide" if wide else "cluster",
+                       "pre_chain": an(read(pre)), "fused_boundary": an(read(boundary))}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -772,6 +893,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-head", action="store_true", help="skip the gated-head exit measurement")
     ap.add_argument("--rounds", type=int, default=5, help="rounds of the per-kernel timing")
+    ap.add_argument("--stamps", action="store_true",
+                    help="per-phase timing from the phase-stamp build of the fused pre kernel (not a bench line)")
     ap.add_argument("--round-launches", type=int, default=300, help="back-to-back launches per round")
     args = ap.parse_args(argv)
     if args.warmup < 3:
@@ -781,6 +904,8 @@ def main(argv=None):
         ap.error(f"--gpus {args.gpus} but WORLD_SIZE={world}")
     if args.impl == "reference":
         return run_reference(args)
+    if args.stamps:
+        return run_stamps(args)
     return run_gpu(args)
 
 

@@ -66,9 +66,13 @@ enum hc_status {
 enum hc_pre_path {
     HC_PATH_AUTO = 0,     /* what hc_pre_fused runs                                   */
     HC_PATH_GENERIC = 1,  /* any supported shape: split-K mixes kernel + finish kernel */
-    HC_PATH_CLUSTER = 2   /* one fused launch, x read once: thread-block clusters split
+    HC_PATH_CLUSTER = 2,  /* one fused launch, x read once: thread-block clusters split
                              the hidden dimension; needs s <= 4 and s*d <= 16384 with
                              d % 64 == 0                                               */
+    HC_PATH_WIDE = 3      /* one fused launch over every SM, x read once, for 5 <= s <= 8:
+                             each CTA keeps a fixed hidden range of fn_w resident; needs a
+                             balanced split of d (e.g. s = 8 with d % 8 == 0 and d >= 256,
+                             s = 5 or 7 with d % 64 == 0 and d >= 2048)                */
 };
 
 /* Human-readable name of a status code (static string, never NULL). */
@@ -151,9 +155,10 @@ int hc_pre_auto_path(int T, int s, int d);
  * Same arguments, layouts, validation and results as hc_pre_fused run on the
  * generic path (HC_PATH_GENERIC), minus workspace and ws_bytes.  The split-K
  * scratch lives in a 4 MiB static device buffer inside the library, which every
- * GPU that loads the library holds until the process exits; shapes needing
- * more than that (hc_pre_workspace_bytes(T, s, d) > 4 MiB, e.g. T above about
- * 41,000 at s = 4) return HC_ERR_TOO_LARGE before anything runs.  The call
+ * GPU that loads the library holds until the process exits; shapes whose
+ * generic-path scratch (the 256-byte status block and the split-K partial
+ * sums) needs more than that (e.g. T above about 41,000 at s = 4) return
+ * HC_ERR_TOO_LARGE before anything runs.  The call
  * allocates nothing (no cudaMalloc, cudaFree or allocating library routine).
  * Its first call on a device looks the buffer's address up with that device
  * current; make that first call before any stream capture.  All calls share the

@@ -92,6 +92,19 @@ bool dims_ok(int T, int s, int d)
 
 int cuda_rc(cudaError_t e) { return e == cudaSuccess ? HC_OK : HC_ERR_CUDA; }
 
+// Workspace bytes the given (resolved) kernel path needs; hc_pre_workspace_bytes is the
+// largest over the paths, so a workspace of that size serves any of them.
+size_t path_workspace_bytes(int path, int T, int s, int d)
+{
+    const size_t status = kStatusBytes + hc::kWorkspaceExtra;
+    size_t need = status;
+    if (path == HC_PATH_GENERIC)
+        need = hc::generic_workspace_bytes(T, s, d);
+    else if (path == HC_PATH_WIDE)
+        need = hc::wide_workspace_bytes(T, s, d);
+    return need > status ? need : status;
+}
+
 cudaStream_t as_stream(void *s) { return static_cast<cudaStream_t>(s); }
 
 }  // namespace
@@ -171,9 +184,13 @@ size_t hc_pre_workspace_bytes(int T, int s, int d)
 {
     if (!dims_ok(T, s, d))
         return 0;
-    // Any path may be asked for, so size for the larger of the two.
+    // Any path may be asked for, so size for the larger of the two (a phase-stamp build
+    // keeps its stamps after the status block).
     const size_t g = hc::generic_workspace_bytes(T, s, d);
-    return g > kStatusBytes ? g : kStatusBytes;
+    const size_t c = kStatusBytes + hc::kWorkspaceExtra;
+    const size_t w = hc::wide_workspace_bytes(T, s, d);
+    const size_t m = g > c ? g : c;
+    return m > w ? m : w;
 }
 
 int hc_workspace_init(void *workspace, size_t ws_bytes, void *stream)
@@ -202,7 +219,9 @@ int hc_pre_auto_path(int T, int s, int d)
     (void)T;
     if (!dims_ok(T, s, d) || d % 4)
         return HC_PATH_GENERIC;
-    return hc::cluster_supported(s, d) ? HC_PATH_CLUSTER : HC_PATH_GENERIC;
+    if (hc::cluster_supported(s, d))
+        return HC_PATH_CLUSTER;
+    return hc::wide_supported(s, d) ? HC_PATH_WIDE : HC_PATH_GENERIC;
 }
 
 int hc_pre_fused_path(const float *x, const float *fn_w, const float *scale, const float *base,
@@ -211,7 +230,7 @@ int hc_pre_fused_path(const float *x, const float *fn_w, const float *scale, con
 {
     if (!dims_ok(T, s, d) || iters < 1 || !(eps > 0.f) || !std::isfinite(eps))
         return HC_ERR_DIM;
-    if (path != HC_PATH_AUTO && path != HC_PATH_GENERIC && path != HC_PATH_CLUSTER)
+    if (path != HC_PATH_AUTO && path != HC_PATH_GENERIC && path != HC_PATH_CLUSTER && path != HC_PATH_WIDE)
         return HC_ERR_DIM;
     if (T == 0)
         return HC_OK;
@@ -235,7 +254,9 @@ int hc_pre_fused_path(const float *x, const float *fn_w, const float *scale, con
             if (overlap(outs[o], out_b[o], outs[o2], out_b[o2]))
                 return HC_ERR_ALIAS;
     }
-    if (!workspace || !aligned(workspace, 16) || ws_bytes < hc_pre_workspace_bytes(T, s, d))
+    if (path == HC_PATH_AUTO)
+        path = hc_pre_auto_path(T, s, d);
+    if (!workspace || !aligned(workspace, 16) || ws_bytes < path_workspace_bytes(path, T, s, d))
         return HC_ERR_WORKSPACE;
     for (int o = 0; o < 4; ++o)
         if (overlap(outs[o], out_b[o], workspace, ws_bytes))
@@ -244,14 +265,18 @@ int hc_pre_fused_path(const float *x, const float *fn_w, const float *scale, con
         if (overlap(ins[i], in_b[i], workspace, ws_bytes))
             return HC_ERR_ALIAS;
 
-    if (path == HC_PATH_AUTO)
-        path = hc::cluster_supported(s, d) ? HC_PATH_CLUSTER : HC_PATH_GENERIC;
     cudaStream_t st = as_stream(stream);
     if (path == HC_PATH_CLUSTER) {
         if (!hc::cluster_supported(s, d))
             return HC_ERR_UNSUPPORTED;
         return cuda_rc(hc::launch_pre_cluster(x, fn_w, scale, base, T, s, d, iters, eps, pre, post,
                                               comb, y, workspace, st));
+    }
+    if (path == HC_PATH_WIDE) {
+        if (!hc::wide_supported(s, d))
+            return HC_ERR_UNSUPPORTED;
+        return cuda_rc(hc::launch_pre_wide(x, fn_w, scale, base, T, s, d, iters, eps, pre, post, comb,
+                                           y, workspace, st));
     }
     return cuda_rc(hc::launch_pre_generic(x, fn_w, scale, base, T, s, d, iters, eps, pre, post,
                                           comb, y, workspace, st));
@@ -333,7 +358,7 @@ int hc_post_pre_fused_path(const float *x_prev, const float *f, const float *pos
 {
     if (!dims_ok(T, s, d) || iters < 1 || !(eps > 0.f) || !std::isfinite(eps))
         return HC_ERR_DIM;
-    if (path != HC_PATH_AUTO && path != HC_PATH_GENERIC && path != HC_PATH_CLUSTER)
+    if (path != HC_PATH_AUTO && path != HC_PATH_GENERIC && path != HC_PATH_CLUSTER && path != HC_PATH_WIDE)
         return HC_ERR_DIM;
     if (T == 0)
         return HC_OK;
@@ -359,7 +384,11 @@ int hc_post_pre_fused_path(const float *x_prev, const float *f, const float *pos
             if (overlap(outs[o], out_b[o], outs[o2], out_b[o2]))
                 return HC_ERR_ALIAS;
     }
-    if (!workspace || !aligned(workspace, 16) || ws_bytes < hc_pre_workspace_bytes(T, s, d))
+    if (path == HC_PATH_AUTO) {
+        path = hc::cluster_fused_supported(s, d) ? HC_PATH_CLUSTER
+                                                  : (hc::wide_supported(s, d) ? HC_PATH_WIDE : HC_PATH_GENERIC);
+    }
+    if (!workspace || !aligned(workspace, 16) || ws_bytes < path_workspace_bytes(path, T, s, d))
         return HC_ERR_WORKSPACE;
     for (int o = 0; o < 5; ++o)
         if (overlap(outs[o], out_b[o], workspace, ws_bytes))
@@ -368,8 +397,6 @@ int hc_post_pre_fused_path(const float *x_prev, const float *f, const float *pos
         if (overlap(ins[i], in_b[i], workspace, ws_bytes))
             return HC_ERR_ALIAS;
 
-    if (path == HC_PATH_AUTO)
-        path = hc::cluster_fused_supported(s, d) ? HC_PATH_CLUSTER : HC_PATH_GENERIC;
     cudaStream_t st = as_stream(stream);
     if (path == HC_PATH_CLUSTER) {
         if (!hc::cluster_fused_supported(s, d))
@@ -377,10 +404,16 @@ int hc_post_pre_fused_path(const float *x_prev, const float *f, const float *pos
         return cuda_rc(hc::launch_post_pre_cluster(x_prev, f, post_prev, comb_prev, fn_w, scale, base, T, s, d,
                                                    iters, eps, x_new, pre, post, comb, y, workspace, st));
     }
-    // Shapes the fused kernel does not take: hc_post, then the generic pre-chain on its output.
+    if (path == HC_PATH_WIDE && !hc::wide_supported(s, d))
+        return HC_ERR_UNSUPPORTED;
+    // Shapes the fused kernel does not take: hc_post, then the pre-chain (wide or generic
+    // path) on its output.
     const cudaError_t e = hc::launch_post(x_prev, f, post_prev, comb_prev, x_new, T, s, d, st);
     if (e != cudaSuccess)
         return HC_ERR_CUDA;
+    if (path == HC_PATH_WIDE)
+        return cuda_rc(hc::launch_pre_wide(x_new, fn_w, scale, base, T, s, d, iters, eps, pre, post, comb, y,
+                                           workspace, st));
     return cuda_rc(hc::launch_pre_generic(x_new, fn_w, scale, base, T, s, d, iters, eps, pre, post, comb, y,
                                           workspace, st));
 }
@@ -400,10 +433,12 @@ int hc_head_path(const float *x, const float *fn_w, const float *scale, const fl
 {
     if (!dims_ok(T, s, d) || !(eps > 0.f) || !std::isfinite(eps))
         return HC_ERR_DIM;
-    if (path != HC_PATH_AUTO && path != HC_PATH_GENERIC && path != HC_PATH_CLUSTER)
+    if (path != HC_PATH_AUTO && path != HC_PATH_GENERIC && path != HC_PATH_CLUSTER && path != HC_PATH_WIDE)
         return HC_ERR_DIM;
     if (T == 0)
         return HC_OK;
+    if (path == HC_PATH_WIDE)
+        return HC_ERR_UNSUPPORTED;   // the gated head has no wide-stream kernel
     if (!x || !fn_w || !scale || !base || !y)
         return HC_ERR_NULL;
     if (d % 4 || !aligned(x, 16) || !aligned(fn_w, 16) || !aligned(y, 16) || !aligned(scale, 4) ||
@@ -421,7 +456,9 @@ int hc_head_path(const float *x, const float *fn_w, const float *scale, const fl
                 return HC_ERR_ALIAS;
     if (overlap(gates, gb, y, yb))
         return HC_ERR_ALIAS;
-    if (!workspace || !aligned(workspace, 16) || ws_bytes < hc_pre_workspace_bytes(T, s, d))
+    if (path == HC_PATH_AUTO)
+        path = hc::cluster_supported(s, d, true) ? HC_PATH_CLUSTER : HC_PATH_GENERIC;
+    if (!workspace || !aligned(workspace, 16) || ws_bytes < path_workspace_bytes(path, T, s, d))
         return HC_ERR_WORKSPACE;
     for (int o = 0; o < 2; ++o)
         if (overlap(outs[o], out_b[o], workspace, ws_bytes))
@@ -430,8 +467,6 @@ int hc_head_path(const float *x, const float *fn_w, const float *scale, const fl
         if (overlap(ins[i], in_b[i], workspace, ws_bytes))
             return HC_ERR_ALIAS;
 
-    if (path == HC_PATH_AUTO)
-        path = hc::cluster_supported(s, d, true) ? HC_PATH_CLUSTER : HC_PATH_GENERIC;
     cudaStream_t st = as_stream(stream);
     if (path == HC_PATH_CLUSTER) {
         if (!hc::cluster_supported(s, d, true))

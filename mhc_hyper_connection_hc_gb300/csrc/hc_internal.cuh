@@ -25,6 +25,35 @@ struct StatusBlock {
 };
 static_assert(sizeof(StatusBlock) == kStatusBytes, "status block is 256 bytes");
 
+// ---------------------------------------------------------------- phase stamps
+// A build with -DHC_STAMPS (build.build(stamps=True), a separate library) makes the
+// cluster pre kernel write %globaltimer at phase boundaries of every tile into the
+// workspace, right after the status block: [kStampCtas][kStampTiles][kStampEvents]
+// 64-bit nanosecond stamps, for CTAs 0 and 8 of cluster 0 (the owners of tokens 0 and 8
+// of every tile).  Stamps of tiles beyond kStampTiles are dropped.
+constexpr int kStampCtas = 2, kStampTiles = 256, kStampEvents = 16;
+constexpr size_t kStampBytes = (size_t)kStampCtas * kStampTiles * kStampEvents * 8;
+enum StampEvent : int {
+    kEvStageReady = 0,   // compute warpgroup 0: the tile's stage is ready
+    kEvDotsDone,         // compute warpgroup 0: dots and squares done (thread 0)
+    kEvShipped,          // compute warpgroup 0: partials shipped (thread 0)
+    kEvPartials,         // finisher: every partial of the owned token arrived
+    kEvGatesSent,        // finisher: pre sent to every CTA
+    kEvPreArrived,       // collapse: the tile's pre gates are all in
+    kEvCollapsed,        // collapse: y written
+    kEvRefilled,         // collapse: the stage's next load issued
+    kEvXfStart,          // fused: transform of the tile begins (collapse warps)
+    kEvXfLanded,         // fused: the tile's stage and f slice have landed
+    kEvXfDone,           // fused: x' stored, stage released to the compute warps
+    kEvSinkDone,         // Sinkhorn warp: the tile's comb blocks written
+    kEvKernelStart,      // (tile 0 only) kernel entry
+};
+#ifdef HC_STAMPS
+constexpr size_t kWorkspaceExtra = kStampBytes;
+#else
+constexpr size_t kWorkspaceExtra = 0;
+#endif
+
 enum DevErr : unsigned int {
     kDevOk = 0,
     kDevWaitTimeout = 1,   // a bounded wait on an mbarrier gave up
@@ -70,6 +99,15 @@ cudaError_t launch_pre_generic(const float *x, const float *fn_w, const float *s
                                const float *base, int T, int s, int d, int iters, float eps,
                                float *pre, float *post, float *comb, float *y,
                                void *workspace, cudaStream_t st);
+
+// Wide-stream pre path (5 <= s <= 8): one persistent whole-GPU launch, every CTA a fixed
+// K slice of fn_w in TMEM; wide_supported() says whether the shape has a balanced split
+// and the device can run it.
+size_t wide_workspace_bytes(int T, int s, int d);
+bool wide_supported(int s, int d);
+cudaError_t launch_pre_wide(const float *x, const float *fn_w, const float *scale, const float *base,
+                            int T, int s, int d, int iters, float eps, float *pre, float *post,
+                            float *comb, float *y, void *workspace, cudaStream_t st);
 
 // Cluster pre path (one fused launch).  cluster_supported() says whether the
 // shape fits and the device can co-schedule the clusters.

@@ -60,9 +60,11 @@ extern "C" int hc_pre_fused_noalloc(const float *x, const float *fn_w, const flo
                                     const float *base, int T, int s, int d, int iters, float eps,
                                     float *pre, float *post, float *comb, float *y, void *stream)
 {
-    const size_t need = hc_pre_workspace_bytes(T, s, d);
-    if (need == 0)
+    if (hc_pre_workspace_bytes(T, s, d) == 0)   // 0: the shape is outside the limits
         return HC_ERR_DIM;
+    // This entry point always runs the generic path: only its scratch (the status block
+    // and the split-K partials) has to fit.
+    const size_t need = hc::generic_workspace_bytes(T, s, d);
     if (need > hc::kNoallocScratchBytes)
         return HC_ERR_TOO_LARGE;
     if (T == 0)

@@ -193,9 +193,24 @@ struct Params {
     const float *f, *post_prev, *comb_prev;
     float *x_new;
     StatusBlock *status;
+    unsigned long long *stamps;   // phase stamps (HC_STAMPS builds), else null
     int T, d, hs, hsc, LK, NJ, iters, tm_tile, ntiles;
     float eps, invK;   // invK = 1 / (s*d)
 };
+
+// Phase stamp of tile `it`, event `ev`, by CTAs 0 and 8 of cluster 0 (HC_STAMPS builds only).
+#ifdef HC_STAMPS
+__device__ __forceinline__ void stamp_at(const Params &p, int cid, uint32_t rank, int it, int ev)
+{
+    if (p.stamps && cid == 0 && (rank & 7u) == 0u && it >= 0 && it < kStampTiles)
+        p.stamps[((size_t)(rank >> 3) * kStampTiles + it) * kStampEvents + ev] = ptx::globaltimer();
+}
+#define HC_STAMP(it, ev) stamp_at(p, cid, rank, (it), (ev))
+#else
+#define HC_STAMP(it, ev) \
+    do {                 \
+    } while (0)
+#endif
 
 // Bounded wait on an mbarrier phase.  honor_abort = false is used only to let
 // this CTA's own bulk copies land before it exits.
@@ -450,6 +465,8 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const __gri
     };
 
     // ------------------------------------------------------------------ set-up
+    if (threadIdx.x == 0)
+        HC_STAMP(0, kEvKernelStart);
     if (threadIdx.x == 0) {
         for (int s = 0; s < L.nst; ++s) {
             ptx::mbar_init(BAR(kBarXFull + s), 1);
@@ -559,6 +576,8 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const __gri
                 threadIdx.x != 0 || wait_bar<true>(BAR(kBarPre + q), (itc / kNQ) & 1, abort_flag, sb, kSitePre);
             if (!ptx::named_bar_and(1, kComputeThreads, got))
                 return false;
+            if (threadIdx.x == 0)
+                HC_STAMP(itc, kEvPreArrived);
             int t0, tm;
             tile_tokens(itc, t0, tm);
             const int s = itc % L.nst;
@@ -584,6 +603,8 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const __gri
                 }
                 *reinterpret_cast<float4 *>(p.y + (size_t)(t0 + t) * p.d + (size_t)rank * p.hs + 4 * h4) = a;
             }
+            if (threadIdx.x == 0)
+                HC_STAMP(itc, kEvCollapsed);
             return true;
         };
 
@@ -636,6 +657,8 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const __gri
                      (!tf_here || wait_bar<false>(BAR(kBarFFull), it & 1, abort_flag, sb, kSiteXFull))));
             if (!ok)
                 break;
+            if (threadIdx.x == 0)   // compute stamps: warpgroup 0
+                HC_STAMP(it, kEvStageReady);
             int t0, tm;
             tile_tokens(it, t0, tm);
             if (tf_here) {
@@ -739,6 +762,8 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const __gri
                     dots_step_smem<G::B, NT, RG, C::NSS>(acc, ssa, w, xs_addr, cofs, lk4, rg);
                 }
             }
+            if (threadIdx.x == 0)
+                HC_STAMP(it, kEvDotsDone);
             if (!arrived) {
                 ptx::named_bar_arrive(kNbStagger, kComputeThreads);
                 arrived = true;
@@ -782,6 +807,8 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const __gri
                                       ptx::mapa(BAR(kBarRecv + qb), t));
                 }
             }
+            if (threadIdx.x == 0)
+                HC_STAMP(it, kEvShipped);
             if (!PERSIST) {
                 if (threadIdx.x == 0)   // the owners will answer with tm pre gates
                     ptx::mbar_arrive_expect_tx(BAR(kBarPre + qb), (uint32_t)(tm * 16));
@@ -835,6 +862,8 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const __gri
                     __syncwarp();
                     break;
                 }
+                if (lane == 0)
+                    HC_STAMP(it, kEvPartials);
                 if (own) {
                     float val = 0.f;
                     if (lane <= G::R) {
@@ -868,6 +897,8 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const __gri
                         const uint32_t dst = ptx::smem_u32(sinkbuf + (int)rank * 16 + (lane - 2 * S));
                         ptx::st_async_f32(ptx::mapa(dst, sc), __expf(logit), ptx::mapa(BAR(kBarSink), sc));
                     }
+                    if (lane == 0)
+                        HC_STAMP(it, kEvGatesSent);
                     const size_t tok = (size_t)t0 + rank;
                     if (lane < S) {
                         if (p.pre)   // the head's gates are an optional output
@@ -906,8 +937,10 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const __gri
                         dst[q] = cm[q];
                 }
                 __syncwarp();
-                if (lane == 0)
+                if (lane == 0) {
+                    HC_STAMP(it, kEvSinkDone);
                     ptx::mbar_arrive(BAR(kBarSinkDone));   // the buffer may be refilled
+                }
             }
         } else if (PERSIST && warp >= kCollapseWarp0) {
             // -------------------------------------------------------------- collapse warps
@@ -930,6 +963,8 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const __gri
                 const int s = k % L.nst;
                 int t0, tm;
                 tile_tokens(k, t0, tm);
+                if (ct == 0)
+                    HC_STAMP(k, kEvXfStart);
                 for (int e = ct; e < tm * NC; e += kCollapseThreads) {   // the tile's post / comb
                     const int tt = e / NC, cc = e - tt * NC;
                     coefs[e] = cc < S ? __ldg(p.post_prev + (size_t)(t0 + tt) * S + cc)
@@ -941,6 +976,8 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const __gri
                           wait_bar<false>(BAR(kBarFFull), k & 1, abort_flag, sb, kSiteXFull);
                 if (!ptx::named_bar_and(kNbCollapse, kCollapseThreads, got))
                     return false;
+                if (ct == 0)
+                    HC_STAMP(k, kEvXfLanded);
                 if (t < tm) {
                     float cf[NC];
     #pragma unroll
@@ -977,6 +1014,7 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const __gri
                     ptx::tma_store_4d(&p.tmap_xnew, 0, (int)rank * p.hsc, 0, t0, ptx::smem_u32(stages + s * stage_floats));
                     ptx::bulk_commit();
                     ptx::mbar_arrive(BAR(kBarXReady + s));   // the compute warps may read x'
+                    HC_STAMP(k, kEvXfDone);
                     if (tile_exists(k + 1))
                         load_f(k + 1);
                 }
@@ -1006,6 +1044,8 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const __gri
                 }
                 if (!ptx::named_bar_and(kNbCollapse, kCollapseThreads, got))
                     break;
+                if (ct == 0)
+                    HC_STAMP(it, kEvPreArrived);
                 if (t < tm) {
                     const float4 pv = ptx::lds128(ptx::smem_u32(preb + (q * kTMT + t) * 4));
                     const float pr[4] = {pv.x, pv.y, pv.z, pv.w};
@@ -1039,12 +1079,15 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const __gri
                     }
                 }
                 ptx::named_bar_sync(kNbCollapse, kCollapseThreads);
+                if (ct == 0)
+                    HC_STAMP(it, kEvCollapsed);
                 if (ct == 0 && tile_exists(it + L.nst)) {
                     // Fused: tile it's x' store has read the stage (only the stores of
                     // tiles it + 1 and it + 2 may still be pending).
                     if (fused)
                         ptx::bulk_wait_read<2>();
                     load_tile(it + L.nst);
+                    HC_STAMP(it, kEvRefilled);
                 }
             }
             if (fused && ct == 0)
@@ -1225,6 +1268,9 @@ cudaError_t run_s(const float *x, const float *fn_w, const float *scale, const f
     p.comb = comb;
     p.y = y;
     p.status = static_cast<StatusBlock *>(workspace);
+#ifdef HC_STAMPS
+    p.stamps = reinterpret_cast<unsigned long long *>(static_cast<char *>(workspace) + kStatusBytes);
+#endif
     p.T = T;
     p.d = d;
     p.hs = d / kCS;

@@ -22,7 +22,7 @@ HC_OK = 0
 HC_ERR_NULL, HC_ERR_DIM, HC_ERR_ALIGN, HC_ERR_ALIAS = 1, 2, 3, 4
 HC_ERR_WORKSPACE, HC_ERR_CUDA, HC_ERR_DEVICE, HC_ERR_UNSUPPORTED = 5, 6, 7, 8
 HC_ERR_TOO_LARGE = 9
-HC_PATH_AUTO, HC_PATH_GENERIC, HC_PATH_CLUSTER = 0, 1, 2
+HC_PATH_AUTO, HC_PATH_GENERIC, HC_PATH_CLUSTER, HC_PATH_WIDE = 0, 1, 2, 3
 
 EXPORTED = ("hc_status_string", "hc_expand", "hc_pre_workspace_bytes", "hc_workspace_init",
             "hc_workspace_status", "hc_pre_fused", "hc_pre_fused_path", "hc_pre_auto_path",

@@ -144,7 +144,14 @@ def test_workspace_sizes(lib):
         for s, d in ((4, 4096), (8, 7168), (1, 4), (3, 12)):
             n = hc.hc_pre_workspace_bytes(T, s, d)
             assert n >= 256 and n % 4 == 0
-            assert n <= 256 + 4 * ((2 + s) * s + 1) * T * 304 + 4 * ((2 + s) * s + 1) * 304
+            generic = 256 + 4 * ((2 + s) * s + 1) * T * 304 + 4 * ((2 + s) * s + 1) * 304
+            # the wide-stream path (s >= 5): per-tile group counters (10 groups), tile
+            # counters and flags, and 24 slots of per-CTA partials and of group sums (R dots
+            # + squares for 4 tokens, at most 160 CTAs in 10 groups)
+            ntiles = (T + 3) // 4
+            rv = (2 + s) * s + 1
+            wide = 256 + 12 * 4 * ntiles + 24 * (160 + 10) * 4 * rv * 4 + 4 * 256 if s >= 5 else 0
+            assert n <= max(generic, wide)
 
 
 def head_rc(lib, x=A, fn_w=A + 32 * MB, scale=A + 40 * MB, base=A + 40 * MB + 64, gates=A + 41 * MB,

@@ -16,7 +16,7 @@ pytestmark = pytest.mark.gpu
 
 SMALL = [  # (T, s, d)
     (1, 4, 4096), (37, 4, 4096), (200, 4, 4096), (150, 2, 2048), (133, 3, 3072), (19, 1, 1024),
-    (17, 3, 4100), (5, 8, 7168), (33, 6, 40), (130, 1, 1024), (300, 4, 2048),
+    (17, 3, 4100), (5, 8, 7168), (33, 6, 40), (130, 1, 1024), (300, 4, 2048), (37, 8, 7168), (9, 5, 4096),
 ]
 
 
@@ -56,8 +56,9 @@ class Fused:
 def _paths(s, d):
     from mhc_hyper_connection_hc_gb300 import hc
     out = [hc.HC_PATH_GENERIC]
-    if hc.hc_pre_auto_path(1, s, d) == hc.HC_PATH_CLUSTER:
-        out.append(hc.HC_PATH_CLUSTER)
+    auto = hc.hc_pre_auto_path(1, s, d)
+    if auto in (hc.HC_PATH_CLUSTER, hc.HC_PATH_WIDE):
+        out.append(auto)
     return out
 
 

@@ -41,12 +41,14 @@ def _up(a):
 def _paths(s, d):
     from mhc_hyper_connection_hc_gb300 import hc
     out = [hc.HC_PATH_GENERIC]
-    if hc.hc_pre_auto_path(1, s, d) == hc.HC_PATH_CLUSTER:
-        out.append(hc.HC_PATH_CLUSTER)
+    auto = hc.hc_pre_auto_path(1, s, d)
+    if auto in (hc.HC_PATH_CLUSTER, hc.HC_PATH_WIDE):
+        out.append(auto)
     return out
 
 
-@pytest.mark.parametrize("T,s,d", [(37, 4, 4096), (19, 1, 1024), (133, 3, 3072), (17, 3, 4100), (5, 8, 7168)])
+@pytest.mark.parametrize("T,s,d", [(37, 4, 4096), (19, 1, 1024), (133, 3, 3072), (17, 3, 4100), (5, 8, 7168),
+                                   (130, 8, 2048), (9, 5, 4096)])
 def test_outputs_stay_inside_their_buffers(T, s, d):
     from mhc_hyper_connection_hc_gb300 import hc
     inp = synth.site_inputs(970 + T, T, s, d)
@@ -66,7 +68,8 @@ def test_outputs_stay_inside_their_buffers(T, s, d):
                              path=path)
         hw, hs, hb = (_up(a) for a in synth.head_params(970 + T, s, d))
         hd = {"gates": Guarded((T, s)), "y": Guarded((T, d))}
-        hc.hc_head(dv["x"], hw, hs, hb, 1e-6, hd["y"].t, ws, gates=hd["gates"].t, path=path)
+        hpath = hc.HC_PATH_AUTO if path == hc.HC_PATH_WIDE else path   # the head has no wide kernel
+        hc.hc_head(dv["x"], hw, hs, hb, 1e-6, hd["y"].t, ws, gates=hd["gates"].t, path=hpath)
         torch.cuda.synchronize()
         assert hc.hc_workspace_status(ws) == 0
         for name, b in list(g.items()) + [("fused " + k, v) for k, v in fz.items()] + \

@@ -22,14 +22,17 @@ SMALL = [  # (T, s, d)
     (1, 4, 4096), (8, 4, 4096), (37, 4, 4096), (16, 4, 1024), (19, 1, 1024), (3, 2, 64),
     (17, 3, 4100), (2, 5, 12), (33, 6, 40), (4, 7, 8), (1, 8, 4), (5, 8, 7168), (40, 2, 2048),
     (21, 3, 3072), (200, 4, 4096), (150, 2, 2048), (130, 1, 1024), (133, 3, 3072), (300, 4, 2048),
+    # wide-stream kernel shapes (s >= 5): several tiles, ragged tails, unequal CTA widths
+    (37, 8, 7168), (9, 5, 4096), (33, 6, 4096), (17, 7, 7168), (130, 8, 2048), (1, 8, 7168),
 ]
 
 
 def _paths(s, d):
     from mhc_hyper_connection_hc_gb300 import hc
     paths = [hc.HC_PATH_GENERIC]
-    if hc.hc_pre_auto_path(1, s, d) == hc.HC_PATH_CLUSTER:
-        paths.append(hc.HC_PATH_CLUSTER)
+    auto = hc.hc_pre_auto_path(1, s, d)
+    if auto in (hc.HC_PATH_CLUSTER, hc.HC_PATH_WIDE):
+        paths.append(auto)
     return paths
 
 
@@ -277,3 +280,32 @@ def test_prefill_batch_tokens_equal_single_token_calls():
             assert torch.equal(gg[k].view(torch.int32), ref[k][t:t + 1].contiguous().view(torch.int32)), \
                 f"{k} of token {t} differs between T=1 and T={T}"
     assert big.status() == 0 and one.status() == 0
+
+
+def test_wide_stream_batch_tokens_equal_single_token_calls():
+    """Tokens of the full wide-stream workload (T = 2048, s = 8, d = 7168) carry the same
+    bits as the same tokens run alone, on the wide-stream kernel (one K split for every
+    T, a fixed summation order over CTAs)."""
+    from mhc_hyper_connection_hc_gb300 import hc
+    w = synth.WORKLOADS[5]
+    T, s, d = w.T, w.s, w.d
+    if hc.hc_pre_auto_path(T, s, d) != hc.HC_PATH_WIDE:
+        pytest.skip("wide-stream kernel not available")
+    inp = synth.workload_inputs(w)
+    big = GpuSite(T, s, d)
+    dev = {k: big.upload(v) for k, v in inp.items()}
+    g = big.pre(dev["x"], dev["fn_w"], dev["scale"], dev["base"], w.iters, w.eps)
+    ref = {k: g[k].clone() for k in ("pre", "post", "comb", "y")}
+    g = big.pre(dev["x"], dev["fn_w"], dev["scale"], dev["base"], w.iters, w.eps)   # a rerun: same bits
+    for k in ref:
+        assert torch.equal(g[k].view(torch.int32), ref[k].view(torch.int32)), k
+    for n in (1, 5):
+        small = GpuSite(n, s, d)
+        for t in sample_tokens(T - n + 1, n=8):
+            gg = small.pre(dev["x"][t:t + n].contiguous(), dev["fn_w"], dev["scale"], dev["base"], w.iters,
+                           w.eps)
+            for k in ref:
+                assert torch.equal(gg[k].view(torch.int32), ref[k][t:t + n].contiguous().view(torch.int32)), \
+                    f"{k} of tokens {t}..{t + n} differs between T={n} and T={T}"
+        assert small.status() == 0
+    assert big.status() == 0
