@@ -757,7 +757,7 @@ def measure_decode(dev, iters=None, n_sites: int = 300):
 
 STAMP_EVENTS = ("stage_ready", "dots_done", "shipped", "partials", "gates_sent", "pre_arrived", "collapsed",
                 "refilled", "xf_start", "xf_landed", "xf_done", "sink_done", "kernel_start")
-STAMP_TILES, STAMP_EV, STAMP_CTAS = 256, 16, 2
+STAMP_TILES, STAMP_EV, STAMP_CTAS = 512, 16, 2
 
 
 def run_stamps(args):
@@ -837,7 +837,8 @@ def run_stamps(args):
 
     def analyse_wide(st):
         """The wide-stream kernel's stamps: slot 0 CTA 0 (compute warp 0, publisher, collapse
-        warp); slot 1 group 0's sum and the finish of every tile, whichever CTA did them."""
+        warp); slot 1 the reduction of column 0 and the finish of every tile, whichever CTA
+        did them."""
         E = {n: i for i, n in enumerate(STAMP_EVENTS)}
         t0 = st[0, 0, E["kernel_start"]]
         ntile = int(np.max(np.nonzero(st[0, :, E["stage_ready"]])[0])) + 1 if np.any(st[0, :, E["stage_ready"]]) else 0
@@ -847,24 +848,31 @@ def run_stamps(args):
             return v if v > 0 else np.nan
 
         rng = range(2, ntile) if ntile > 4 else range(0, ntile)
+        ready = np.sort(st[0, :ntile, E["stage_ready"]])
         res = {"tiles_stamped": ntile,
-               "kernel_us": round(float(np.nanmax(st[0, :ntile, :12]) - t0), 3) if ntile else None,
+               "kernel_us": round(float(np.nanmax(st[:, :ntile, :]) - t0), 3) if ntile else None,
                "first_stage_ready_us": round(float(ev(0, 0, "stage_ready") - t0), 3) if ntile else None}
         res["dots"] = med(ev(0, i, "dots_done") - ev(0, i, "stage_ready") for i in rng)
         res["reduce_and_ship"] = med(ev(0, i, "shipped") - ev(0, i, "dots_done") for i in rng)
         res["tile_period"] = med(ev(0, i, "stage_ready") - ev(0, i - 1, "stage_ready") for i in rng)
         res["wait_for_stage"] = med(ev(0, i, "stage_ready") - ev(0, i - 1, "shipped") for i in rng)
         res["shipped_to_published"] = med(ev(0, i, "partials") - ev(0, i, "shipped") for i in rng)
-        res["published_to_group0_counter"] = med(ev(1, i, "xf_start") - ev(0, i, "partials") for i in rng)
-        res["group0_sum"] = med(ev(1, i, "xf_done") - ev(1, i, "xf_start") for i in rng)
-        res["group0_sum_to_all_groups_in"] = med(ev(1, i, "xf_landed") - ev(1, i, "xf_done") for i in rng)
-        res["all_groups_in_to_flag_set"] = med(ev(1, i, "gates_sent") - ev(1, i, "xf_landed") for i in rng)
+        res["shipped_to_refill_issued"] = med(ev(0, i, "refilled") - ev(0, i, "shipped") for i in rng)
+        res["published_to_all_ctas_in"] = med(ev(1, i, "xf_start") - ev(0, i, "partials") for i in rng)
+        res["column0_sum"] = med(ev(1, i, "xf_done") - ev(1, i, "xf_start") for i in rng)
+        res["column0_sum_to_all_columns_in"] = med(ev(1, i, "xf_landed") - ev(1, i, "xf_done") for i in rng)
+        res["all_columns_in_to_flag_set"] = med(ev(1, i, "gates_sent") - ev(1, i, "xf_landed") for i in rng)
         res["flag_set_to_seen_by_cta0"] = med(ev(0, i, "pre_arrived") - ev(1, i, "gates_sent") for i in rng)
         res["shipped_to_flag_seen"] = med(ev(0, i, "pre_arrived") - ev(0, i, "shipped") for i in rng)
         res["sinkhorn"] = med(ev(1, i, "sink_done") - ev(1, i, "gates_sent") for i in rng)
         res["collapse"] = med(ev(0, i, "collapsed") - ev(0, i, "pre_arrived") for i in rng)
         res["collapse_period"] = med(ev(0, i, "collapsed") - ev(0, i - 1, "collapsed") for i in rng)
-        res["refill_to_stage_ready"] = med(ev(0, i + 24, "stage_ready") - ev(0, i, "refilled") for i in rng)
+        # how many tiles CTA 0's dot loop is ahead of its collapse
+        res["collapse_lag_tiles"] = med(float(np.searchsorted(ready, ev(0, i, "collapsed")) - i)
+                                        for i in rng if not np.isnan(ev(0, i, "collapsed")))
+        res["last_collapse_after_last_ship_us"] = (
+            round(float(np.nanmax(st[0, :ntile, E["collapsed"]]) - np.nanmax(st[0, :ntile, E["shipped"]])), 3)
+            if ntile else None)
         return res
 
     wide = hc.hc_pre_auto_path(T, s, d) == hc.HC_PATH_WIDE

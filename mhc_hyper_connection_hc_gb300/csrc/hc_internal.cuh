@@ -31,7 +31,7 @@ static_assert(sizeof(StatusBlock) == kStatusBytes, "status block is 256 bytes");
 // workspace, right after the status block: [kStampCtas][kStampTiles][kStampEvents]
 // 64-bit nanosecond stamps, for CTAs 0 and 8 of cluster 0 (the owners of tokens 0 and 8
 // of every tile).  Stamps of tiles beyond kStampTiles are dropped.
-constexpr int kStampCtas = 2, kStampTiles = 256, kStampEvents = 16;
+constexpr int kStampCtas = 2, kStampTiles = 512, kStampEvents = 16;
 constexpr size_t kStampBytes = (size_t)kStampCtas * kStampTiles * kStampEvents * 8;
 enum StampEvent : int {
     kEvStageReady = 0,   // compute warpgroup 0: the tile's stage is ready
