@@ -509,6 +509,7 @@ def run_gpu(args):
             line["e2e"] = measure_e2e(w, {"x": dv["x"], "f": dv["f"]}, dict(out, x_out=x_out), stream, K, site_on)
     if not args.no_decode:
         line["decode_t1"] = measure_decode(dev, args.iters)
+        line["verify_t8"] = measure_decode(dev, args.iters, cid=2)
     if rank == 0 and world == 1 and not args.no_cpu:
         line["cpu_baseline"] = time_oracle(w, max_tokens=args.cpu_tokens, budget_s=10.0, max_reps=3)
     if rank == 0:
@@ -685,49 +686,73 @@ def measure_head(w, dv, ws, stream, peak, reps: int = 20):
             "note": "gated-head trunk exit on the same state, timed separately from the step"}
 
 
-def measure_decode(dev, iters=None, n_sites: int = 300):
-    """T = 1 site latency: 300 back-to-back sites (pre + post) replayed as one CUDA
-    graph, and the same launches issued eagerly on a stream (iters: Sinkhorn
-    iterations, default the single-decode workload's)."""
+def measure_decode(dev, iters=None, n_sites: int = 300, cid: int = 1):
+    """Latency of the site program at a small token count (the single-decode workload by
+    default; cid=2 the verify batch, its two sites chained, each with its own fn_w): per
+    site, pre-chain + hc_post, from a CUDA graph, and the same launches issued eagerly on a
+    stream, both through the checked per-call binding and through Prepared calls (the
+    arguments checked once), plus the pre-chain alone (iters: Sinkhorn iterations,
+    default the workload's)."""
     import torch
     from mhc_hyper_connection_hc_gb300 import hc
-    w = synth.WORKLOADS[1]
+    w = synth.WORKLOADS[cid]
     if iters is not None:
         w = dataclasses.replace(w, iters=iters)
-    inp = synth.workload_inputs(w)
+    T, S, D = w.T, w.s, w.d
     stream = torch.cuda.Stream(device=dev)
     with torch.cuda.stream(stream):
-        dv = {k: torch.from_numpy(v).to(dev) for k, v in inp.items()}
-        ws = hc.new_workspace(1, w.s, w.d, dev, stream)
-        out = hc.new_pre_outputs(1, w.s, w.d, dev)
-        xo = torch.empty(1, w.s, w.d, device=dev)
+        sites = []
+        for k in range(w.sites):
+            inp = synth.site_inputs(w.cid, T, S, D, w.x_dist, site=k)
+            sites.append({n: torch.from_numpy(v).to(dev) for n, v in inp.items()})
+        ws = hc.new_workspace(T, S, D, dev, stream)
+        out = hc.new_pre_outputs(T, S, D, dev)
+        xs = [sites[0]["x"]] + [torch.empty(T, S, D, device=dev) for _ in range(w.sites)]
     stream.synchronize()
 
-    def site():
-        hc.hc_pre_fused(dv["x"], dv["fn_w"], dv["scale"], dv["base"], w.iters, w.eps, out["pre"],
-                        out["post"], out["comb"], out["y"], ws, stream)
-        hc.hc_post(dv["x"], dv["f"], out["post"], out["comb"], xo, stream)
+    def site_calls(k, prepare=False):
+        sk = sites[k]
+        pre = hc.hc_pre_fused(xs[k], sk["fn_w"], sk["scale"], sk["base"], w.iters, w.eps, out["pre"],
+                              out["post"], out["comb"], out["y"], ws, stream, prepare=prepare)
+        post = hc.hc_post(xs[k], sk["f"], out["post"], out["comb"], xs[k + 1], stream, prepare=prepare)
+        return pre, post
+
+    def chain():
+        for k in range(w.sites):
+            site_calls(k)
 
     def pre_only():
-        hc.hc_pre_fused(dv["x"], dv["fn_w"], dv["scale"], dv["base"], w.iters, w.eps, out["pre"],
+        hc.hc_pre_fused(xs[0], sites[0]["fn_w"], sites[0]["scale"], sites[0]["base"], w.iters, w.eps, out["pre"],
                         out["post"], out["comb"], out["y"], ws, stream)
 
-    res = {}
-    for name, fn in (("site", site), ("pre", pre_only)):
+    prepared = [site_calls(k, prepare=True) for k in range(w.sites)]
+    pre_p = prepared[0][0]
+
+    def chain_prepared():
+        for pre, post in prepared:
+            pre()
+            post()
+
+    res = {"workload": workload_config(w)["workload"]}
+    n_rep = max(1, n_sites // w.sites)
+    for name, fn, per in (("site", chain, w.sites), ("pre", pre_only, 1),
+                          ("site_prepared", chain_prepared, w.sites), ("pre_prepared", pre_p, 1)):
         with torch.cuda.stream(stream):
             for _ in range(20):
                 fn()
             stream.synchronize()
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
-            for _ in range(n_sites):
+            for _ in range(n_rep):
                 fn()
             e1.record(stream)
             stream.synchronize()
-            res[f"us_per_{name}_stream"] = e0.elapsed_time(e1) * 1e3 / n_sites
+            res[f"us_per_{name}_stream"] = e0.elapsed_time(e1) * 1e3 / (n_rep * per)
+            if name.endswith("prepared"):
+                continue
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=stream):
-                for _ in range(n_sites):
+                for _ in range(n_rep):
                     fn()
             g.replay()
             stream.synchronize()
@@ -735,23 +760,25 @@ def measure_decode(dev, iters=None, n_sites: int = 300):
             g.replay()
             e1.record(stream)
             stream.synchronize()
-            res[f"us_per_{name}_graph"] = e0.elapsed_time(e1) * 1e3 / n_sites
+            res[f"us_per_{name}_graph"] = e0.elapsed_time(e1) * 1e3 / (n_rep * per)
     # single launch + synchronize wall (the pages' gate measured this way, with allocations)
     walls = []
     for _ in range(20):
         torch.cuda.synchronize(dev)
         t0 = time.perf_counter()
-        site()
+        site_calls(0)
         stream.synchronize()
         walls.append((time.perf_counter() - t0) * 1e6)
     res["us_per_site_wall_sync"] = statistics.median(walls)
-    cold = measure_cold(stream, pre_only, w.T * w.s * w.d * 4 + w.T * w.d * 4, 1.0)
+    cold = measure_cold(stream, pre_only, T * S * D * 4 + T * D * 4, 1.0)
     res["us_per_pre_l2_cold"] = cold["us"]
-    res["l2_cold_note"] = "one pre-chain launch after a 256 MiB L2 flush: fn_w (1.5 MiB) and x from HBM"
+    res["l2_cold_note"] = "one pre-chain launch after a 256 MiB L2 flush: fn_w and x from HBM"
+    res["stream_note"] = ("_stream: back-to-back eager calls, CUDA events around them (host cost per call "
+                          "included when it exceeds the kernel's); _prepared: the same through Prepared calls")
     if hc.hc_workspace_status(ws, stream) != 0:
-        raise RuntimeError("a kernel flagged an error in the decode measurement")
+        raise RuntimeError("a kernel flagged an error in the latency measurement")
     res["iters"] = w.iters
-    res["path"] = "cluster" if hc.hc_pre_auto_path(1, w.s, w.d) == hc.HC_PATH_CLUSTER else "generic"
+    res["path"] = "cluster" if hc.hc_pre_auto_path(T, S, D) == hc.HC_PATH_CLUSTER else "generic"
     return res
 
 

@@ -87,9 +87,12 @@ const char *hc_status_string(int rc);
 int hc_expand(const float *emb, float *x, int T, int s, int d, void *stream);
 
 /*
- * Bytes of device workspace hc_pre_fused needs for this shape.  The workspace
- * holds a status word (first 256 bytes) and, on the generic path, split-K
- * partial sums.  It must be zeroed once before first use (hc_workspace_init);
+ * Bytes of device workspace hc_pre_fused needs for this shape (the most any
+ * path needs; each call checks ws_bytes against the path it runs).  The
+ * workspace holds a status word (first 256 bytes) and, by path: on the generic
+ * path split-K partial sums; on the wide path the tiles' counters and flags
+ * (zeroed by the call itself, on its stream, before its launch) and per-CTA
+ * partial slots.  It must be zeroed once before first use (hc_workspace_init);
  * every call leaves it valid for the next.  Calls that share a workspace must
  * not run concurrently.
  */
@@ -102,6 +105,13 @@ int hc_workspace_init(void *workspace, size_t ws_bytes, void *stream);
  * Read the workspace status word (synchronises `stream`): HC_OK, or
  * HC_ERR_DEVICE if a kernel gave up on a bounded wait.  The word is sticky
  * until hc_workspace_init clears it.
+ *
+ * Outputs are valid only while the word reads HC_OK.  While it is non-zero,
+ * every later hc_pre_fused, hc_post_pre_fused and hc_head call on that
+ * workspace that runs the cluster or wide path still returns HC_OK (the
+ * host cannot see the word without synchronising) but its kernel does
+ * nothing: pre, post, comb, y, gates and x_new are left as they were.  The
+ * generic path has no waits, never sets the word and runs regardless.
  */
 int hc_workspace_status(const void *workspace, void *stream);
 
@@ -123,9 +133,11 @@ int hc_workspace_status(const void *workspace, void *stream);
  *   workspace, ws_bytes: device scratch of >= hc_pre_workspace_bytes(T, s, d).
  *   Outputs must not overlap x, fn_w, scale, base or each other.
  * Results are float32 and repeated calls are bit-identical (every sum has a
- * fixed order; no floating-point atomics).  On the cluster path a token's
- * results are also the same bits whatever else is in the batch; the generic
- * path sizes its K split by T, so there they may differ in the last bits.
+ * fixed order; no floating-point atomics).  On the cluster and wide paths a
+ * token's results are also the same bits whatever else is in the batch; the
+ * generic path sizes its K split by T, so there they may differ in the last
+ * bits.  Outputs are valid only while hc_workspace_status reads HC_OK (see
+ * there: a non-zero status word makes the cluster and wide kernels skip).
  */
 int hc_pre_fused(const float *x, const float *fn_w, const float *scale, const float *base,
                  int T, int s, int d, int iters, float eps,
@@ -225,9 +237,12 @@ int hc_pre_fused_norm(const float *x, const float *fn_w, const float *scale, con
  * x_new is bit-identical to hc_post's output, and pre/post/comb/y to
  * hc_pre_fused on x_new, on the cluster path; there the new state is formed in
  * shared memory from one read of x_prev, so it is not read back from memory.
- * The cluster path takes the shapes hc_pre_fused's does with d <= 4096; other
- * shapes run hc_post then the generic pre-chain.  Outputs must not overlap
- * any input or each other; workspace as for hc_pre_fused.
+ * The cluster path takes the shapes hc_pre_fused's does with d <= 4096; shapes
+ * the wide path takes run hc_post then the wide pre-chain (two launches, the
+ * same bits as the two calls); other shapes run hc_post then the generic
+ * pre-chain.  Outputs must not overlap any input or each other; workspace as
+ * for hc_pre_fused, and outputs are valid only while hc_workspace_status reads
+ * HC_OK (on the cluster path x_new too is left unwritten while it does not).
  */
 int hc_post_pre_fused(const float *x_prev, const float *f, const float *post_prev,
                       const float *comb_prev, const float *fn_w, const float *scale,
@@ -256,7 +271,9 @@ int hc_post_pre_fused_path(const float *x_prev, const float *f, const float *pos
  *   gates [T, s] (out, optional: NULL skips it), y [T, d] (out),
  *   workspace, ws_bytes: >= hc_pre_workspace_bytes(T, s, d), as for hc_pre_fused.
  * Same conventions, limits, determinism and batch invariance (cluster path) as
- * hc_pre_fused; the cluster path takes the shapes it takes there.
+ * hc_pre_fused; the cluster path takes the shapes it takes there, the wide path
+ * has no head variant (HC_ERR_UNSUPPORTED; HC_PATH_AUTO runs the generic path
+ * for s > 4).
  */
 int hc_head(const float *x, const float *fn_w, const float *scale, const float *base,
             int T, int s, int d, float eps, float *gates, float *y,

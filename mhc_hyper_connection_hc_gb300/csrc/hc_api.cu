@@ -9,6 +9,7 @@
 
 #include <cmath>
 #include <cstdint>
+#include <cstring>
 #include <mutex>
 
 #include "hc_internal.cuh"
@@ -39,6 +40,85 @@ unsigned long long context_id()
     if (get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr || get_id(ctx, &id) != CUDA_SUCCESS)
         return 0;
     return id;
+}
+
+namespace {
+
+struct TmapKey {
+    const void *base;
+    int rank;
+    cuuint64_t dims[5];
+    cuuint64_t strides[4];
+    cuuint32_t box[5];
+};
+
+struct TmapEntry {
+    bool used = false;
+    TmapKey key;
+    CUtensorMap map;
+};
+
+PFN_cuTensorMapEncodeTiled_v12000 tmap_encoder()
+{
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+        else
+            cudaGetLastError();
+    });
+    return fn;
+}
+
+}  // namespace
+
+bool tensor_map_f32(CUtensorMap *out, int rank, const void *base, const cuuint64_t *dims,
+                    const cuuint64_t *strides, const cuuint32_t *box)
+{
+    constexpr int kEntries = 32;
+    static std::mutex mu;
+    static TmapEntry table[kEntries];
+    static int next = 0;
+    if (rank < 1 || rank > 5)
+        return false;
+    TmapKey key;
+    memset(&key, 0, sizeof(key));
+    key.base = base;
+    key.rank = rank;
+    for (int i = 0; i < rank; ++i) {
+        key.dims[i] = dims[i];
+        key.box[i] = box[i];
+        if (i + 1 < rank)
+            key.strides[i] = strides[i];
+    }
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        for (int e = 0; e < kEntries; ++e)
+            if (table[e].used && memcmp(&table[e].key, &key, sizeof(key)) == 0) {
+                *out = table[e].map;
+                return true;
+            }
+    }
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tmap_encoder();
+    if (!enc)
+        return false;
+    const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    if (enc(out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, (cuuint32_t)rank, const_cast<void *>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return false;
+    std::lock_guard<std::mutex> lock(mu);
+    TmapEntry &slot = table[next];
+    next = (next + 1) % kEntries;
+    slot.used = true;
+    slot.key = key;
+    slot.map = *out;
+    return true;
 }
 
 bool device_info(DeviceInfo &out)

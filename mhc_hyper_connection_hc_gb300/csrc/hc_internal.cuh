@@ -4,6 +4,7 @@
 // for sm_103a only: it is compiled with -gencode arch=compute_103a,code=sm_103a.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -80,6 +81,14 @@ bool device_info(DeviceInfo &out);
 // Unique id (cuCtxGetId) of the CUDA context current on the calling thread, 0 if none
 // is current yet.  Per-device set-up (function attributes, symbol addresses) is cached
 // under it, so a device reset, which replaces the context, makes the set-up run again.
+// A float32 tensor map (no interleave or swizzle, 256-byte L2 promotion, zero fill
+// out of bounds, unit element strides) of `rank` dimensions: dims[rank], byte strides of
+// dimensions 1.. (strides[rank-1]), box[rank].  A map depends on nothing but these
+// arguments, so maps are kept in a small table keyed on them and repeated calls on the
+// same buffers and shapes skip the encoder.  False if the encoder is missing or refuses.
+bool tensor_map_f32(CUtensorMap *out, int rank, const void *base, const cuuint64_t *dims,
+                    const cuuint64_t *strides, const cuuint32_t *box);
+
 unsigned long long context_id();
 
 // ---------------------------------------------------------------- launchers (host)

@@ -483,7 +483,10 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const __gri
         ptx::mbar_init(BAR(kBarFFull), 1);
         for (int s = 0; s < kNstPersist; ++s)
             ptx::mbar_init(BAR(kBarXReady + s), 1);   // fused persistent: the stage holds x'
-        *abort_flag = 0;
+        // A non-zero status word (an earlier launch on this workspace timed out) makes
+        // this launch skip its work: 2 marks the skip.  The word only changes 2 s into a
+        // launch, so every CTA of the grid reads the same.
+        *abort_flag = *reinterpret_cast<volatile unsigned *>(&sb->code) != 0u ? 2 : 0;
         ptx::fence_mbar_init_cluster();
     }
     if (!PERSIST && warp < kNCW) {   // padding rows of the staged fn_w slice are zero
@@ -501,8 +504,11 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const __gri
     if (PERSIST)
         ptx::tmem_fence_after_sync();
     const uint32_t tmem_base = PERSIST ? *tmem_slot : 0u;
+    const bool skip = *abort_flag == 2;
 
-    if (warp < kNCW) {
+    if (skip) {
+        // nothing is loaded, computed or written
+    } else if (warp < kNCW) {
         ptx::setmaxnreg_inc<kRegsCompute>();
         // -------------------------------------------------------------- compute warps
         // One thread polls each barrier; a named barrier with an AND reduction then
@@ -1101,7 +1107,7 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const __gri
         ptx::tmem_fence_before_sync();
     ptx::cluster_sync_all();   // no CTA leaves while another may still write its shared memory
     // Every TMA load this CTA issued (by whichever warp) lands before it exits.
-    if (threadIdx.x == 0) {
+    if (threadIdx.x == 0 && !skip) {
         wait_bar<false>(BAR(kBarWFull), 0, abort_flag, sb, kSiteDrain, false);
         for (int s = 0; s < L.nst; ++s)
             if (issued[s] > 0)
@@ -1203,24 +1209,6 @@ struct FusedPost {
     float *x_new;
 };
 
-// cuTensorMapEncodeTiled through the runtime's driver entry point (no libcuda link).
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
-{
-    static std::once_flag once;
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    std::call_once(once, [] {
-        void *f = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-        else
-            cudaGetLastError();
-    });
-    return fn;
-}
-
 // Chunks per slice row: the fewest hsc with hs/hsc <= 256 floats, a multiple of 4.
 int slice_chunks(int hs)
 {
@@ -1234,17 +1222,13 @@ int slice_chunks(int hs)
 // a box of (hc, hsc, s, box_rows); reads past the last row are zero-filled.
 bool encode_slab_map(CUtensorMap *m, const float *base, int rows, int s, int d, int hs, int hsc, int box_rows)
 {
-    PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
-    if (!enc || hsc < 1)
+    if (hsc < 1)
         return false;
     const int hc = hs / hsc;
     const cuuint64_t dims[4] = {(cuuint64_t)hc, (cuuint64_t)(d / hc), (cuuint64_t)s, (cuuint64_t)rows};
     const cuuint64_t strides[3] = {(cuuint64_t)hc * 4, (cuuint64_t)d * 4, (cuuint64_t)s * d * 4};   // bytes
     const cuuint32_t box[4] = {(cuuint32_t)hc, (cuuint32_t)hsc, (cuuint32_t)s, (cuuint32_t)box_rows};
-    const cuuint32_t estr[4] = {1, 1, 1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<float *>(base), dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    return tensor_map_f32(m, 4, base, dims, strides, box);
 }
 
 template <int S, bool HEAD>

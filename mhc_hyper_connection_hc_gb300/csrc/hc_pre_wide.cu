@@ -791,37 +791,14 @@ __global__ void __launch_bounds__(kWThreads, 1) hc_pre_wide_kernel(const __grid_
 
 // ---------------------------------------------------------------------- host side
 
-PFN_cuTensorMapEncodeTiled_v12000 w_encode_fn()
-{
-    static std::once_flag once;
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    std::call_once(once, [] {
-        void *f = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-        else
-            cudaGetLastError();
-    });
-    return fn;
-}
-
 // Map a row-major [rows][s][d] float tensor as (d, s, rows) with a box (hw, s, box_rows);
 // reads past the last row are zero-filled.
 bool w_encode(CUtensorMap *m, const float *base, int rows, int s, int d, int hw, int box_rows)
 {
-    PFN_cuTensorMapEncodeTiled_v12000 enc = w_encode_fn();
-    if (!enc)
-        return false;
     const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)s, (cuuint64_t)rows};
     const cuuint64_t strides[2] = {(cuuint64_t)d * 4, (cuuint64_t)s * d * 4};   // bytes
     const cuuint32_t box[3] = {(cuuint32_t)hw, (cuuint32_t)s, (cuuint32_t)box_rows};
-    const cuuint32_t estr[3] = {1, 1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float *>(base), dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    return tensor_map_f32(m, 3, base, dims, strides, box);
 }
 
 // The hidden split: widths are multiples of the unit u (the smallest multiple of 8 with

@@ -3,7 +3,8 @@
 Argument marshalling only: each function takes torch CUDA tensors, checks their
 dtype, device and contiguity, passes raw device pointers, sizes and the CUDA
 stream handle to the C entry point of the same name, and raises HcError on a
-non-zero status.  Every step of the site program runs in the library's CUDA
+non-zero status.  hc_pre_fused, hc_post and hc_post_pre_fused can instead return a
+Prepared call (prepare=True) that repeats the same call without re-checking.  Every step of the site program runs in the library's CUDA
 kernels; there is no fallback.  If the library has not been built the first
 call raises.
 """
@@ -105,6 +106,34 @@ def _stream(stream) -> ctypes.c_void_p:
     return ctypes.c_void_p(handle)
 
 
+class Prepared:
+    """One library call whose arguments were checked and converted once.  Calling it runs
+    the C entry point again on the same device pointers, sizes and stream, with none of
+    the per-call Python checks: the decode loop's form of a call (the tensors must stay
+    alive, at the same addresses and shapes, for as long as it is used; their contents
+    may change between calls)."""
+
+    __slots__ = ("_fn", "_name", "_args", "_keep")
+
+    def __init__(self, name: str, args: tuple, keep: tuple):
+        self._fn = getattr(load(), name)
+        self._name = name
+        self._args = args
+        self._keep = keep   # the tensors the pointers belong to
+
+    def __call__(self) -> None:
+        rc = self._fn(*self._args)
+        if rc != HC_OK:
+            raise HcError(self._name, rc)
+
+
+def _run(name: str, args: tuple, prepare: bool, keep: tuple):
+    if prepare:
+        return Prepared(name, args, keep)
+    _check(name, getattr(load(), name)(*args))
+    return None
+
+
 def _shape(x: torch.Tensor):
     if x.dim() != 3:
         raise ValueError("stream state must be [T, s, d]")
@@ -121,11 +150,12 @@ def hc_mean(x: torch.Tensor, out: torch.Tensor, stream=None) -> None:
     _check("hc_mean", load().hc_mean(_ptr(x, "x"), _ptr(out, "out"), T, s, d, _stream(stream)))
 
 
-def hc_post(x, f, post, comb, x_out, stream=None) -> None:
+def hc_post(x, f, post, comb, x_out, stream=None, prepare: bool = False):
+    """x_out = post . f + comb^T x.  With prepare=True, returns a Prepared call instead."""
     T, s, d = _shape(x)
-    _check("hc_post", load().hc_post(_ptr(x, "x"), _ptr(f, "f"), _ptr(post, "post"),
-                                     _ptr(comb, "comb"), _ptr(x_out, "x_out"), T, s, d,
-                                     _stream(stream)))
+    args = (_ptr(x, "x"), _ptr(f, "f"), _ptr(post, "post"), _ptr(comb, "comb"), _ptr(x_out, "x_out"), T, s, d,
+            _stream(stream))
+    return _run("hc_post", args, prepare, (x, f, post, comb, x_out))
 
 
 def hc_pre_workspace_bytes(T: int, s: int, d: int) -> int:
@@ -146,16 +176,17 @@ def hc_pre_auto_path(T: int, s: int, d: int) -> int:
 
 
 def hc_pre_fused(x, fn_w, scale, base, iters: int, eps: float, pre, post, comb, y, workspace,
-                 stream=None, path: int | None = None) -> None:
+                 stream=None, path: int | None = None, prepare: bool = False):
+    """The site's pre-chain.  With prepare=True, returns a Prepared call instead."""
     T, s, d = _shape(x)
     args = (_ptr(x, "x"), _ptr(fn_w, "fn_w"), _ptr(scale, "scale"), _ptr(base, "base"), T, s, d,
             int(iters), float(eps), _ptr(pre, "pre"), _ptr(post, "post"), _ptr(comb, "comb"),
             _ptr(y, "y"), _ptr(workspace, "workspace", torch.uint8), workspace.numel(),
             _stream(stream))
+    keep = (x, fn_w, scale, base, pre, post, comb, y, workspace)
     if path is None:
-        _check("hc_pre_fused", load().hc_pre_fused(*args))
-    else:
-        _check("hc_pre_fused_path", load().hc_pre_fused_path(*args, int(path)))
+        return _run("hc_pre_fused", args, prepare, keep)
+    return _run("hc_pre_fused_path", args + (int(path),), prepare, keep)
 
 
 def hc_pre_fused_noalloc(x, fn_w, scale, base, iters: int, eps: float, pre, post, comb, y,
@@ -192,19 +223,21 @@ def hc_pre_fused_norm(x, fn_w, scale, base, iters: int, eps: float, norm_w, eps_
 
 
 def hc_post_pre_fused(x_prev, f, post_prev, comb_prev, fn_w, scale, base, iters: int, eps: float,
-                      x_new, pre, post, comb, y, workspace, stream=None, path: int | None = None) -> None:
+                      x_new, pre, post, comb, y, workspace, stream=None, path: int | None = None,
+                      prepare: bool = False):
     """Site i's hc_post and site i+1's pre-chain in one call: x_new = post_prev . f +
-    comb_prev^T x_prev, then pre/post/comb/y of the next site on x_new."""
+    comb_prev^T x_prev, then pre/post/comb/y of the next site on x_new.  With
+    prepare=True, returns a Prepared call instead."""
     T, s, d = _shape(x_prev)
     args = (_ptr(x_prev, "x_prev"), _ptr(f, "f"), _ptr(post_prev, "post_prev"),
             _ptr(comb_prev, "comb_prev"), _ptr(fn_w, "fn_w"), _ptr(scale, "scale"), _ptr(base, "base"),
             T, s, d, int(iters), float(eps), _ptr(x_new, "x_new"), _ptr(pre, "pre"), _ptr(post, "post"),
             _ptr(comb, "comb"), _ptr(y, "y"), _ptr(workspace, "workspace", torch.uint8),
             workspace.numel(), _stream(stream))
+    keep = (x_prev, f, post_prev, comb_prev, fn_w, scale, base, x_new, pre, post, comb, y, workspace)
     if path is None:
-        _check("hc_post_pre_fused", load().hc_post_pre_fused(*args))
-    else:
-        _check("hc_post_pre_fused_path", load().hc_post_pre_fused_path(*args, int(path)))
+        return _run("hc_post_pre_fused", args, prepare, keep)
+    return _run("hc_post_pre_fused_path", args + (int(path),), prepare, keep)
 
 
 def hc_head(x, fn_w, scale, base, eps: float, y, workspace, gates=None, stream=None,

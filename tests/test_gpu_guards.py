@@ -5,7 +5,8 @@ a byte pattern; after the call the bands must be intact (no out-of-bounds writes
 both kernel paths, at ragged shapes.  And the workspace status word: a code written on
 the host is reported by hc_workspace_status (HC_ERR_DEVICE), survives further calls
 (it is sticky) and is cleared by hc_workspace_init.  The injection uses the generic
-path, whose kernels have no device-side waits."""
+path, whose kernels have no device-side waits; a word set before a cluster- or wide-path
+call makes that kernel skip its work, leaving every output as it was."""
 
 import numpy as np
 import pytest
@@ -107,3 +108,49 @@ def test_device_error_word_is_reported_and_sticky():
     run()
     assert hc.hc_workspace_status(ws) == hc.HC_OK
     assert torch.equal(out["y"], y_before)                                   # the context is still usable
+
+
+@pytest.mark.parametrize("T,s,d", [(37, 4, 4096), (1, 4, 4096), (9, 8, 7168)])
+def test_nonzero_status_word_makes_waiting_kernels_skip(T, s, d):
+    """While the status word is non-zero, the cluster and wide kernels (the ones with
+    bounded waits) do nothing: the call returns HC_OK, every output keeps its sentinel
+    (NaN), the word is unchanged.  After hc_workspace_init the same call writes them."""
+    from mhc_hyper_connection_hc_gb300 import hc
+    path = hc.hc_pre_auto_path(T, s, d)
+    if path not in (hc.HC_PATH_CLUSTER, hc.HC_PATH_WIDE):
+        pytest.skip("shape runs the generic path here")
+    inp = synth.site_inputs(990 + T, T, s, d, "normal" if s > 4 else "uniform")
+    dv = {k: _up(v) for k, v in inp.items()}
+    ws = hc.new_workspace(T, s, d)
+    code = torch.tensor([1, 0, 0, 0], dtype=torch.uint8, device="cuda")
+
+    def sentinel_outputs():
+        out = hc.new_pre_outputs(T, s, d)
+        for v in out.values():
+            v.fill_(float("nan"))
+        return out
+
+    out = sentinel_outputs()
+    ws[:4] = code
+    hc.hc_pre_fused(dv["x"], dv["fn_w"], dv["scale"], dv["base"], 20, 1e-6, out["pre"], out["post"],
+                    out["comb"], out["y"], ws, path=path)
+    x_new = torch.full((T, s, d), float("nan"), device="cuda")
+    fz = sentinel_outputs()
+    post_prev = torch.full((T, s), 0.5, device="cuda")
+    comb_prev = torch.eye(s, device="cuda").expand(T, s, s).contiguous()
+    hc.hc_post_pre_fused(dv["x"], dv["f"], post_prev, comb_prev, dv["fn_w"], dv["scale"], dv["base"], 20, 1e-6,
+                         x_new, fz["pre"], fz["post"], fz["comb"], fz["y"], ws, path=path)
+    torch.cuda.synchronize()
+    assert hc.hc_workspace_status(ws) == hc.HC_ERR_DEVICE
+    assert ws[:4].cpu().tolist() == [1, 0, 0, 0]
+    for name, v in list(out.items()) + [("fused " + k, v) for k, v in fz.items()]:
+        assert bool(torch.isnan(v).all()), f"{name} was written while the status word was set"
+    if path == hc.HC_PATH_CLUSTER:
+        assert bool(torch.isnan(x_new).all()), "x_new was written while the status word was set"
+    hc.hc_workspace_init(ws)
+    hc.hc_pre_fused(dv["x"], dv["fn_w"], dv["scale"], dv["base"], 20, 1e-6, out["pre"], out["post"],
+                    out["comb"], out["y"], ws, path=path)
+    torch.cuda.synchronize()
+    assert hc.hc_workspace_status(ws) == hc.HC_OK
+    for name, v in out.items():
+        assert bool(torch.isfinite(v).all()), f"{name} not written once the word was cleared"
