@@ -492,7 +492,7 @@ def run_gpu(args):
 
     if not args.no_head:
         line["exit_head"] = measure_head(w, dv, ws, stream, peak)
-        line["branch_norm"] = measure_norm(w, out["y"], stream, peak)
+        line["branch_norm"] = measure_norm(w, out["y"], stream, peak, pre_inputs=(dv, ws))
     if not args.no_e2e:
         if fused:
             def boundary_on(bi, bo):
@@ -618,10 +618,13 @@ def measure_e2e(w, dev_in, dev_out, stream, K, run):
             "pipelining": "2 device buffer sets; copy-in, compute and copy-out streams"}
 
 
-def measure_norm(w, y, stream, peak, reps: int = 20):
-    """The branch-input norm with its Q8_0 pair (hc_rms_norm_q8) on the step's y,
-    outside the timed step: mean of `reps` event-timed launches after 3 warm-up
-    launches.  Algorithmic bytes: y read; z, q and the block scales written."""
+def measure_norm(w, y, stream, peak, reps: int = 20, pre_inputs=None):
+    """The branch-input norm with its Q8_0 pair on the step's y, outside the timed step:
+    mean of `reps` event-timed launches after 3 warm-up launches, of hc_rms_norm_q8 alone
+    (algorithmic bytes: y read; z, q and the block scales written), and, with
+    pre_inputs = (dv, ws), of the pre-chain with the norm (hc_pre_fused_norm, one launch
+    on the cluster path) beside the pre-chain alone: their difference is what the norm
+    adds to the site."""
     import torch
     from mhc_hyper_connection_hc_gb300 import hc
     T, d = y.shape
@@ -634,22 +637,43 @@ def measure_norm(w, y, stream, peak, reps: int = 20):
         q = torch.empty(T, d, dtype=torch.int8, device=y.device)
         qs = torch.empty(T, d // 32, dtype=torch.float32, device=y.device)
 
-    def norm():
-        hc.hc_rms_norm_q8(y, norm_w, 1e-5, z, q, qs, stream=stream)
+    def timed(fn):
+        for _ in range(3):
+            fn()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+        for e0, e1 in ev:
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+        stream.synchronize()
+        return statistics.mean(e0.elapsed_time(e1) for e0, e1 in ev) * 1e3
 
-    for _ in range(3):
-        norm()
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
-    for e0, e1 in ev:
-        e0.record(stream)
-        norm()
-        e1.record(stream)
-    stream.synchronize()
-    us = statistics.mean(e0.elapsed_time(e1) for e0, e1 in ev) * 1e3
+    us = timed(lambda: hc.hc_rms_norm_q8(y, norm_w, 1e-5, z, q, qs, stream=stream))
     nbytes = T * d * 4 + T * d * 4 + T * d + T * (d // 32) * 4
     gbs = nbytes / us / 1e3
-    return {"us": us, "algorithmic_bytes": nbytes, "GB/s": gbs, "frac_hbm": gbs / peak,
-            "note": "rms_norm of y (eps 1e-5) and its Q8_0 pair, timed separately from the step"}
+    res = {"us": us, "algorithmic_bytes": nbytes, "GB/s": gbs, "frac_hbm": gbs / peak,
+           "note": "rms_norm of y (eps 1e-5) and its Q8_0 pair, timed separately from the step"}
+    if pre_inputs is not None:
+        dv, ws = pre_inputs
+        with torch.cuda.stream(stream):
+            o = hc.new_pre_outputs(T, w.s, d, y.device)
+        pre_us = timed(lambda: hc.hc_pre_fused(dv["x"], dv["fn_w"], dv["scale"], dv["base"], w.iters, w.eps,
+                                               o["pre"], o["post"], o["comb"], o["y"], ws, stream))
+        def fused(path=None):
+            hc.hc_pre_fused_norm(dv["x"], dv["fn_w"], dv["scale"], dv["base"], w.iters, w.eps, norm_w, 1e-5,
+                                 o["pre"], o["post"], o["comb"], o["y"], z, ws, q=q, q_scale=qs, stream=stream,
+                                 path=path)
+        fz_us = timed(fused)
+        fz_bytes = T * w.s * d * 4 + T * d * 4 * 2 + T * d + T * (d // 32) * 4   # x read; y, z, q, scales written
+        res["pre_fused_norm"] = {
+            "us": fz_us, "pre_alone_us": pre_us, "norm_adds_us": fz_us - pre_us,
+            "separate_calls_us": pre_us + us, "algorithmic_bytes": fz_bytes,
+            "GB/s": fz_bytes / fz_us / 1e3, "frac_hbm": fz_bytes / fz_us / 1e3 / peak,
+            "note": ("hc_pre_fused_norm as called (HC_PATH_AUTO: one launch while the cluster path runs its "
+                     "decode variant, else the pre-chain then the norm kernel)")}
+        if hc.hc_pre_auto_path(T, w.s, d) == hc.HC_PATH_CLUSTER and (d // 16) % 32 == 0:
+            res["pre_fused_norm"]["one_launch_us"] = timed(lambda: fused(hc.HC_PATH_CLUSTER))
+    return res
 
 
 def measure_head(w, dv, ws, stream, peak, reps: int = 20):
@@ -727,6 +751,20 @@ def measure_decode(dev, iters=None, n_sites: int = 300, cid: int = 1):
 
     prepared = [site_calls(k, prepare=True) for k in range(w.sites)]
     pre_p = prepared[0][0]
+    with torch.cuda.stream(stream):
+        norm_w = torch.ones(D, device=dev)
+        z = torch.empty(T, D, device=dev)
+        qn = torch.empty(T, D, dtype=torch.int8, device=dev)
+        qsn = torch.empty(T, D // 32, device=dev)
+
+    def pre_norm():
+        hc.hc_pre_fused_norm(xs[0], sites[0]["fn_w"], sites[0]["scale"], sites[0]["base"], w.iters, w.eps, norm_w,
+                             1e-5, out["pre"], out["post"], out["comb"], out["y"], z, ws, q=qn, q_scale=qsn,
+                             stream=stream)
+
+    def pre_then_norm():
+        pre_only()
+        hc.hc_rms_norm_q8(out["y"], norm_w, 1e-5, z, qn, qsn, stream=stream)
 
     def chain_prepared():
         for pre, post in prepared:
@@ -736,7 +774,8 @@ def measure_decode(dev, iters=None, n_sites: int = 300, cid: int = 1):
     res = {"workload": workload_config(w)["workload"]}
     n_rep = max(1, n_sites // w.sites)
     for name, fn, per in (("site", chain, w.sites), ("pre", pre_only, 1),
-                          ("site_prepared", chain_prepared, w.sites), ("pre_prepared", pre_p, 1)):
+                          ("site_prepared", chain_prepared, w.sites), ("pre_prepared", pre_p, 1),
+                          ("pre_norm", pre_norm, 1), ("pre_then_norm", pre_then_norm, 1)):
         with torch.cuda.stream(stream):
             for _ in range(20):
                 fn()
@@ -774,7 +813,9 @@ def measure_decode(dev, iters=None, n_sites: int = 300, cid: int = 1):
     res["us_per_pre_l2_cold"] = cold["us"]
     res["l2_cold_note"] = "one pre-chain launch after a 256 MiB L2 flush: fn_w and x from HBM"
     res["stream_note"] = ("_stream: back-to-back eager calls, CUDA events around them (host cost per call "
-                          "included when it exceeds the kernel's); _prepared: the same through Prepared calls")
+                          "included when it exceeds the kernel's); _prepared: the same through Prepared calls; "
+                          "pre_norm: hc_pre_fused_norm with the Q8_0 pair (one launch at this size), "
+                          "pre_then_norm: hc_pre_fused then hc_rms_norm_q8")
     if hc.hc_workspace_status(ws, stream) != 0:
         raise RuntimeError("a kernel flagged an error in the latency measurement")
     res["iters"] = w.iters

@@ -211,10 +211,23 @@ int hc_rms_norm_q8(const float *y, const float *norm_w, int T, int d, float eps_
                    float *z, signed char *q, float *q_scale, void *stream);
 
 /*
- * hc_pre_fused_norm -- hc_pre_fused, then hc_rms_norm_q8 on its y (two launches;
- * the pages' v4z does both in one).  Arguments as for those two calls; z, q and
- * q_scale must not overlap any other argument.  Everything is validated before
- * the first launch.
+ * hc_pre_fused_norm -- the pre-chain and the branch input f's norm, the pages' v4z
+ * pre kernel (hc_fused_gate.rs page, the v4z arm: the rms_norm and its int8 / float
+ * pair emitted by the pre kernel after the collapse): hc_pre_fused's outputs plus
+ * hc_rms_norm_q8's z (and q, q_scale) of its y.  Arguments as for those two calls;
+ * z, q and q_scale must not overlap any other argument.  Everything is validated
+ * before anything is launched.
+ * When the cluster path runs the shape and d / 16 is a multiple of 32 (e.g.
+ * s <= 4, d = 4096) it can be ONE launch: each CTA of a cluster sends its share of
+ * every token's sum of y^2 to the other fifteen, then writes z and the Q8_0 pair of
+ * its own columns, so y is not read back by a second kernel.  Its sum of squares has
+ * another fixed order than hc_rms_norm_q8's, so z may differ from the two-call result
+ * in the last bits (still bit-identical run to run, and the same bits at any T).
+ * hc_pre_fused_norm takes the one launch while the cluster path runs its one-tile
+ * decode variant (up to 112 tokens at s = 4, d = 4096 on a GB300), where it is the
+ * faster choice; for larger T, and for other shapes, it runs hc_pre_fused then
+ * hc_rms_norm_q8 (at prefill sizes the persistent kernel's collapse warps, which
+ * would also write z and the pair, are slower than a second launch over every SM).
  */
 int hc_pre_fused_norm(const float *x, const float *fn_w, const float *scale, const float *base,
                       int T, int s, int d, int iters, float eps,
@@ -222,6 +235,19 @@ int hc_pre_fused_norm(const float *x, const float *fn_w, const float *scale, con
                       float *pre, float *post, float *comb, float *y,
                       float *z, signed char *q, float *q_scale,
                       void *workspace, size_t ws_bytes, void *stream);
+
+/*
+ * hc_pre_fused_norm with an explicit kernel path for the pre-chain (enum
+ * hc_pre_path): HC_PATH_CLUSTER is one launch at any T where the shape allows it
+ * (above), else the cluster pre-chain then hc_rms_norm_q8; the other paths are
+ * always the two launches.
+ */
+int hc_pre_fused_norm_path(const float *x, const float *fn_w, const float *scale, const float *base,
+                           int T, int s, int d, int iters, float eps,
+                           const float *norm_w, float eps_norm,
+                           float *pre, float *post, float *comb, float *y,
+                           float *z, signed char *q, float *q_scale,
+                           void *workspace, size_t ws_bytes, void *stream, int path);
 
 /*
  * hc_post_pre_fused -- the boundary between two sites in one call: site i's

@@ -304,9 +304,15 @@ int hc_pre_auto_path(int T, int s, int d)
     return hc::wide_supported(s, d) ? HC_PATH_WIDE : HC_PATH_GENERIC;
 }
 
-int hc_pre_fused_path(const float *x, const float *fn_w, const float *scale, const float *base,
-                      int T, int s, int d, int iters, float eps, float *pre, float *post,
-                      float *comb, float *y, void *workspace, size_t ws_bytes, void *stream, int path)
+}  // extern "C"
+
+namespace {
+
+// Every check of hc_pre_fused_path, with HC_PATH_AUTO resolved into `path`; HC_OK (with
+// nothing to run when T == 0) or the status to return.
+int pre_checks(const float *x, const float *fn_w, const float *scale, const float *base, int T, int s, int d,
+               int iters, float eps, float *pre, float *post, float *comb, float *y, void *workspace,
+               size_t ws_bytes, int &path)
 {
     if (!dims_ok(T, s, d) || iters < 1 || !(eps > 0.f) || !std::isfinite(eps))
         return HC_ERR_DIM;
@@ -344,7 +350,21 @@ int hc_pre_fused_path(const float *x, const float *fn_w, const float *scale, con
     for (int i = 0; i < 4; ++i)
         if (overlap(ins[i], in_b[i], workspace, ws_bytes))
             return HC_ERR_ALIAS;
+    return HC_OK;
+}
 
+}  // namespace
+
+extern "C" {
+
+int hc_pre_fused_path(const float *x, const float *fn_w, const float *scale, const float *base,
+                      int T, int s, int d, int iters, float eps, float *pre, float *post,
+                      float *comb, float *y, void *workspace, size_t ws_bytes, void *stream, int path)
+{
+    const int rc = pre_checks(x, fn_w, scale, base, T, s, d, iters, eps, pre, post, comb, y, workspace, ws_bytes,
+                              path);
+    if (rc != HC_OK || T == 0)
+        return rc;
     cudaStream_t st = as_stream(stream);
     if (path == HC_PATH_CLUSTER) {
         if (!hc::cluster_supported(s, d))
@@ -390,12 +410,12 @@ int hc_rms_norm_q8(const float *y, const float *norm_w, int T, int d, float eps_
     return cuda_rc(hc::launch_rms_norm_q8(y, norm_w, T, d, eps_norm, z, q, q_scale, as_stream(stream)));
 }
 
-int hc_pre_fused_norm(const float *x, const float *fn_w, const float *scale, const float *base, int T, int s,
-                      int d, int iters, float eps, const float *norm_w, float eps_norm, float *pre, float *post,
-                      float *comb, float *y, float *z, signed char *q, float *q_scale, void *workspace,
-                      size_t ws_bytes, void *stream)
+int hc_pre_fused_norm_path(const float *x, const float *fn_w, const float *scale, const float *base, int T,
+                           int s, int d, int iters, float eps, const float *norm_w, float eps_norm, float *pre,
+                           float *post, float *comb, float *y, float *z, signed char *q, float *q_scale,
+                           void *workspace, size_t ws_bytes, void *stream, int path)
 {
-    // Every argument is checked before either launch.
+    // Every argument is checked before anything is launched.
     if (!(eps_norm >= 0.f) || !std::isfinite(eps_norm))
         return HC_ERR_DIM;
     if (T > 0) {
@@ -423,11 +443,36 @@ int hc_pre_fused_norm(const float *x, const float *fn_w, const float *scale, con
                     return HC_ERR_ALIAS;
         }
     }
-    const int rc = hc_pre_fused(x, fn_w, scale, base, T, s, d, iters, eps, pre, post, comb, y, workspace, ws_bytes,
-                                stream);
+    const int asked = path;
+    const int rc = pre_checks(x, fn_w, scale, base, T, s, d, iters, eps, pre, post, comb, y, workspace, ws_bytes,
+                              path);
     if (rc != HC_OK || T == 0)
         return rc;
+    cudaStream_t st = as_stream(stream);
+    // One launch when the cluster path runs the shape and its slices hold whole Q8_0 blocks:
+    // always when that path was asked for, and under HC_PATH_AUTO while the decode variant
+    // runs (above that size the persistent kernel's collapse warps, which would also write
+    // z and the pair, are slower than a second, whole-GPU norm launch).
+    if (path == HC_PATH_CLUSTER && hc::cluster_norm_supported(s, d) &&
+        (asked == HC_PATH_CLUSTER || T <= hc::cluster_decode_tokens(s, d)))
+        return cuda_rc(hc::launch_pre_norm_cluster(x, fn_w, scale, base, T, s, d, iters, eps, norm_w, eps_norm, pre,
+                                                   post, comb, y, z, q, q_scale, workspace, st));
+    if (asked == HC_PATH_CLUSTER && !hc::cluster_supported(s, d))
+        return HC_ERR_UNSUPPORTED;
+    const int rc2 = hc_pre_fused_path(x, fn_w, scale, base, T, s, d, iters, eps, pre, post, comb, y, workspace,
+                                      ws_bytes, stream, path);
+    if (rc2 != HC_OK)
+        return rc2;
     return hc_rms_norm_q8(y, norm_w, T, d, eps_norm, z, q, q_scale, stream);
+}
+
+int hc_pre_fused_norm(const float *x, const float *fn_w, const float *scale, const float *base, int T, int s,
+                      int d, int iters, float eps, const float *norm_w, float eps_norm, float *pre, float *post,
+                      float *comb, float *y, float *z, signed char *q, float *q_scale, void *workspace,
+                      size_t ws_bytes, void *stream)
+{
+    return hc_pre_fused_norm_path(x, fn_w, scale, base, T, s, d, iters, eps, norm_w, eps_norm, pre, post, comb, y,
+                                  z, q, q_scale, workspace, ws_bytes, stream, HC_PATH_AUTO);
 }
 
 int hc_post_pre_fused_path(const float *x_prev, const float *f, const float *post_prev,

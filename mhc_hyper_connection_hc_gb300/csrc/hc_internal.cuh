@@ -124,6 +124,18 @@ bool cluster_shape_ok(int s, int d);
 bool cluster_supported(int s, int d);
 bool cluster_supported(int s, int d, bool head);
 bool cluster_fused_supported(int s, int d);   // fused post -> pre: also d / 16 <= 256
+bool cluster_norm_supported(int s, int d);    // pre + branch-input norm: also (d / 16) % 32 == 0
+// Tokens up to which the cluster path runs its one-tile (decode) variant for this shape (0 if
+// the norm cannot run in it): there the pre-chain and norm in one launch are the faster
+// choice; above it the persistent variant's collapse warps make two launches faster.
+int cluster_decode_tokens(int s, int d);
+// The pre-chain and the branch-input norm (z, and the Q8_0 pair when q is given) in one
+// launch of the cluster kernel.
+cudaError_t launch_pre_norm_cluster(const float *x, const float *fn_w, const float *scale,
+                                    const float *base, int T, int s, int d, int iters, float eps,
+                                    const float *norm_w, float eps_norm, float *pre, float *post, float *comb,
+                                    float *y, float *z, signed char *q, float *q_scale, void *workspace,
+                                    cudaStream_t st);
 cudaError_t launch_pre_cluster(const float *x, const float *fn_w, const float *scale,
                                const float *base, int T, int s, int d, int iters, float eps,
                                float *pre, float *post, float *comb, float *y,

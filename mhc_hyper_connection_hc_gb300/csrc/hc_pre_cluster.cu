@@ -104,11 +104,14 @@ constexpr unsigned kFull = 0xffffffffu;
 // tile it + 3 reach this CTA only after it has shipped tile it + 3, whose stage its
 // collapse of tile it released, so three slots would do; four leave a margin.
 constexpr int kNQ = 4;
+constexpr int kNY = 8;   // slots of the norm's exchange of sums of y^2
+static_assert(kNY * kCS * kTMT <= kTMT * kMaxFusedHs, "the norm's sums fit in the f buffer");
 constexpr int kBarXFull = 0, kBarRecv = 3, kBarPre = kBarRecv + kNQ, kBarSink = kBarPre + kNQ,
               kBarWFull = kBarSink + 1, kBarSinkDone = kBarWFull + 1, kBarFFull = kBarSinkDone + 1,
-              kBarXReady = kBarFFull + 1, kNumBars = kBarXReady + 3;   // kBarXReady: per stage
+              kBarXReady = kBarFFull + 1, kBarYss = kBarXReady + 3, kNumBars = kBarYss + kNY;
+// kBarXReady: per stage; kBarYss: per exchange slot, the branch-input norm's sums of y^2
 enum WaitSite : unsigned {
-    kSiteWFull = 1, kSiteXFull, kSiteRecv, kSitePre, kSiteSink, kSiteDrain, kSiteSinkDone
+    kSiteWFull = 1, kSiteXFull, kSiteRecv, kSitePre, kSiteSink, kSiteDrain, kSiteSinkDone, kSiteYss
 };
 
 // Compute-warp map.  Warp w runs on SM sub-partition w%4, whose TMEM lane quarter it
@@ -145,7 +148,7 @@ struct CT {
 };
 
 struct Lay {   // shared-memory layout in bytes
-    int stage_bytes, nst, off_w, off_recv, off_pre, off_sink, off_coef, off_f, off_bar, off_misc, total;
+    int stage_bytes, nst, off_w, off_recv, off_pre, off_sink, off_coef, off_f, off_yss, off_bar, off_misc, total;
 };
 
 template <int S, bool PERSIST, bool HEAD>
@@ -169,6 +172,9 @@ __host__ __device__ inline Lay make_lay(int LK)
     o += (kTMT * (S + S * S) * 4 + 127) / 128 * 128;
     L.off_f = o;                     // [16 tokens][hs <= 256]: fused post -> pre, the tile's slice of f
     o += kTMT * kMaxFusedHs * 4;
+    // [kNY slots][16 source CTAs][16 tokens]: the norm's sums of y^2, over the f buffer
+    // (the norm runs in the pre-chain mode only, which has no f)
+    L.off_yss = L.off_f;
     L.off_bar = o;
     o += kNumBars * 8;
     L.off_misc = o;                  // TMEM address, abort flag, TMA loads issued per stage, f loads
@@ -192,6 +198,13 @@ struct Params {
     // to x_new), on which this site's pre-chain then runs.
     const float *f, *post_prev, *comb_prev;
     float *x_new;
+    // Branch-input norm (z != nullptr; pre-chain mode only): z = y * rsqrt(mean(y^2) +
+    // eps_norm) * norm_w and, if q != nullptr, its Q8_0 pair (blocks of 32 columns).
+    const float *norm_w;
+    float *z;
+    signed char *q;
+    float *q_scale;
+    float eps_norm, inv_d;   // inv_d = 1 / d
     StatusBlock *status;
     unsigned long long *stamps;   // phase stamps (HC_STAMPS builds), else null
     int T, d, hs, hsc, LK, NJ, iters, tm_tile, ntiles;
@@ -463,6 +476,107 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const __gri
         ptx::tma_load_4d(ptx::smem_u32(fbuf), &p.tmap_f, 0, (int)rank * p.hsc, 0, t0, BAR(kBarFFull));
         *f_issued = *f_issued + 1;
     };
+    // Branch-input norm (p.z set), by 128 threads ct = 0..127: thread (t = ct / 8,
+    // hb = ct % 8) owns float4 columns hb, hb + 8, ... of token t's slice of y (in the
+    // persistent variant exactly the columns its collapse wrote).  (1) ss: its sum of y^2
+    // over them in column order (the persistent collapse accumulates it as it writes y;
+    // the decode variant reads y back); (2) norm_send: an xor tree over the token's eight
+    // threads, then that CTA sum to every CTA of the cluster (st.async, counted on slot
+    // it % kNY of kBarYss); (3) norm_finish, once all 16 CTAs' sums are in: r = rsqrt(their
+    // sum, CTA c into accumulator c % 4 in CTA order, then (a0 + a1) + (a2 + a3), / d +
+    // eps_norm), then z = y * r * norm_w over the thread's columns and, with q, the Q8_0
+    // pair of each block of 32 (one block = the m-th float4 of the token's eight threads;
+    // d / 16 % 32 == 0 keeps blocks inside a CTA's slice).  The persistent collapse
+    // finishes tile it after sending tile it + 1.  Slot reuse: a CTA can send tile
+    // it + kNY's sums only after collapsing it, which needs this CTA's partials of that
+    // tile, so this CTA's stage refill after collapsing tile it + kNY - 3 -- later than
+    // its finish of tile it.
+    float *yss = reinterpret_cast<float *>(smem + L.off_yss);
+    auto norm_send = [&](int it, int ct, float ss) {
+        const int q = it % kNY;
+        ss += __shfl_xor_sync(kFull, ss, 1);
+        ss += __shfl_xor_sync(kFull, ss, 2);
+        ss += __shfl_xor_sync(kFull, ss, 4);
+        if (ct == 0)
+            ptx::mbar_arrive_expect_tx(BAR(kBarYss + q), (uint32_t)(kCS * kTMT * 4));
+        if ((ct & 7) == 0) {
+            const uint32_t dst = ptx::smem_u32(yss + (q * kCS + (int)rank) * kTMT + (ct >> 3));
+            for (int c = 0; c < kCS; ++c)
+                ptx::st_async_f32(ptx::mapa(dst, (uint32_t)c), ss, ptx::mapa(BAR(kBarYss + q), (uint32_t)c));
+        }
+    };
+    auto norm_finish = [&](int it, int ct, uint32_t nb) -> bool {
+        const int q = it % kNY;
+        int t0, tm;
+        tile_tokens(it, t0, tm);
+        const int t = ct >> 3, hb = ct & 7;
+        const bool act = t < tm;
+        const int h4n = p.hs / 4;
+        const size_t col0 = (size_t)rank * p.hs;
+        const size_t row = (size_t)(t0 + (act ? t : 0)) * p.d + col0;
+        bool got = true;
+        if (ct == 0) {
+            got = wait_bar<true>(BAR(kBarYss + q), (it / kNY) & 1, abort_flag, sb, kSiteYss);
+            if (!got)   // giving up: still let the sums already on their way land before exit
+                wait_bar<true>(BAR(kBarYss + q), (it / kNY) & 1, abort_flag, sb, kSiteDrain, false);
+        }
+        if (!ptx::named_bar_and(nb, 128, got))
+            return false;
+        float a4[4] = {0.f, 0.f, 0.f, 0.f};   // CTA c into a4[c % 4], in CTA order
+#pragma unroll
+        for (int c = 0; c < kCS; ++c)
+            a4[c & 3] += yss[(q * kCS + c) * kTMT + t];
+        const float r = rsqrtf(((a4[0] + a4[1]) + (a4[2] + a4[3])) * p.inv_d + p.eps_norm);
+#pragma unroll 8   // every load of the pass in flight together (one round trip to L2)
+        for (int m = 0; m < h4n / 8; ++m) {
+            const int h4 = hb + 8 * m;
+            float4 zv = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (act) {
+                const float4 v = __ldcg(reinterpret_cast<const float4 *>(p.y + row + 4 * h4));
+                const float4 w = __ldg(reinterpret_cast<const float4 *>(p.norm_w + col0 + 4 * h4));
+                zv = make_float4(v.x * r * w.x, v.y * r * w.y, v.z * r * w.z, v.w * r * w.w);
+                *reinterpret_cast<float4 *>(p.z + row + 4 * h4) = zv;
+            }
+            if (p.q) {
+                float amax = fmaxf(fmaxf(fabsf(zv.x), fabsf(zv.y)), fmaxf(fabsf(zv.z), fabsf(zv.w)));
+                amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 1));
+                amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 2));
+                amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 4));
+                if (act) {
+                    const float sc = __fdiv_rn(amax, 127.0f);
+                    const float inv = sc != 0.0f ? __frcp_rn(sc) : 0.0f;
+                    auto code = [&](float a) {
+                        return (signed char)fminf(fmaxf(roundf(__fmul_rn(a, inv)), -127.0f), 127.0f);
+                    };
+                    *reinterpret_cast<char4 *>(p.q + row + 4 * h4) =
+                        make_char4(code(zv.x), code(zv.y), code(zv.z), code(zv.w));
+                    if (hb == 0)
+                        p.q_scale[(row + 32 * m) / 32] = sc;
+                }
+            }
+        }
+        return true;
+    };
+    // The decode variant's whole norm of its one tile (y written by all compute warps
+    // and made visible by a barrier before this call).
+    auto norm_tile = [&](int it, int ct, uint32_t nb) -> bool {
+        int t0, tm;
+        tile_tokens(it, t0, tm);
+        const int t = ct >> 3, hb = ct & 7;
+        float ss = 0.f;
+        if (t < tm) {
+            const float *yrow = p.y + (size_t)(t0 + t) * p.d + (size_t)rank * p.hs;
+            for (int h4 = hb; h4 < p.hs / 4; h4 += 8) {
+                const float4 v = __ldcg(reinterpret_cast<const float4 *>(yrow + 4 * h4));
+                ss = fmaf(v.x, v.x, ss);
+                ss = fmaf(v.y, v.y, ss);
+                ss = fmaf(v.z, v.z, ss);
+                ss = fmaf(v.w, v.w, ss);
+            }
+        }
+        norm_send(it, ct, ss);
+        return norm_finish(it, ct, nb);
+    };
 
     // ------------------------------------------------------------------ set-up
     if (threadIdx.x == 0)
@@ -483,6 +597,8 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const __gri
         ptx::mbar_init(BAR(kBarFFull), 1);
         for (int s = 0; s < kNstPersist; ++s)
             ptx::mbar_init(BAR(kBarXReady + s), 1);   // fused persistent: the stage holds x'
+        for (int q = 0; q < kNY; ++q)
+            ptx::mbar_init(BAR(kBarYss + q), 1);      // armed by this CTA; sums by remote stores
         // A non-zero status word (an earlier launch on this workspace timed out) makes
         // this launch skip its work: 2 marks the skip.  The word only changes 2 s into a
         // launch, so every CTA of the grid reads the same.
@@ -820,6 +936,11 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const __gri
                     ptx::mbar_arrive_expect_tx(BAR(kBarPre + qb), (uint32_t)(tm * 16));
                 if (!(ok = collapse(it)))
                     break;
+                if (p.z) {   // the branch-input norm, by warps 0-3 once every y column is written
+                    ptx::named_bar_sync(kNbCompute, kComputeThreads);
+                    if (warp < 4 && !(ok = norm_tile(it, threadIdx.x, kNbGroup0)))
+                        break;
+                }
             }
         }
         if (!arrived)
@@ -1034,6 +1155,7 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const __gri
                 for (; tok && nt < 2 && tile_exists(nt); ++nt)
                     tok = transform(nt);
             }
+            int ndone = 0;   // tiles collapsed
             for (int it = 0; tok && tile_exists(it); ++it) {
                 if (fused && tile_exists(nt)) {   // nt = it + 2
                     if (!(tok = transform(nt)))
@@ -1052,6 +1174,7 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const __gri
                     break;
                 if (ct == 0)
                     HC_STAMP(it, kEvPreArrived);
+                float ssy = 0.f;   // the norm's sum of y^2 over this thread's columns, in column order
                 if (t < tm) {
                     const float4 pv = ptx::lds128(ptx::smem_u32(preb + (q * kTMT + t) * 4));
                     const float pr[4] = {pv.x, pv.y, pv.z, pv.w};
@@ -1081,6 +1204,12 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const __gri
                                 a.w = fmaf(pr[k], xv[u][k].w, a.w);
                             }
                             *reinterpret_cast<float4 *>(yrow + 4 * h4) = a;
+                            if (p.z) {
+                                ssy = fmaf(a.x, a.x, ssy);
+                                ssy = fmaf(a.y, a.y, ssy);
+                                ssy = fmaf(a.z, a.z, ssy);
+                                ssy = fmaf(a.w, a.w, ssy);
+                            }
                         }
                     }
                 }
@@ -1095,7 +1224,15 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const __gri
                     load_tile(it + L.nst);
                     HC_STAMP(it, kEvRefilled);
                 }
+                if (p.z) {   // send this tile's sums, finish the previous tile's norm
+                    norm_send(it, ct, ssy);
+                    if (it > 0 && !(tok = norm_finish(it - 1, ct, kNbCollapse)))
+                        break;
+                }
+                ++ndone;
             }
+            if (p.z && tok && ndone > 0)
+                tok = norm_finish(ndone - 1, ct, kNbCollapse);
             if (fused && ct == 0)
                 ptx::bulk_wait_all();   // every x' store complete before the CTA can exit
         }
@@ -1209,6 +1346,15 @@ struct FusedPost {
     float *x_new;
 };
 
+// The branch-input norm's inputs and outputs (pre-chain mode).
+struct NormOut {
+    const float *norm_w;
+    float eps_norm;
+    float *z;
+    signed char *q;
+    float *q_scale;
+};
+
 // Chunks per slice row: the fewest hsc with hs/hsc <= 256 floats, a multiple of 4.
 int slice_chunks(int hs)
 {
@@ -1234,9 +1380,18 @@ bool encode_slab_map(CUtensorMap *m, const float *base, int rows, int s, int d, 
 template <int S, bool HEAD>
 cudaError_t run_s(const float *x, const float *fn_w, const float *scale, const float *base, int T,
                   int d, int iters, float eps, float *pre, float *post, float *comb, float *y,
-                  void *workspace, cudaStream_t st, int device, const FusedPost *fp = nullptr)
+                  void *workspace, cudaStream_t st, int device, const FusedPost *fp = nullptr,
+                  const NormOut *no = nullptr)
 {
     Params p = {};
+    if (no) {
+        p.norm_w = no->norm_w;
+        p.eps_norm = no->eps_norm;
+        p.z = no->z;
+        p.q = no->q;
+        p.q_scale = no->q_scale;
+        p.inv_d = 1.0f / (float)d;
+    }
     if (fp) {
         p.f = fp->f;
         p.post_prev = fp->post_prev;
@@ -1336,6 +1491,45 @@ cudaError_t launch_pre_cluster(const float *x, const float *fn_w, const float *s
     case S:                                                                                         \
         return run_s<S, false>(x, fn_w, scale, base, T, d, iters, eps, pre, post, comb, y, workspace, st, \
                                di.device);
+        HC_CASE(1) HC_CASE(2) HC_CASE(3) HC_CASE(4)
+#undef HC_CASE
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+bool cluster_norm_supported(int s, int d) { return (d / kCS) % 32 == 0 && cluster_supported(s, d, false); }
+
+int cluster_decode_tokens(int s, int d)
+{
+    DeviceInfo di;
+    if (!cluster_norm_supported(s, d) || !device_info(di))
+        return 0;
+    int nc = 0;
+    switch (s) {
+    case 1: nc = max_clusters_for<1, false, 8, false>(di.device); break;
+    case 2: nc = max_clusters_for<2, false, 8, false>(di.device); break;
+    case 3: nc = max_clusters_for<3, false, 8, false>(di.device); break;
+    case 4: nc = max_clusters_for<4, false, 8, false>(di.device); break;
+    default: return 0;
+    }
+    return nc * kTMT;
+}
+
+cudaError_t launch_pre_norm_cluster(const float *x, const float *fn_w, const float *scale,
+                                    const float *base, int T, int s, int d, int iters, float eps,
+                                    const float *norm_w, float eps_norm, float *pre, float *post, float *comb,
+                                    float *y, float *z, signed char *q, float *q_scale, void *workspace,
+                                    cudaStream_t st)
+{
+    DeviceInfo di;
+    if (!device_info(di))
+        return cudaErrorNoDevice;
+    const NormOut no{norm_w, eps_norm, z, q, q_scale};
+    switch (s) {
+#define HC_CASE(S)                                                                                  \
+    case S:                                                                                         \
+        return run_s<S, false>(x, fn_w, scale, base, T, d, iters, eps, pre, post, comb, y, workspace, st, \
+                               di.device, nullptr, &no);
         HC_CASE(1) HC_CASE(2) HC_CASE(3) HC_CASE(4)
 #undef HC_CASE
     default: return cudaErrorInvalidValue;

@@ -28,7 +28,8 @@ HC_PATH_AUTO, HC_PATH_GENERIC, HC_PATH_CLUSTER, HC_PATH_WIDE = 0, 1, 2, 3
 EXPORTED = ("hc_status_string", "hc_expand", "hc_pre_workspace_bytes", "hc_workspace_init",
             "hc_workspace_status", "hc_pre_fused", "hc_pre_fused_path", "hc_pre_auto_path",
             "hc_post", "hc_mean", "hc_pre_fused_noalloc", "hc_head", "hc_head_path",
-            "hc_post_pre_fused", "hc_post_pre_fused_path", "hc_rms_norm_q8", "hc_pre_fused_norm")
+            "hc_post_pre_fused", "hc_post_pre_fused_path", "hc_rms_norm_q8", "hc_pre_fused_norm",
+            "hc_pre_fused_norm_path")
 
 
 class HcError(RuntimeError):
@@ -69,6 +70,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.hc_post_pre_fused_path.argtypes = fused_args + [i]
     lib.hc_rms_norm_q8.argtypes = [vp, vp, i, i, f, vp, vp, vp, vp]
     lib.hc_pre_fused_norm.argtypes = [vp, vp, vp, vp, i, i, i, i, f, vp, f, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    lib.hc_pre_fused_norm_path.argtypes = lib.hc_pre_fused_norm.argtypes + [i]
     for name in EXPORTED[1:]:
         if name != "hc_pre_workspace_bytes":
             getattr(lib, name).restype = i
@@ -212,14 +214,20 @@ def hc_rms_norm_q8(y, norm_w, eps_norm: float, z, q=None, q_scale=None, stream=N
 
 
 def hc_pre_fused_norm(x, fn_w, scale, base, iters: int, eps: float, norm_w, eps_norm: float, pre, post,
-                      comb, y, z, workspace, q=None, q_scale=None, stream=None) -> None:
-    """hc_pre_fused, then hc_rms_norm_q8 on its y."""
+                      comb, y, z, workspace, q=None, q_scale=None, stream=None, path: int | None = None,
+                      prepare: bool = False):
+    """The pre-chain and the branch-input norm of its y (z, and the Q8_0 pair q / q_scale
+    if given): one launch on the cluster path where the shape allows, else hc_pre_fused
+    then hc_rms_norm_q8.  With prepare=True, returns a Prepared call instead."""
     T, s, d = _shape(x)
-    _check("hc_pre_fused_norm", load().hc_pre_fused_norm(
-        _ptr(x, "x"), _ptr(fn_w, "fn_w"), _ptr(scale, "scale"), _ptr(base, "base"), T, s, d, int(iters),
-        float(eps), _ptr(norm_w, "norm_w"), float(eps_norm), _ptr(pre, "pre"), _ptr(post, "post"),
-        _ptr(comb, "comb"), _ptr(y, "y"), _ptr(z, "z"), _ptr(q, "q", torch.int8), _ptr(q_scale, "q_scale"),
-        _ptr(workspace, "workspace", torch.uint8), workspace.numel(), _stream(stream)))
+    args = (_ptr(x, "x"), _ptr(fn_w, "fn_w"), _ptr(scale, "scale"), _ptr(base, "base"), T, s, d, int(iters),
+            float(eps), _ptr(norm_w, "norm_w"), float(eps_norm), _ptr(pre, "pre"), _ptr(post, "post"),
+            _ptr(comb, "comb"), _ptr(y, "y"), _ptr(z, "z"), _ptr(q, "q", torch.int8), _ptr(q_scale, "q_scale"),
+            _ptr(workspace, "workspace", torch.uint8), workspace.numel(), _stream(stream))
+    keep = (x, fn_w, scale, base, norm_w, pre, post, comb, y, z, q, q_scale, workspace)
+    if path is None:
+        return _run("hc_pre_fused_norm", args, prepare, keep)
+    return _run("hc_pre_fused_norm_path", args + (int(path),), prepare, keep)
 
 
 def hc_post_pre_fused(x_prev, f, post_prev, comb_prev, fn_w, scale, base, iters: int, eps: float,

@@ -309,3 +309,14 @@ def test_wide_stream_batch_tokens_equal_single_token_calls():
                     f"{k} of tokens {t}..{t + n} differs between T={n} and T={T}"
         assert small.status() == 0
     assert big.status() == 0
+
+
+def test_benchmark_shapes_run_their_fused_paths():
+    """The workloads' shapes must run the fused kernels on a GB300, not fall back silently:
+    the cluster path for s = 4, d = 4096 at T = 1, 8 and 4096, the wide path for the
+    wide-stream workload (a layout that outgrew shared memory would otherwise only show
+    up as skipped tests and a slower bench)."""
+    from mhc_hyper_connection_hc_gb300 import hc
+    for T in (1, 8, 512, 4096):
+        assert hc.hc_pre_auto_path(T, 4, 4096) == hc.HC_PATH_CLUSTER, T
+    assert hc.hc_pre_auto_path(2048, 8, 7168) == hc.HC_PATH_WIDE
