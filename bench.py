@@ -298,12 +298,18 @@ def run_reference(args):
 
 
 def selected_workload(args) -> synth.Workload:
-    """The workload named on the command line, with --iters overriding its Sinkhorn iterations."""
+    """The workload named on the command line, with --iters overriding its Sinkhorn
+    iterations and --tokens its token count (a smaller case of the same shape, for
+    profiler captures; the line then names the workload with that T)."""
     w = synth.WORKLOADS[WORKLOAD_IDS[args.workload]]
     if args.iters is not None:
         if args.iters < 1:
             raise SystemExit("--iters must be >= 1")
         w = dataclasses.replace(w, iters=args.iters)
+    if getattr(args, "tokens", None) is not None:
+        if args.tokens < 1:
+            raise SystemExit("--tokens must be >= 1")
+        w = dataclasses.replace(w, T=args.tokens)
     return w
 
 
@@ -960,6 +966,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=("gb300", "reference"), default="gb300")
     ap.add_argument("--workload", choices=tuple(WORKLOAD_IDS), default="prefill")
     ap.add_argument("--iters", type=int, default=None, help="override the workload's Sinkhorn iterations")
+    ap.add_argument("--tokens", type=int, default=None,
+                    help="override the workload's token count (smaller cases for profiler captures)")
     ap.add_argument("--pipeline", choices=("fused", "separate"), default="fused",
                     help="a step is one site boundary: hc_post_pre_fused (fused) or hc_pre_fused + hc_post")
     ap.add_argument("--cpu-tokens", type=int, default=4096, help="tokens of the CPU-oracle sample")

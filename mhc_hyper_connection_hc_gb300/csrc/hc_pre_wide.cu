@@ -73,7 +73,7 @@ constexpr int kWCollapseWarp = 11;        // collapse, with its own ring
 constexpr int kWM = 4;                    // tokens per tile
 constexpr int kWNstMax = 16;              // dot-ring stages (the launcher fits as many as it can)
 constexpr int kWNcsMax = 8;               // collapse-ring stages
-constexpr int kWNp = 128;                 // partial and tile-sum slots in the workspace
+constexpr int kWNp = 64;                  // partial and tile-sum slots in the workspace (bounds how far a CTA runs ahead)
 constexpr int kWNb = 4;                   // buffers of the compute warps' values
 constexpr int kWMaxCtas = 160;            // workspace sizing bound on the grid
 constexpr uint32_t kWTmemCols = 256;
@@ -347,16 +347,21 @@ __global__ void __launch_bounds__(kWThreads, 1) hc_pre_wide_kernel(const __grid_
     auto LEFT = [&](int b) { return bar0 + 8u * (uint32_t)(kWNstMax + kWNcsMax + 1 + b); };
     auto FREED = [&](int b) { return bar0 + 8u * (uint32_t)(kWNstMax + kWNcsMax + 1 + kWNb + b); };
     const uint32_t tile_bytes = (uint32_t)(kWM * LK * 4);
+    // The dot ring's loads keep the tile's lines in L2 (evict_last) for the collapse ring,
+    // which reads the same slice again a few tens of microseconds later, for the last time
+    // (evict_first): x then comes from HBM once.
     auto load_tile = [&](int it) {   // one thread; the dot stage must be free
         const int s = it % nst;
         ptx::mbar_arrive_expect_tx(FULL(s), tile_bytes);
-        ptx::tma_load_3d(ptx::smem_u32(stages + s * stage_floats), tmx, h0, 0, it * kWM, FULL(s));
+        ptx::tma_load_3d_hint(ptx::smem_u32(stages + s * stage_floats), tmx, h0, 0, it * kWM, FULL(s),
+                              ptx::l2_evict_last());
         issued[s] = issued[s] + 1;
     };
     auto load_ctile = [&](int it) {   // one thread; the collapse stage must be free
         const int s = it % ncs;
         ptx::mbar_arrive_expect_tx(CFULL(s), tile_bytes);
-        ptx::tma_load_3d(ptx::smem_u32(cstages + s * stage_floats), tmx, h0, 0, it * kWM, CFULL(s));
+        ptx::tma_load_3d_hint(ptx::smem_u32(cstages + s * stage_floats), tmx, h0, 0, it * kWM, CFULL(s),
+                              ptx::l2_evict_first());
         cissued[s] = cissued[s] + 1;
     };
 

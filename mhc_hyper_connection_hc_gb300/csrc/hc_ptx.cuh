@@ -173,6 +173,31 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *tmap, int 
                  "l"(tmap), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
                  : "memory");
 }
+// The same with an L2 cache-eviction policy for the loaded lines (from l2_evict_last /
+// l2_evict_first below).
+__device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const void *tmap, int c0, int c1, int c2, uint32_t bar,
+                                                 uint64_t policy)
+{
+    asm volatile("cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+                 " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+                 "l"(tmap), "r"(c0), "r"(c1), "r"(c2), "r"(bar), "l"(policy)
+                 : "memory");
+}
+// L2 eviction policies for cache-hinted accesses: lines loaded under evict_last are kept
+// in preference to others (data that will be read again soon), evict_first ones are the
+// first to go (data read for the last time).
+__device__ __forceinline__ uint64_t l2_evict_last()
+{
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+__device__ __forceinline__ uint64_t l2_evict_first()
+{
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
 __device__ __forceinline__ void prefetch_tmap(const void *tmap)
 {
     asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");

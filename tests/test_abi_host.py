@@ -145,12 +145,12 @@ def test_workspace_sizes(lib):
             n = hc.hc_pre_workspace_bytes(T, s, d)
             assert n >= 256 and n % 4 == 0
             generic = 256 + 4 * ((2 + s) * s + 1) * T * 304 + 4 * ((2 + s) * s + 1) * 304
-            # the wide-stream path (s >= 5): per-tile counters and flags, and 128 slots of
+            # the wide-stream path (s >= 5): per-tile counters and flags, and 64 slots of
             # per-CTA partials and of tile sums (R dots + squares for 4 tokens, at most 160
             # CTAs)
             ntiles = (T + 3) // 4
             rv = (2 + s) * s + 1
-            wide = 256 + 12 * ntiles + 128 * (160 + 1) * 4 * rv * 4 + 3 * 256 if s >= 5 else 0
+            wide = 256 + 12 * ntiles + 64 * (160 + 1) * 4 * rv * 4 + 3 * 256 if s >= 5 else 0
             assert n <= max(generic, wide)
 
 
