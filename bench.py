@@ -350,7 +350,8 @@ def run_gpu(args):
         x_out = torch.empty(T, s, d, dtype=torch.float32, device=dev)
     stream.synchronize()
     path = hc.hc_pre_auto_path(T, s, d)
-    pre_launches = 1 if path == hc.HC_PATH_CLUSTER else 2
+    pre_launches = 1 if path in (hc.HC_PATH_CLUSTER, hc.HC_PATH_WIDE) else 2
+    path_name = {hc.HC_PATH_CLUSTER: "cluster", hc.HC_PATH_WIDE: "wide"}.get(path, "generic")
     fused = args.pipeline == "fused"
     fused_cluster = path == hc.HC_PATH_CLUSTER and d // 16 <= 256   # else hc_post + generic pre
     if fused:
@@ -449,7 +450,7 @@ def run_gpu(args):
                          "TFLOP/s": pre_flops / pre_avg / 1e12,
                          "frac_fp32": pre_flops / pre_avg / 1e12 / fp32_peak,
                          "launches_per_step": pre_launches,
-                         "path": "cluster" if path == hc.HC_PATH_CLUSTER else "generic"},
+                         "path": path_name},
         "hc_post": {"us": post_avg * 1e6, "algorithmic_bytes": post_bytes,
                     "GB/s": post_bytes / post_avg / 1e9, "frac_hbm": post_bytes / post_avg / 1e9 / peak,
                     "launches_per_step": 1},
@@ -463,7 +464,7 @@ def run_gpu(args):
             "TFLOP/s": (pre_flops + 2 * (s + 1) * s * d * T) / fz_avg / 1e12,
             "frac_fp32": (pre_flops + 2 * (s + 1) * s * d * T) / fz_avg / 1e12 / fp32_peak,
             "launches_per_step": 1 if fused_cluster else 1 + pre_launches,
-            "path": "cluster" if fused_cluster else "generic (hc_post, then the generic pre-chain)"}
+            "path": "cluster" if fused_cluster else f"{path_name} (hc_post, then the {path_name} pre-chain)"}
         kernels["hc_pre_fused"]["launches_per_step"] = 0
         kernels["hc_post"]["launches_per_step"] = 0
         dom = "hc_post_pre_fused"
@@ -483,6 +484,17 @@ def run_gpu(args):
                 "frac_nominal_8tbs": kd["GB/s"] / NOMINAL_HBM_GBS,
                 "traffic": profiled_traffic(dom, wl_tag),
                 "algorithmic_bytes_per_launch": kd["algorithmic_bytes"]}
+    if path == hc.HC_PATH_WIDE:
+        # At s > 4 the pre-chain is float32-FMA bound (~36 FLOP per byte at s = 8) and it is
+        # the step's dominant kernel: report it against the FP32 peak of the sampled clock.
+        kp = kernels["hc_pre_fused"]
+        roofline = {"bound": "alu", "kernel": "hc_pre_fused", "achieved": kp["TFLOP/s"], "peak": fp32_peak,
+                    "unit": "TFLOP/s", "frac": kp["TFLOP/s"] / fp32_peak,
+                    "peak_note": (f"FP32 FMA peak: {GB300_SMS} SMs x {FP32_LANES} lanes x 2 FLOP x "
+                                  f"{clocks.get('sm_mhz') or GB300_MAX_MHZ:.0f} MHz (the sampled median clock)"),
+                    "traffic": profiled_traffic("hc_pre_fused", wl_tag),
+                    "algorithmic_flop_per_launch": pre_flops,
+                    "step_hbm": {"kernel": dom, "GB/s": kd["GB/s"], "frac": kd["GB/s"] / peak}}
 
     line = {"metric": METRIC, "value": all_tokens / max_s, "unit": "tokens/s", "n_gpus": world,
             "steps": K, "warmup": args.warmup, "ms_per_step": 1e3 * max_s / K,
@@ -710,6 +722,7 @@ def measure_head(w, dv, ws, stream, peak, reps: int = 20):
     us = statistics.mean(e0.elapsed_time(e1) for e0, e1 in ev) * 1e3
     nbytes = T * s * d * 4 + T * d * 4   # x read once, y written
     gbs = nbytes / us / 1e3
+    # the head has no wide kernel: HC_PATH_AUTO runs the generic one for s > 4
     path = hc.HC_PATH_CLUSTER if hc.hc_pre_auto_path(T, s, d) == hc.HC_PATH_CLUSTER else hc.HC_PATH_GENERIC
     return {"us": us, "algorithmic_bytes": nbytes, "GB/s": gbs, "frac_hbm": gbs / peak,
             "path": "cluster" if path == hc.HC_PATH_CLUSTER else "generic",
