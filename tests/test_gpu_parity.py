@@ -320,3 +320,32 @@ def test_benchmark_shapes_run_their_fused_paths():
     for T in (1, 8, 512, 4096):
         assert hc.hc_pre_auto_path(T, 4, 4096) == hc.HC_PATH_CLUSTER, T
     assert hc.hc_pre_auto_path(2048, 8, 7168) == hc.HC_PATH_WIDE
+
+
+@pytest.mark.parametrize("s,d", [(5, 4096), (6, 4096), (7, 7168)])
+def test_wide_kernel_other_streams_invariant_and_against_oracle(s, d):
+    """The wide kernel at s = 5, 6 and 7 (other row counts R, lane-pair row groups RB and
+    split units): a T = 300 batch against the oracle on every token, and tokens of it the
+    same bits as the same tokens run alone or in fives."""
+    from mhc_hyper_connection_hc_gb300 import hc
+    T = 300
+    if hc.hc_pre_auto_path(T, s, d) != hc.HC_PATH_WIDE:
+        pytest.skip("the wide kernel does not run this shape here")
+    inp = synth.site_inputs(940 + s, T, s, d, "normal")
+    want = oracle.pre(inp["x"], inp["fn_w"], inp["scale"], inp["base"], 20, eps32(1e-6))
+    big = GpuSite(T, s, d)
+    dev = {k: big.upload(v) for k, v in inp.items()}
+    g = big.pre(dev["x"], dev["fn_w"], dev["scale"], dev["base"], 20, 1e-6, path=hc.HC_PATH_WIDE)
+    ref = {k: g[k].clone() for k in ("pre", "post", "comb", "y")}
+    for k in ref:
+        assert rel_err(to_np(ref[k]), want[k]) <= TOL, k
+    for n in (1, 5):
+        small = GpuSite(n, s, d)
+        for t in sample_tokens(T - n + 1, n=6):
+            gg = small.pre(dev["x"][t:t + n].contiguous(), dev["fn_w"], dev["scale"], dev["base"], 20, 1e-6,
+                           path=hc.HC_PATH_WIDE)
+            for k in ref:
+                assert torch.equal(gg[k].view(torch.int32), ref[k][t:t + n].contiguous().view(torch.int32)), \
+                    f"{k} of tokens {t}..{t + n} differs between T={n} and T={T}"
+        assert small.status() == 0
+    assert big.status() == 0
