@@ -118,10 +118,10 @@ def test_norm_rejects_pair_with_ragged_blocks():
                           torch.empty(2, 1, device="cuda"))
 
 
-@pytest.mark.parametrize("T,s,d", [(1, 4, 4096), (37, 4, 4096), (4096, 4, 4096), (130, 2, 1024), (5, 4, 576)])
+@pytest.mark.parametrize("T,s,d", [(1, 4, 4096), (37, 4, 4096), (4096, 4, 4096), (130, 2, 1024), (5, 4, 768)])
 def test_pre_fused_norm_one_launch(T, s, d):
     """The cluster path's one-launch pre-chain + norm (where d / 16 is a multiple of 32;
-    (5, 4, 576) is a cluster shape whose slices do not hold whole blocks, so it runs the
+    (5, 4, 768) is a cluster shape whose slices do not hold whole blocks, so it runs the
     cluster pre-chain then the norm kernel): every token against the oracle (T = 4096
     reaches the exchange-slot and stage-ring reuse), pre/post/comb/y the same bits as
     hc_pre_fused on the cluster path, the Q8_0 pair first-hand and bit for bit against the
