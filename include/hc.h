@@ -69,10 +69,16 @@ enum hc_pre_path {
     HC_PATH_CLUSTER = 2,  /* one fused launch, x read once: thread-block clusters split
                              the hidden dimension; needs s <= 4 and s*d <= 16384 with
                              d % 64 == 0                                               */
-    HC_PATH_WIDE = 3      /* one fused launch over every SM, x read once, for 5 <= s <= 8:
-                             each CTA keeps a fixed hidden range of fn_w resident; needs a
-                             balanced split of d (e.g. s = 8 with d % 8 == 0 and d >= 256,
-                             s = 5 or 7 with d % 64 == 0 and d >= 2048)                */
+    HC_PATH_WIDE = 3      /* one fused launch over every SM, x read once from HBM, for
+                             5 <= s <= 8: each CTA keeps a fixed hidden range of fn_w
+                             resident.  Needs d split over at least 32 CTAs (at most one
+                             per SM) into widths that are multiples of the unit u (the
+                             smallest multiple of 8 with s*u % 64 == 0: 64, 32, 64, 8 for
+                             s = 5..8), at most one unit apart and balanced to 3/4, with
+                             the slice fitting TMEM and shared memory (e.g. s = 8 with
+                             d = 7168 or 4096, s = 5..7 with d = 4096, s = 5 or 7 with
+                             d = 7168; not s = 6 with d = 7168);
+                             hc_pre_auto_path says whether it runs a shape             */
 };
 
 /* Human-readable name of a status code (static string, never NULL). */

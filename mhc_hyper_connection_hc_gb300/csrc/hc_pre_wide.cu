@@ -23,8 +23,8 @@
 //    of a tile.  Packed float32 FMAs (x from shared memory, four columns a step;
 //    fn_w from TMEM, the next step's load in flight); the pair's halves are added by
 //    one shuffle level and each warp leaves its values in one of kWNb shared-memory
-//    buffers, then goes on with the next tile: the compute warps never wait for one
-//    another.
+//    buffers, then goes on with the next tile: a compute warp waits for the others
+//    only when it is kWNb tiles ahead of the slowest.
 //  * A publisher warp, once the eight warps have left a tile's values, refills the
 //    stage the tile used, sums the eight warps' values in warp order into the tile's
 //    partial dots and sums of squares (a slot of the workspace), frees the buffer and
@@ -37,22 +37,24 @@
 //    out), sets the tile's flag and then runs the tile's Sinkhorn.  Each CTA has one
 //    warp for each step; each takes its duties in tile order and waits (bounded) for
 //    the counters they need.
-//  * A collapse warp in every CTA waits (bounded) for each tile's flag and writes y
-//    for the CTA's hidden columns from its own ring (the collapse ring), which loads
-//    the tile's slice a second time, some tens of microseconds after the dot ring did
-//    (from L2 as a rule).  So the dot ring never waits for a tile's cross-CTA chain;
-//    it waits only for the partial slot it writes to, kWNp tiles on.  No wait depends
-//    on a later tile, so the grid cannot deadlock.
+//  * A collapse warp in every CTA takes the runs of tiles whose flags are set (a
+//    bounded wait for the first), loads their gates in one round trip and writes y for
+//    the CTA's hidden columns from its own ring (the collapse ring), which loads the
+//    tile's slice a second time, some tens of microseconds after the dot ring did: the
+//    dot ring's loads keep the lines in L2 (evict_last) and no CTA runs more than kWNp
+//    tiles ahead, so x comes from HBM about once.  The dot ring never waits for a
+//    tile's cross-CTA chain; it waits only for the partial slot it writes to, kWNp
+//    tiles on.  No wait depends on a later tile, so the grid cannot deadlock.
 //  * Every wait is bounded (2 s); on timeout the kernel records the site in the
 //    workspace status word and winds down.  The host zeroes the tiles' counters and
 //    flags (a memset on the stream) before each launch, so what other paths or
 //    earlier calls left in the workspace does not matter.
 //
-// Determinism: every partial has a fixed summation order (per lane, then the
-// transpose's fixed order), the partials of a token are summed over CTAs in a fixed
-// order (per lane over CTAs l, l+32, ..., then an xor tree), and no float atomics are
-// used: repeated calls give the same bits, and a token's results do not depend on the
-// other tokens of the batch.
+// Determinism: every partial has a fixed summation order (per lane in column order,
+// the lane pair's halves, the eight warps in warp order), the partials of a token are
+// summed over CTAs in a fixed order (per lane over CTAs l, l+32, ..., then an xor
+// tree), and no float atomics are used: repeated calls give the same bits, and a
+// token's results do not depend on the other tokens of the batch.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -65,7 +67,7 @@ namespace hc {
 namespace {
 
 constexpr int kWThreads = 384;            // 12 warps
-constexpr int kWNCW = 8;                  // compute warps 0-7, one row group each
+constexpr int kWNCW = 8;                  // compute warps 0-7, one eighth of the slice each
 constexpr int kWPublishWarp = 8;          // publishes this CTA's partials, refills the dot ring
 constexpr int kWReduceWarp = 9;           // column sums of the (tile, column) pairs this CTA reduces
 constexpr int kWTileWarp = 10;            // tile finishes (gates, flag, Sinkhorn) of this CTA's tiles
@@ -82,7 +84,7 @@ constexpr unsigned long long kWWaitNs = 2000000000ull;
 constexpr unsigned kFullMask = 0xffffffffu;
 
 enum WSite : unsigned {
-    kWSiteW = 32, kWSiteFull, kWSiteShipped, kWSiteFlag, kWSiteReduce, kWSiteTile, kWSiteDrain, kWSiteSlot, kWSiteCFull,
+    kWSiteW = 32, kWSiteFull, kWSiteLeft, kWSiteFlag, kWSiteReduce, kWSiteTile, kWSiteDrain, kWSiteSlot, kWSiteCFull,
     kWSiteFreed
 };
 
@@ -258,8 +260,10 @@ __device__ __forceinline__ bool w_warp_wait_count(int lane, const unsigned *ctr,
     return ok;
 }
 
-// One level of the xor reduce-scatter over the 32 lanes of a warp (lanes whose M bit
-// is clear keep the lower half of the list and add their partner's copy of it).
+// One level of an xor reduce-scatter over the lanes of a warp: lanes whose M bit is clear
+// keep the lower half of the list and add their partner's copy of it, the others the
+// upper half (used with M = 1 for a lane pair's halves and M = 4, 2, 1 for the
+// Sinkhorn's column sums over a token's eight lanes).
 template <int N, int M>
 __device__ __forceinline__ void w_rs_level(float *v, int lane)
 {
@@ -536,7 +540,7 @@ __global__ void __launch_bounds__(kWThreads, 1) hc_pre_wide_kernel(const __grid_
         int pend = 0;       // tiles [pend, it] are stored but their counters not raised
         for (int it = 0; it < p.ntiles; ++it) {
             const int b = it % kWNb;
-            if (!w_warp_wait(lane, LEFT(b), (it / kWNb) & 1, abort_flag, sb, kWSiteShipped))
+            if (!w_warp_wait(lane, LEFT(b), (it / kWNb) & 1, abort_flag, sb, kWSiteLeft))
                 break;
             bool good = true;
             if (it + nst < p.ntiles) {
@@ -848,7 +852,7 @@ bool wide_split_for(int d, int nsm, int max_smem, WideSplit &w)
     const WLay L = make_wlay<S>(lk_max, nst, ncs);
     if (L.total > max_smem)
         return false;
-    if (G::R * lk_max * 4 > L.off_red)   // the fn_w slice is staged through the rings and transpose rows
+    if (G::R * lk_max * 4 > L.off_red)   // the fn_w slice is staged through the rings and value buffers
         return false;
     w.nst = nst;
     w.ncs = ncs;

@@ -349,3 +349,18 @@ def test_wide_kernel_other_streams_invariant_and_against_oracle(s, d):
                     f"{k} of tokens {t}..{t + n} differs between T={n} and T={T}"
         assert small.status() == 0
     assert big.status() == 0
+
+
+def test_wide_path_shape_rule():
+    """HC_PATH_AUTO takes the wide kernel exactly where include/hc.h says it runs: the
+    balanced splits of d into widths of the stream count's unit, over at least 32 CTAs."""
+    from mhc_hyper_connection_hc_gb300 import hc
+    for s, d in ((8, 7168), (8, 4096), (5, 4096), (6, 4096), (7, 4096), (5, 7168), (7, 7168)):
+        assert hc.hc_pre_auto_path(64, s, d) == hc.HC_PATH_WIDE, (s, d)
+    # 224 units of 32 over 152 CTAs: widths of 64 and 32 columns, balanced to 0.74
+    assert hc.hc_pre_auto_path(64, 6, 7168) == hc.HC_PATH_GENERIC
+    # 153 units of 8: widths of 16 and 8 columns, balanced to 0.50
+    assert hc.hc_pre_auto_path(64, 8, 1224) == hc.HC_PATH_GENERIC
+    # fewer than 32 CTAs' worth of units
+    assert hc.hc_pre_auto_path(64, 8, 248) == hc.HC_PATH_GENERIC
+    assert hc.hc_pre_auto_path(64, 5, 1984) == hc.HC_PATH_GENERIC
