@@ -364,3 +364,34 @@ def test_wide_path_shape_rule():
     # fewer than 32 CTAs' worth of units
     assert hc.hc_pre_auto_path(64, 8, 248) == hc.HC_PATH_GENERIC
     assert hc.hc_pre_auto_path(64, 5, 1984) == hc.HC_PATH_GENERIC
+
+
+def test_wide_kernel_largest_state():
+    """The wide kernel at T*s*d just under 2^31 elements (s = 8, d = 7168: T = 37,448, an
+    8.6 GB state): tiles, flags and partial slots far past 2^16, 64-bit row offsets.
+    Sampled tokens against the oracle, and the same bits as those tokens run alone."""
+    from mhc_hyper_connection_hc_gb300 import hc
+    s, d = 8, 7168
+    T = (2 ** 31 - 1) // (s * d)
+    if hc.hc_pre_auto_path(T, s, d) != hc.HC_PATH_WIDE:
+        pytest.skip("the wide kernel does not run this shape here")
+    base_T = 64
+    inp = synth.site_inputs(42, base_T, s, d, "normal")
+    gs = GpuSite(T, s, d)
+    x_small = gs.upload(inp["x"])
+    x = x_small.repeat((T + base_T - 1) // base_T, 1, 1)[:T].contiguous()
+    fw, sc, bs = gs.upload(inp["fn_w"]), gs.upload(inp["scale"]), gs.upload(inp["base"])
+    g = gs.pre(x, fw, sc, bs, 20, 1e-6, path=hc.HC_PATH_WIDE)
+    assert gs.status() == 0
+    idx = np.array([0, 1, 3, 4, T // 2, T - 5, T - 2, T - 1])
+    src = idx % base_T
+    want = oracle.pre(inp["x"][src], inp["fn_w"], inp["scale"], inp["base"], 20, eps32(1e-6))
+    sel = torch.from_numpy(idx).cuda()
+    _check_pre({k: g[k].index_select(0, sel) for k in ("pre", "post", "comb", "y")}, want)
+    one = GpuSite(1, s, d)
+    for t in idx:
+        gg = one.pre(x[t:t + 1].contiguous(), fw, sc, bs, 20, 1e-6, path=hc.HC_PATH_WIDE)
+        for k in ("pre", "post", "comb", "y"):
+            assert torch.equal(gg[k].view(torch.int32), g[k][t:t + 1].contiguous().view(torch.int32)), (k, int(t))
+    assert one.status() == 0
+    del x
