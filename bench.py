@@ -6,8 +6,9 @@ mixes contraction, gates, Sinkhorn, collapse) then hc_post -- over one batch of
 synthetic tokens already resident in HBM.  The default workload is the prefill
 chunk (T = 4096 tokens, s = 4 streams, hidden 4096, 20 Sinkhorn iterations,
 eps 1e-6): its 256 MiB stream state is larger than L2, so every step streams
-from HBM without a flush.  The JSON line also carries the T = 1 decode latency
-per site (CUDA-graph replay of back-to-back sites).
+from HBM without a flush.  The JSON line also carries the T = 1 and T = 8 per-site
+latencies (CUDA-graph replay, eager and Prepared calls).  At s > 4 (the wide-stream
+workload) the roofline is the pre-chain's against the FP32 peak.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
 
@@ -848,10 +849,11 @@ STAMP_TILES, STAMP_EV, STAMP_CTAS = 512, 16, 2
 
 
 def run_stamps(args):
-    """Per-phase timing of the fused pre kernel from its phase-stamp build (HC_STAMPS):
-    %globaltimer stamps of CTAs 0 and 8 of cluster 0 at every tile's phase boundaries,
-    for the pre-chain and the fused site boundary of the selected workload; medians
-    over the tiles (the first two skipped) of each phase, in microseconds."""
+    """Per-phase timing of the pre kernel from its phase-stamp build (HC_STAMPS):
+    %globaltimer stamps at every tile's phase boundaries (cluster kernel: CTAs 0 and 8 of
+    cluster 0; wide kernel: CTA 0, and the reductions and finishes wherever they ran),
+    for the pre-chain and the fused site boundary of the selected workload; medians over
+    the tiles (the first two skipped) of each phase, in microseconds."""
     import torch
     from mhc_hyper_connection_hc_gb300 import build as lib_build, hc
     hc.load(lib_build.build(stamps=True))

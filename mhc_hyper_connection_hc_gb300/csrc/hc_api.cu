@@ -415,10 +415,16 @@ int hc_pre_fused_norm_path(const float *x, const float *fn_w, const float *scale
                            float *post, float *comb, float *y, float *z, signed char *q, float *q_scale,
                            void *workspace, size_t ws_bytes, void *stream, int path)
 {
-    // Every argument is checked before anything is launched.
+    // Every argument is checked before anything is launched: the pre-chain's (which also
+    // bound T, s and d), then the norm's.
     if (!(eps_norm >= 0.f) || !std::isfinite(eps_norm))
         return HC_ERR_DIM;
-    if (T > 0) {
+    const int asked = path;
+    const int rc = pre_checks(x, fn_w, scale, base, T, s, d, iters, eps, pre, post, comb, y, workspace, ws_bytes,
+                              path);
+    if (rc != HC_OK || T == 0)
+        return rc;
+    {
         if (!norm_w || !z || (!q) != (!q_scale))
             return HC_ERR_NULL;
         if ((q && d % 32) || !aligned(norm_w, 16) || !aligned(z, 16) ||
@@ -443,11 +449,6 @@ int hc_pre_fused_norm_path(const float *x, const float *fn_w, const float *scale
                     return HC_ERR_ALIAS;
         }
     }
-    const int asked = path;
-    const int rc = pre_checks(x, fn_w, scale, base, T, s, d, iters, eps, pre, post, comb, y, workspace, ws_bytes,
-                              path);
-    if (rc != HC_OK || T == 0)
-        return rc;
     cudaStream_t st = as_stream(stream);
     // One launch when the cluster path runs the shape and its slices hold whole Q8_0 blocks:
     // always when that path was asked for, and under HC_PATH_AUTO while the decode variant

@@ -28,10 +28,12 @@ static_assert(sizeof(StatusBlock) == kStatusBytes, "status block is 256 bytes");
 
 // ---------------------------------------------------------------- phase stamps
 // A build with -DHC_STAMPS (build.build(stamps=True), a separate library) makes the
-// cluster pre kernel write %globaltimer at phase boundaries of every tile into the
-// workspace, right after the status block: [kStampCtas][kStampTiles][kStampEvents]
-// 64-bit nanosecond stamps, for CTAs 0 and 8 of cluster 0 (the owners of tokens 0 and 8
-// of every tile).  Stamps of tiles beyond kStampTiles are dropped.
+// cluster and wide pre kernels write %globaltimer at phase boundaries of every tile into
+// the workspace, right after the status block: [kStampCtas][kStampTiles][kStampEvents]
+// 64-bit nanosecond stamps.  Cluster kernel: CTAs 0 and 8 of cluster 0 (the owners of
+// tokens 0 and 8 of every tile).  Wide kernel: slot 0 CTA 0's own phases, slot 1 the
+// reduction of column 0 and the finish of every tile, by whichever CTA did them.  Stamps
+// of tiles beyond kStampTiles are dropped.
 constexpr int kStampCtas = 2, kStampTiles = 512, kStampEvents = 16;
 constexpr size_t kStampBytes = (size_t)kStampCtas * kStampTiles * kStampEvents * 8;
 enum StampEvent : int {
