@@ -52,10 +52,17 @@
 //    the tile's Sinkhorn CTA (tile index mod 16), whose Sinkhorn warp
 //    normalises all the tile's comb blocks at once, one token per lane, in
 //    registers, off the path that the next tiles' gates take.
+//  * Branch-input norm mode (hc_pre_fused_norm): after a tile's collapse each CTA
+//    sends its share of every token's sum of y^2 to the other fifteen (st.async,
+//    an 8-slot exchange over the f buffer, which this mode does not use) and then
+//    writes z = y * rsqrt(mean(y^2) + eps_norm) * norm_w and its Q8_0 pair for its
+//    own columns (the persistent variant one tile later, from the sum it took
+//    while writing y; the decode variant reads its tile back).
 //  * Every wait on an mbarrier is bounded (2 s of %globaltimer); on timeout the
 //    kernel records the site in the workspace status word, stops issuing work,
 //    lets its TMA loads land, meets the other CTAs at the final cluster
-//    barrier, frees TMEM and returns.
+//    barrier, frees TMEM and returns.  A launch that finds the status word
+//    already set does nothing at all.
 //
 // Determinism: every sum has a fixed order independent of T, of the tile a
 // token lands in and of the variant, so a token's outputs are the same bits
