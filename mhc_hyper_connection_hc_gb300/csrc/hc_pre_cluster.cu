@@ -175,8 +175,8 @@ __host__ __device__ inline Lay make_lay(int LK)
     o += kNQ * kTMT * 4 * 4;
     L.off_sink = o;                  // [16 tokens][16]: the comb blocks this CTA scales
     o += kTMT * 16 * 4;
-    L.off_coef = o;                  // [16 tokens][s + s*s]: fused post -> pre, the tile's post/comb
-    o += (kTMT * (S + S * S) * 4 + 127) / 128 * 128;
+    L.off_coef = o;                  // [2][16 tokens][s + s*s]: fused post -> pre, two tiles' post/comb
+    o += (2 * kTMT * (S + S * S) * 4 + 127) / 128 * 128;
     L.off_f = o;                     // [16 tokens][hs <= 256]: fused post -> pre, the tile's slice of f
     o += kTMT * kMaxFusedHs * 4;
     // [kNY slots][16 source CTAs][16 tokens]: the norm's sums of y^2, over the f buffer
@@ -1092,6 +1092,19 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const __gri
             const int t = ct >> 3, hb = ct & 7;
             const bool fused = p.x_new != nullptr;
             constexpr int NC = S + S * S;
+            // Fused: tile k's post / comb values (at most 16 tokens x (s + s*s)) into coef
+            // buffer k % 2 by asynchronous copies, issued one transform ahead.
+            auto load_coefs_c = [&](int k) {
+                int t0n, tmn;
+                tile_tokens(k, t0n, tmn);
+                float *cb = coefs + (k & 1) * (kTMT * NC);
+                for (int e = ct; e < tmn * NC; e += kCollapseThreads) {
+                    const int tt = e / NC, cc = e - tt * NC;
+                    ptx::cp_async4(ptx::smem_u32(cb + e), cc < S ? p.post_prev + (size_t)(t0n + tt) * S + cc
+                                                                 : p.comb_prev + (size_t)(t0n + tt) * S * S + (cc - S));
+                }
+                ptx::cp_async_commit();
+            };
             // x -> x' for tile k (the same operations, in the same order, as hc_post_kernel).
             auto transform = [&](int k) -> bool {
                 const int s = k % L.nst;
@@ -1099,11 +1112,7 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const __gri
                 tile_tokens(k, t0, tm);
                 if (ct == 0)
                     HC_STAMP(k, kEvXfStart);
-                for (int e = ct; e < tm * NC; e += kCollapseThreads) {   // the tile's post / comb
-                    const int tt = e / NC, cc = e - tt * NC;
-                    coefs[e] = cc < S ? __ldg(p.post_prev + (size_t)(t0 + tt) * S + cc)
-                                      : __ldg(p.comb_prev + (size_t)(t0 + tt) * S * S + (cc - S));
-                }
+                ptx::cp_async_wait_all();   // this thread's copies of the tile's post / comb
                 bool got = true;
                 if (ct == 0)
                     got = wait_bar<false>(BAR(kBarXFull + s), (k / L.nst) & 1, abort_flag, sb, kSiteXFull) &&
@@ -1112,11 +1121,12 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const __gri
                     return false;
                 if (ct == 0)
                     HC_STAMP(k, kEvXfLanded);
-                if (t < tm) {
+                if (t < tm) {   // (the barrier above made every thread's coef copies visible)
+                    const float *cb = coefs + (k & 1) * (kTMT * NC);
                     float cf[NC];
     #pragma unroll
                     for (int c = 0; c < NC; ++c)
-                        cf[c] = coefs[t * NC + c];
+                        cf[c] = cb[t * NC + c];
                     float *xr = stages + s * stage_floats + t * p.LK;
                     const float *fr = fbuf + t * p.hs;
                     for (int h4 = hb; h4 < h4n; h4 += 8) {
@@ -1152,6 +1162,8 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const __gri
                     if (tile_exists(k + 1))
                         load_f(k + 1);
                 }
+                if (tile_exists(k + 1))
+                    load_coefs_c(k + 1);
                 return true;
             };
             int nt = 0;   // the next tile to transform
@@ -1159,11 +1171,19 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const __gri
             if (fused) {
                 if (ct == 0)
                     load_f(0);
+                load_coefs_c(0);
                 for (; tok && nt < 2 && tile_exists(nt); ++nt)
                     tok = transform(nt);
             }
             int ndone = 0;   // tiles collapsed
             for (int it = 0; tok && tile_exists(it); ++it) {
+                if (ct == 0 && tile_exists(it + L.nst + 1)) {
+                    // The box of the tile whose stage load the next iteration issues, into L2
+                    // now, so that load reads L2 (fused: the transform after it waits for it).
+                    int t0n, tmn;
+                    tile_tokens(it + L.nst + 1, t0n, tmn);
+                    ptx::tma_prefetch_l2_4d(&p.tmap_x, 0, (int)rank * p.hsc, 0, t0n);
+                }
                 if (fused && tile_exists(nt)) {   // nt = it + 2
                     if (!(tok = transform(nt)))
                         break;
