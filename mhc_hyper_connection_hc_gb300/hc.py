@@ -88,24 +88,34 @@ def _check(fn: str, rc: int) -> None:
 
 
 def _ptr(t: torch.Tensor | None, name: str, dtype=torch.float32):
+    """The tensor's device address as an int (None for no tensor or an empty one), after
+    checking device, dtype and contiguity; the common case costs four attribute reads."""
     if t is None:
         return None
+    if isinstance(t, torch.Tensor) and t.is_cuda and t.dtype is dtype and t.is_contiguous():
+        return t.data_ptr() if t.numel() else None
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
-    if t.device.type != "cuda":
+    if not t.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor (got {t.device})")
     if t.dtype != dtype:
         raise TypeError(f"{name} must be {dtype} (got {t.dtype})")
-    if not t.is_contiguous():
-        raise ValueError(f"{name} must be contiguous")
-    return ctypes.c_void_p(t.data_ptr()) if t.numel() else None
+    raise ValueError(f"{name} must be contiguous")
 
 
-def _stream(stream) -> ctypes.c_void_p:
+# The current stream's raw handle without building a torch.cuda.Stream object (about 3 us
+# per call through torch.cuda.current_stream()); the public call where it is missing.
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
+def _stream(stream) -> int:
+    """The CUDA stream handle to pass: `stream` (a torch.cuda.Stream or a raw handle), or
+    the current device's current stream when it is None."""
     if stream is None:
+        if _raw_stream is not None:
+            return int(_raw_stream(torch.cuda.current_device()))
         stream = torch.cuda.current_stream()
-    handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
-    return ctypes.c_void_p(handle)
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
 
 
 class Prepared:
@@ -137,9 +147,10 @@ def _run(name: str, args: tuple, prepare: bool, keep: tuple):
 
 
 def _shape(x: torch.Tensor):
-    if x.dim() != 3:
+    shape = x.shape
+    if len(shape) != 3:
         raise ValueError("stream state must be [T, s, d]")
-    return int(x.shape[0]), int(x.shape[1]), int(x.shape[2])
+    return shape[0], shape[1], shape[2]
 
 
 def hc_expand(emb: torch.Tensor, x: torch.Tensor, stream=None) -> None:

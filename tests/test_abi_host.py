@@ -239,3 +239,18 @@ def test_host_checks_in_a_process_without_devices():
                        capture_output=True, text=True, timeout=600, cwd=root, env=env)
     assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-2000:]
     assert " passed" in r.stdout and " skipped" not in r.stdout.splitlines()[-1], r.stdout[-2000:]
+
+
+def test_binding_refuses_bad_tensors_before_any_call():
+    """The binding's argument check (hc._ptr): None and empty tensors pass no pointer; a
+    non-tensor, a host tensor and (through the slow path's messages) the wrong kind of
+    tensor are refused with TypeError / ValueError before the library is called."""
+    import torch
+    assert hc._ptr(None, "x") is None
+    with pytest.raises(TypeError):
+        hc._ptr([1.0, 2.0], "x")
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        hc._ptr(torch.zeros(4), "x")
+    with pytest.raises(ValueError, match=r"\[T, s, d\]"):
+        hc._shape(torch.zeros(4, 4))
+    assert hc._shape(torch.zeros(2, 3, 8)) == (2, 3, 8)

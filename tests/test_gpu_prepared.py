@@ -68,3 +68,25 @@ def test_prepared_calls_match_checked_calls(T, s, d):
     torch.cuda.synchronize()
     for k in ref:
         assert _bits_equal(got[k], ref[k]), "after new x: " + k
+
+
+def test_binding_checks_and_stream_handle():
+    """The checked binding refuses a float64, a non-contiguous and an int8-for-float tensor;
+    an empty tensor passes no pointer; and the stream it passes by default is the current
+    stream of the current device, inside a torch.cuda.stream context as well."""
+    from mhc_hyper_connection_hc_gb300 import hc
+    x = torch.zeros(2, 4, 64, device="cuda")
+    assert hc._ptr(x, "x") == x.data_ptr()
+    assert hc._ptr(torch.empty(0, device="cuda"), "x") is None
+    with pytest.raises(TypeError, match="float32"):
+        hc._ptr(x.double(), "x")
+    with pytest.raises(TypeError):
+        hc._ptr(torch.zeros(8, dtype=torch.int8, device="cuda"), "x")
+    with pytest.raises(ValueError, match="contiguous"):
+        hc._ptr(x.transpose(1, 2), "x")
+    assert hc._ptr(torch.zeros(8, dtype=torch.int8, device="cuda"), "q", torch.int8) is not None
+    assert hc._stream(None) == torch.cuda.current_stream().cuda_stream
+    side = torch.cuda.Stream()
+    with torch.cuda.stream(side):
+        assert hc._stream(None) == side.cuda_stream
+    assert hc._stream(side) == side.cuda_stream
