@@ -98,7 +98,10 @@ int hc_expand(const float *emb, float *x, int T, int s, int d, void *stream);
  * workspace holds a status word (first 256 bytes) and, by path: on the generic
  * path split-K partial sums; on the wide path the tiles' counters and flags
  * (zeroed by the call itself, on its stream, before its launch) and per-CTA
- * partial slots.  It must be zeroed once before first use (hc_workspace_init);
+ * partial slots; on the cluster path at prefill sizes the helper kernel's
+ * partial sums (a smaller workspace, down to the 256-byte status word, only
+ * keeps the helper from running: see hc_pre_helper_tokens).  It must be zeroed
+ * once before first use (hc_workspace_init);
  * every call leaves it valid for the next.  Calls that share a workspace must
  * not run concurrently.
  */
@@ -161,6 +164,21 @@ int hc_pre_fused_path(const float *x, const float *fn_w, const float *scale, con
 
 /* The path HC_PATH_AUTO picks for this shape on the current device. */
 int hc_pre_auto_path(int T, int s, int d);
+
+/*
+ * hc_pre_helper_tokens -- on the cluster path at prefill sizes the cluster kernel,
+ * whose 16-CTA clusters cannot be placed on every SM, is followed on the stream by a
+ * helper kernel on the SMs it leaves free (programmatic dependent launch: both run
+ * at once).  The helper takes the batch's last tokens and plays each cluster's 16
+ * CTAs in turn with the same arithmetic in the same order, so every token's outputs
+ * are the same bits whichever kernel computed them.  This returns how many tokens
+ * it takes for a call of this shape on the current device with a workspace of
+ * ws_bytes: fused != 0 for hc_post_pre_fused, 0 for hc_pre_fused (the gated head and
+ * hc_pre_fused_norm's one-launch mode never use it).  0 means the cluster kernel
+ * alone (small T, another path, or a workspace without room for the helper's
+ * partials); -1 for dimensions out of range.
+ */
+int hc_pre_helper_tokens(int T, int s, int d, int fused, size_t ws_bytes);
 
 /*
  * hc_pre_fused_noalloc -- hc_pre_fused for callers that cannot allocate device

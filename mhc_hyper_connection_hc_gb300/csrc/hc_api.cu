@@ -267,7 +267,8 @@ size_t hc_pre_workspace_bytes(int T, int s, int d)
     // Any path may be asked for, so size for the larger of the two (a phase-stamp build
     // keeps its stamps after the status block).
     const size_t g = hc::generic_workspace_bytes(T, s, d);
-    const size_t c = kStatusBytes + hc::kWorkspaceExtra;
+    const size_t c0 = kStatusBytes + hc::kWorkspaceExtra, ch = hc::cluster_helper_workspace_bytes(T, s, d);
+    const size_t c = c0 > ch ? c0 : ch;
     const size_t w = hc::wide_workspace_bytes(T, s, d);
     const size_t m = g > c ? g : c;
     return m > w ? m : w;
@@ -302,6 +303,15 @@ int hc_pre_auto_path(int T, int s, int d)
     if (hc::cluster_supported(s, d))
         return HC_PATH_CLUSTER;
     return hc::wide_supported(s, d) ? HC_PATH_WIDE : HC_PATH_GENERIC;
+}
+
+int hc_pre_helper_tokens(int T, int s, int d, int fused, size_t ws_bytes)
+{
+    if (!dims_ok(T, s, d))
+        return -1;
+    if (d % 4 || T == 0 || !hc::cluster_supported(s, d))
+        return 0;
+    return hc::cluster_helper_tokens(T, s, d, fused != 0, ws_bytes);
 }
 
 }  // extern "C"
@@ -370,7 +380,7 @@ int hc_pre_fused_path(const float *x, const float *fn_w, const float *scale, con
         if (!hc::cluster_supported(s, d))
             return HC_ERR_UNSUPPORTED;
         return cuda_rc(hc::launch_pre_cluster(x, fn_w, scale, base, T, s, d, iters, eps, pre, post,
-                                              comb, y, workspace, st));
+                                              comb, y, workspace, ws_bytes, st));
     }
     if (path == HC_PATH_WIDE) {
         if (!hc::wide_supported(s, d))
@@ -528,7 +538,7 @@ int hc_post_pre_fused_path(const float *x_prev, const float *f, const float *pos
         if (!hc::cluster_fused_supported(s, d))
             return HC_ERR_UNSUPPORTED;
         return cuda_rc(hc::launch_post_pre_cluster(x_prev, f, post_prev, comb_prev, fn_w, scale, base, T, s, d,
-                                                   iters, eps, x_new, pre, post, comb, y, workspace, st));
+                                                   iters, eps, x_new, pre, post, comb, y, workspace, ws_bytes, st));
     }
     if (path == HC_PATH_WIDE && !hc::wide_supported(s, d))
         return HC_ERR_UNSUPPORTED;

@@ -138,10 +138,16 @@ cudaError_t launch_pre_norm_cluster(const float *x, const float *fn_w, const flo
                                     const float *norm_w, float eps_norm, float *pre, float *post, float *comb,
                                     float *y, float *z, signed char *q, float *q_scale, void *workspace,
                                     cudaStream_t st);
+// At prefill sizes the cluster kernel's launch is followed by the helper kernel, on the SMs
+// the clusters leave free, for the batch's last tokens, when ws_bytes holds its partials
+// (cluster_helper_workspace_bytes; the same bits either way).
+size_t cluster_helper_workspace_bytes(int T, int s, int d);
+// Tokens the helper kernel takes from the end of a batch (0: the cluster kernel alone).
+int cluster_helper_tokens(int T, int s, int d, bool fused, size_t ws_bytes);
 cudaError_t launch_pre_cluster(const float *x, const float *fn_w, const float *scale,
                                const float *base, int T, int s, int d, int iters, float eps,
                                float *pre, float *post, float *comb, float *y,
-                               void *workspace, cudaStream_t st);
+                               void *workspace, size_t ws_bytes, cudaStream_t st);
 
 // Fused post -> pre: x_new = post_prev . f + comb_prev^T x_prev, then the pre-chain of
 // the next site on x_new, in one launch of the cluster kernel.
@@ -149,7 +155,7 @@ cudaError_t launch_post_pre_cluster(const float *x_prev, const float *f, const f
                                     const float *comb_prev, const float *fn_w, const float *scale,
                                     const float *base, int T, int s, int d, int iters, float eps,
                                     float *x_new, float *pre, float *post, float *comb, float *y,
-                                    void *workspace, cudaStream_t st);
+                                    void *workspace, size_t ws_bytes, cudaStream_t st);
 
 // Gated-head trunk exit: rows = streams, one scale, gates (optional output) + collapse.
 cudaError_t launch_head_cluster(const float *x, const float *fn_w, const float *scale,

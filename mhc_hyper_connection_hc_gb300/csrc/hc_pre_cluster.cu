@@ -73,6 +73,8 @@
 #include "hc_internal.cuh"
 #include "hc_ptx.cuh"
 
+#include <algorithm>
+#include <cmath>
 #include <mutex>
 
 namespace hc {
@@ -588,6 +590,8 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const __gri
     // ------------------------------------------------------------------ set-up
     if (threadIdx.x == 0)
         HC_STAMP(0, kEvKernelStart);
+    if (PERSIST && threadIdx.x == 0)   // the helper kernel queued behind this one may start now
+        ptx::griddep_launch_dependents();
     if (threadIdx.x == 0) {
         for (int s = 0; s < L.nst; ++s) {
             ptx::mbar_init(BAR(kBarXFull + s), 1);
@@ -1287,6 +1291,445 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const __gri
     }
 }
 
+// ---------------------------------------------------------------------- helper kernel
+// The persistent cluster kernel fills only the SMs that 16-CTA clusters can be placed on
+// (112 of 152 on a GB300); the others would idle.  The helper kernel runs on them, launched
+// right behind the cluster kernel on the same stream with programmatic dependent launch (the
+// cluster kernel lets it start at once).  It takes whole 8-token tiles from the end of the
+// batch, never the cluster kernel's tokens, and each of its CTAs plays the 16 CTAs of a
+// cluster in turn, with the decode variant's arithmetic in the decode variant's order, so
+// every token's outputs are the same bits whichever kernel computed them:
+//  * phase 1, slice c = 0..15 (hidden columns [c*hs, (c+1)*hs) of every stream): the fn_w
+//    slice into TMEM (staged through shared memory while the previous slice is in use, then
+//    copied in one pass); then for each of the CTA's tiles the tile's slice by TMA (two
+//    buffers, one tile ahead; fused mode: with the f slice, then the previous site's hc_post
+//    in place and the x' slice stored by TMA), the eight warps' dots, the 16-lane
+//    reduce-scatter, and the two column halves' partials of every token into the workspace;
+//  * phase 2: per token, the 2 x 16 partials in the finisher's order, the gates, pre/post;
+//    the Sinkhorn, one token per thread; then y over all d columns from x (fused: x') read
+//    back from memory.
+// Waits are bounded as in the cluster kernel.  Before it exits the helper waits for the
+// cluster kernel to complete (griddepcontrol.wait), so whatever the stream runs next sees
+// the outputs of both.
+constexpr int kHT = 8;                         // tokens per helper tile
+constexpr int kHNT = 4;                        // token slots per half-warp: two half-warps, 8 tokens
+constexpr int kHThreads = kComputeThreads;     // the eight compute warps of the decode variant
+constexpr int kHMaxTok = 64;                   // tokens per chunk of a helper CTA (eight tiles)
+constexpr int kHB = 3;                         // tile-slice buffers (steps in flight); token buffers
+
+struct HParams {
+    CUtensorMap tmap_x;      // x (fused: x_prev) as (hc, d/hc, s, T), box (hc, hsc, s, kHT)
+    CUtensorMap tmap_w;      // fn_w, box (hc, hsc, s, R)
+    CUtensorMap tmap_f;      // fused: f as [T][1][d], box (hc, hsc, 1, kHT)
+    CUtensorMap tmap_xnew;   // fused: x_new, boxes as for x
+    const float *x, *scale, *base, *post_prev, *comb_prev;
+    float *pre, *post, *comb, *y, *x_new;
+    float *part;             // [tokens from t0][2 * kCS][RV]: the helper tokens' partials
+    StatusBlock *status;
+    int T, d, hs, hsc, LK, NJ, iters;
+    int t0;                  // first helper token
+    int ntiles;              // helper tiles: tile i holds tokens [t0 + kHT*i, t0 + kHT*i + kHT) below T
+    float eps, invK;
+};
+
+struct HLay {
+    int off_w, off_x, off_f, off_coef, off_sink, off_pre, off_bar, off_misc, total;
+};
+
+template <int S>
+__host__ __device__ inline HLay make_hlay()
+{
+    using G = CG<S, false, 4>;
+    HLay L;
+    int o = 0;
+    L.off_w = o;      // [RP][LK]: the fn_w slice (rows past R zero)
+    o += G::RP * kMaxLK * 4;
+    L.off_x = o;      // [kHB][kHT][LK]: tile slices in flight
+    o += kHB * kHT * kMaxLK * 4;
+    L.off_f = o;      // [kHB][kHT][hs]: fused, their f slices
+    o += kHB * kHT * kMaxFusedHs * 4;
+    // Phase 2 lays kHB token slabs (s*d <= 16 * kMaxLK floats each) over all of the above.
+    o = o > kHB * 16 * kMaxLK * 4 ? o : kHB * 16 * kMaxLK * 4;
+    L.off_coef = o;   // [kHMaxTok][s + s*s]: fused, post/comb of the CTA's tokens
+    o += kHMaxTok * (S + S * S) * 4;
+    L.off_sink = o;   // [kHMaxTok][16]: exp(comb logits)
+    o += kHMaxTok * 16 * 4;
+    L.off_pre = o;    // [kHMaxTok][4]: pre gates
+    o += kHMaxTok * 4 * 4;
+    L.off_bar = o;    // xfull[kHB], wfull, tfull[kHB]
+    o += (2 * kHB + 1) * 8;
+    L.off_misc = o;   // abort flag; loads issued into each x buffer, fn_w, each token buffer; TMEM address
+    o += 48;
+    L.total = o;
+    return L;
+}
+
+template <int S>
+__global__ void __launch_bounds__(kHThreads, 1) hc_pre_helper_kernel(const __grid_constant__ HParams p)
+{
+    constexpr int RG = 4, NT = kHNT;
+    using G = CG<S, false, RG>;
+    using C = CT<S, NT, false, RG>;
+    constexpr int NC = S + S * S;
+    constexpr int kHCT = kHMaxTok / kHT;   // tiles per chunk
+    extern __shared__ __align__(128) unsigned char smem[];
+    const HLay L = make_hlay<S>();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    float *wsm = reinterpret_cast<float *>(smem + L.off_w);
+    float *xb = reinterpret_cast<float *>(smem + L.off_x);
+    float *fb = reinterpret_cast<float *>(smem + L.off_f);
+    float *coef_s = reinterpret_cast<float *>(smem + L.off_coef);
+    float *sink_s = reinterpret_cast<float *>(smem + L.off_sink);
+    float *pre_s = reinterpret_cast<float *>(smem + L.off_pre);
+    const uint32_t bar0 = ptx::smem_u32(smem + L.off_bar);
+    auto XFULL = [&](int b) { return bar0 + 8u * (uint32_t)b; };
+    const uint32_t WFULL = bar0 + 8u * kHB;
+    auto TFULL = [&](int b) { return bar0 + 8u * (uint32_t)(kHB + 1 + b); };   // phase 2: token buffers
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L.off_misc);
+    volatile int *issued = reinterpret_cast<volatile int *>(smem + L.off_misc + 4);   // x [kHB], fn_w, tokens [kHB]
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L.off_misc + 40);
+    StatusBlock *sb = p.status;
+    const bool fused = p.x_new != nullptr;
+    // This CTA's tiles [k0, k1), taken in chunks of at most kHCT tiles (kHMaxTok tokens):
+    // chunk q, slice c, tile j of the chunk is step g = 16 kHCT q + c nq + j.
+    const int k0 = (int)((long long)blockIdx.x * p.ntiles / gridDim.x);
+    const int k1 = (int)((long long)(blockIdx.x + 1) * p.ntiles / gridDim.x);
+    const int nmy = k1 - k0;
+    const int nchunk = (nmy + kHCT - 1) / kHCT;
+    auto chunk_tiles = [&](int q) { return min(kHCT, nmy - q * kHCT); };
+    const int stage_floats = kHT * p.LK;
+    const uint32_t xbytes = (uint32_t)(stage_floats * 4), fbytes = (uint32_t)(kHT * p.hs * 4);
+
+    if (threadIdx.x == 0) {
+        for (int b = 0; b < kHB; ++b) {
+            ptx::mbar_init(XFULL(b), 1);
+            ptx::mbar_init(TFULL(b), 1);
+        }
+        ptx::mbar_init(WFULL, 1);
+        for (int i = 0; i < 2 * kHB + 1; ++i)
+            issued[i] = 0;
+        *abort_flag = *reinterpret_cast<volatile unsigned *>(&sb->code) != 0u ? 2 : 0;
+        ptx::fence_mbar_init_cluster();
+    }
+    if (warp == 0) {   // the fn_w slice in use lives in TMEM (the CTA is alone on its SM)
+        ptx::tmem_alloc(ptx::smem_u32(tmem_slot), kTmemCols);
+        ptx::tmem_relinquish();
+    }
+    ptx::tmem_fence_before_sync();
+    __syncthreads();
+    ptx::tmem_fence_after_sync();
+    const uint32_t tmem_base = *tmem_slot;
+    const bool skip = *abort_flag == 2 || nmy <= 0;
+
+    auto issue = [&](int g) {   // one thread: step g's tile slice (and f slice) into buffer g % kHB
+        const int q = g / (kCS * kHCT), r = g - q * kCS * kHCT, nq = chunk_tiles(q);
+        const int c = r / nq, j = r - c * nq, b = g % kHB;
+        const int t0 = p.t0 + (k0 + q * kHCT + j) * kHT;
+        ptx::mbar_arrive_expect_tx(XFULL(b), xbytes + (fused ? fbytes : 0u));
+        ptx::tma_load_4d(ptx::smem_u32(xb + b * stage_floats), &p.tmap_x, 0, c * p.hsc, 0, t0, XFULL(b));
+        if (fused)
+            ptx::tma_load_4d(ptx::smem_u32(fb + b * kHT * kMaxFusedHs), &p.tmap_f, 0, c * p.hsc, 0, t0, XFULL(b));
+        issued[b] = issued[b] + 1;
+    };
+    auto load_w = [&](int c) {   // one thread: fn_w slice c
+        ptx::mbar_arrive_expect_tx(WFULL, (uint32_t)(G::R * p.LK * 4));
+        ptx::tma_load_4d(ptx::smem_u32(wsm), &p.tmap_w, 0, c * p.hsc, 0, 0, WFULL);
+        issued[kHB] = issued[kHB] + 1;
+        ptx::tma_prefetch_l2_4d(&p.tmap_w, 0, ((c + 1) % kCS) * p.hsc, 0, 0);   // the next slice into L2
+    };
+
+    bool ok = !skip;
+    if (ok && threadIdx.x == 0) {
+        ptx::prefetch_tmap(&p.tmap_x);
+        ptx::prefetch_tmap(&p.tmap_w);
+    }
+    const int tg = lane >> 4, kg = lane & 15;
+    const int rg = warp & 3, half = warp >> 2;
+    const int njh = (p.NJ + 1) / 2;
+    const int j0 = half * njh, nj = half ? p.NJ - njh : njh;
+    const int lk4 = p.LK * 4;
+    const int slot0 = tg * NT;
+    const uint32_t trow = tmem_base + ((uint32_t)(32 * rg) << 16);   // this sub-partition's lanes
+    const int tcol0 = half * (kMaxLK / 128) * G::WQ;                    // this column half's columns
+    const int h4n = p.hs / 4;
+    const int grp = lane < S ? 0 : (lane < 2 * S ? 1 : 2);
+    const float my_scale = lane < G::R ? p.scale[grp] : 0.f;
+    const float my_base = lane < G::R ? p.base[lane] : 0.f;
+    int tl = 0;   // phase 2's token loads so far (token buffer tl % 2, phase tl / 2)
+    for (int q = 0; ok && q < nchunk; ++q) {
+        const int nq = chunk_tiles(q);
+        const int tok0 = p.t0 + (k0 + q * kHCT) * kHT;   // the chunk's first token
+        const int ntok = min(p.T, tok0 + nq * kHT) - tok0;
+        const int g0 = kCS * kHCT * q, g1 = g0 + kCS * nq;   // the chunk's steps
+        if (threadIdx.x == 0) {   // fn_w slice 0 and the first two steps (phase 2 of the last chunk
+            load_w(0);            // is done with the buffers)
+            for (int g = g0; g < g0 + kHB && g < g1; ++g)
+                issue(g);
+        }
+        if (fused) {   // the chunk's post/comb (the previous chunk is done with the buffer)
+            for (int e = threadIdx.x; e < ntok * NC; e += kHThreads) {
+                const int tt = e / NC, cc = e - tt * NC;
+                coef_s[e] = cc < S ? __ldg(p.post_prev + (size_t)(tok0 + tt) * S + cc)
+                                   : __ldg(p.comb_prev + (size_t)(tok0 + tt) * S * S + (cc - S));
+            }
+        }
+        // ------------------------------------------------------------ phase 1: slices
+        for (int c = 0; ok && c < kCS; ++c) {
+            // fn_w slice c: staged in shared memory (loaded during slice c - 1), then copied into
+            // this thread's TMEM lane, which every warp is done reading for slice c - 1: warp
+            // (rg, half) lane kg's values of column group jj at columns half*8*WQ + jj*WQ, row r's
+            // pairs (2kg, 2kg+1) and (32+2kg, 33+2kg) at 4r .. 4r+3 (rows past R zero).
+            ok = __syncthreads_and(threadIdx.x != 0 || wait_bar<false>(WFULL, c & 1, abort_flag, sb, kSiteWFull)) != 0;
+            if (!ok)
+                break;
+            for (int jj = 0; jj < nj; ++jj) {
+                const int col = 64 * (j0 + jj) + 2 * kg;
+#pragma unroll
+                for (int r = 0; r < G::B; ++r) {
+                    const int row = rg * G::B + r;
+                    float2 v0 = make_float2(0.f, 0.f), v1 = make_float2(0.f, 0.f);
+                    if (row < G::R) {
+                        v0 = *reinterpret_cast<const float2 *>(wsm + row * p.LK + col);
+                        v1 = *reinterpret_cast<const float2 *>(wsm + row * p.LK + col + 32);
+                    }
+                    const float a[4] = {v0.x, v0.y, v1.x, v1.y};
+                    ptx::tmem_st4(trow + (uint32_t)(tcol0 + jj * G::WQ + 4 * r), a);
+                }
+            }
+            ptx::tmem_wait_st();
+            ptx::tmem_fence_before_sync();
+            __syncthreads();   // the staging buffer is free, the slice is in TMEM
+            ptx::tmem_fence_after_sync();
+            if (threadIdx.x == 0 && c + 1 < kCS)
+                load_w(c + 1);
+            for (int j = 0; ok && j < nq; ++j) {
+                const int g = kCS * kHCT * q + c * nq + j, b = g % kHB;
+                ok = __syncthreads_and(threadIdx.x != 0 ||
+                                       wait_bar<false>(XFULL(b), (g / kHB) & 1, abort_flag, sb, kSiteXFull)) != 0;
+                if (!ok)
+                    break;
+                const int t0 = tok0 + j * kHT;
+                const int tm = min(kHT, p.T - t0);
+                float *xs = xb + b * stage_floats;
+                if (fused) {
+                    // The previous site's hc_post on the slice, in place (hc_post's operations
+                    // in hc_post's order): warp t owns token t of the tile, lanes its float4s.
+                    const int t = warp;
+                    if (t < tm) {
+                        float cf[NC];
+#pragma unroll
+                        for (int m = 0; m < NC; ++m)
+                            cf[m] = coef_s[(j * kHT + t) * NC + m];
+                        const float *fr = fb + b * kHT * kMaxFusedHs + t * p.hs;
+                        for (int h4 = lane; h4 < h4n; h4 += 32) {
+                            float4 *xt = reinterpret_cast<float4 *>(xs + t * p.LK + 4 * h4);
+                            const float4 fv = *reinterpret_cast<const float4 *>(fr + 4 * h4);
+                            float4 xv[S];
+#pragma unroll
+                            for (int m = 0; m < S; ++m)
+                                xv[m] = xt[m * h4n];
+#pragma unroll
+                            for (int k = 0; k < S; ++k) {
+                                const float pk = cf[k];
+                                float4 o = make_float4(pk * fv.x, pk * fv.y, pk * fv.z, pk * fv.w);
+#pragma unroll
+                                for (int m = 0; m < S; ++m) {
+                                    const float cc = cf[S + m * S + k];
+                                    o.x = fmaf(cc, xv[m].x, o.x);
+                                    o.y = fmaf(cc, xv[m].y, o.y);
+                                    o.z = fmaf(cc, xv[m].z, o.z);
+                                    o.w = fmaf(cc, xv[m].w, o.w);
+                                }
+                                xt[k * h4n] = o;
+                            }
+                        }
+                    }
+                    ptx::fence_proxy_async_smem();   // the TMA store reads the slice
+                    __syncthreads();
+                    if (threadIdx.x == 0) {
+                        ptx::tma_store_4d(&p.tmap_xnew, 0, c * p.hsc, 0, t0, ptx::smem_u32(xs));
+                        ptx::bulk_commit();
+                    }
+                }
+                // The decode variant's dots of slice c: warp (row group rg, column half),
+                // half-warp tg on token slots [4 tg, 4 tg + 4), lane kg a K-group.
+                const int ntok_h = min(NT, max(0, tm - slot0));
+                const uint32_t xs_addr = ptx::smem_u32(xs + slot0 * p.LK) + 8u * kg;
+                float2 acc[NT][G::B];
+                float2 ssa[C::NSS];
+#pragma unroll
+                for (int i = 0; i < NT; ++i)
+#pragma unroll
+                    for (int r = 0; r < G::B; ++r)
+                        acc[i][r] = make_float2(0.f, 0.f);
+#pragma unroll
+                for (int m = 0; m < C::NSS; ++m)
+                    ssa[m] = make_float2(0.f, 0.f);
+                for (int jj = 0; jj < nj; ++jj) {
+                    const uint32_t cofs = 256u * (uint32_t)(j0 + jj);
+                    float w[G::WQ];   // the values the decode variant reads from its shared copy
+                    ptx::tmem_ld_issue<G::WQ>(trow + (uint32_t)(tcol0 + jj * G::WQ), w);
+                    ptx::tmem_ld_wait_regs<G::WQ>(w);
+                    dots_step_smem<G::B, NT, RG, C::NSS>(acc, ssa, w, xs_addr, cofs, lk4, rg);
+                }
+                float v[C::NVP];
+#pragma unroll
+                for (int i = 0; i < NT; ++i)
+#pragma unroll
+                    for (int r = 0; r < G::B; ++r)
+                        v[i * G::B + r] = acc[i][r].x + acc[i][r].y;
+#pragma unroll
+                for (int m = 0; m < C::NSS; ++m)
+                    v[NT * G::B + m] = ssa[m].x + ssa[m].y;
+#pragma unroll
+                for (int m = C::NV; m < C::NVP; ++m)
+                    v[m] = 0.f;
+                reduce_scatter16<C::NVP>(v, kg);
+                // Partials of (token, slice c, column half), in the cluster kernel's
+                // receive layout.
+#pragma unroll
+                for (int m = 0; m < C::VPL; ++m) {
+                    const int o = C::VPL * kg + m;
+                    int i = NT, vid = -1;
+                    if (o < NT * G::B) {
+                        i = o / G::B;
+                        const int row = rg * G::B + (o - i * G::B);
+                        vid = row < G::R ? row : -1;
+                    } else if (o < C::NV) {
+                        i = rg + RG * (o - NT * G::B);
+                        vid = G::R;
+                    }
+                    if (vid >= 0 && i < ntok_h) {
+                        const int tr = t0 + slot0 + i - p.t0;
+                        p.part[((size_t)tr * 2 * kCS + 2 * c + half) * G::RV + vid] = v[m];
+                    }
+                }
+                __syncthreads();   // buffer b is free (fused: once its x' store has read it)
+                if (threadIdx.x == 0 && g + kHB < g1) {
+                    if (fused)
+                        ptx::bulk_wait_read<0>();
+                    issue(g + kHB);
+                }
+            }
+        }
+        // ------------------------------------------------------------ phase 2: the chunk's tokens
+        ok = __syncthreads_and(ok ? 1 : 0) != 0;
+        if (!ok)
+            break;
+        // y comes from each token's whole slab of x (fused: x', as stored above; s*d floats,
+        // contiguous, at most 64 KiB), one bulk copy per token into kHB buffers laid over the
+        // fn_w staging buffer and the tile-slice buffers, which phase 1 no longer needs.  The
+        // first copies start now, under the gates and the Sinkhorn.
+        const float *xsrc = fused ? p.x_new : p.x;
+        const int d4 = p.d / 4;
+        const uint32_t slab_bytes = (uint32_t)(S * p.d * 4);
+        float *tbuf = wsm;
+        const int tlb = tl;   // token i of the chunk is the (tlb + i)-th token load
+        auto load_token = [&](int i) {   // one thread
+            const int b = (tlb + i) % kHB;
+            ptx::mbar_arrive_expect_tx(TFULL(b), slab_bytes);
+            ptx::bulk_g2s(ptx::smem_u32(tbuf + (size_t)b * (16 * kMaxLK)), xsrc + (size_t)(tok0 + i) * S * p.d,
+                          slab_bytes, TFULL(b));
+            issued[kHB + 1 + b] = issued[kHB + 1 + b] + 1;
+        };
+        if (threadIdx.x == 0) {
+            if (fused) {
+                ptx::bulk_wait_all();   // the chunk's x' slices are in memory before they are read back
+                ptx::fence_proxy_async_global();
+            }
+            for (int i = 0; i < kHB && i < ntok; ++i)
+                load_token(i);
+        }
+        for (int i = warp; i < ntok; i += kHThreads / 32) {   // gates: one warp per token
+            const int tr = tok0 + i - p.t0;
+            float val = 0.f;
+            if (lane <= G::R) {
+                float src[2 * kCS];
+#pragma unroll
+                for (int m = 0; m < 2 * kCS; ++m)
+                    src[m] = p.part[((size_t)tr * 2 * kCS + m) * G::RV + lane];
+                val = tree_sum<2 * kCS>(src);   // the finisher's fixed order
+            }
+            const float ss = __shfl_sync(kFull, val, G::R);
+            const float rinv = rsqrtf(ss * p.invK + p.eps);
+            const float logit = lane < G::R ? val * rinv * my_scale + my_base : 0.f;
+            const float sg = __fdividef(1.f, 1.f + __expf(-logit));
+            const size_t tok = (size_t)tok0 + i;
+            if (lane < S) {
+                const float pre_v = sg + p.eps;
+                p.pre[tok * S + lane] = pre_v;
+                pre_s[i * 4 + lane] = pre_v;
+            } else if (lane < 2 * S) {
+                p.post[tok * S + (lane - S)] = 2.f * sg;
+            } else if (lane < G::R) {
+                sink_s[i * 16 + (lane - 2 * S)] = __expf(logit);
+            }
+        }
+        __syncthreads();
+        for (int i = threadIdx.x; i < ntok; i += kHThreads) {   // Sinkhorn: one token per thread
+            float cm[S * S];
+#pragma unroll
+            for (int m = 0; m < S * S; ++m)
+                cm[m] = sink_s[i * 16 + m];
+            sinkhorn_regs<S>(cm, p.iters, p.eps);
+            float *dst = p.comb + (size_t)(tok0 + i) * S * S;
+#pragma unroll
+            for (int m = 0; m < S * S; ++m)
+                dst[m] = cm[m];
+        }
+        for (int i = 0; ok && i < ntok; ++i, ++tl) {   // y, in the collapse's order
+            const int b = tl % kHB;
+            ok = __syncthreads_and(threadIdx.x != 0 ||
+                                   wait_bar<false>(TFULL(b), (tl / kHB) & 1, abort_flag, sb, kSiteXFull)) != 0;
+            if (!ok)
+                break;
+            const float4 *xs4 = reinterpret_cast<const float4 *>(tbuf + (size_t)b * (16 * kMaxLK));
+            const float4 pv = *reinterpret_cast<const float4 *>(pre_s + i * 4);
+            const float pr[4] = {pv.x, pv.y, pv.z, pv.w};
+            float *yrow = p.y + (size_t)(tok0 + i) * p.d;
+            for (int e = threadIdx.x; e < d4; e += kHThreads) {
+                float4 xv[S];
+#pragma unroll
+                for (int k = 0; k < S; ++k)
+                    xv[k] = xs4[k * d4 + e];
+                float4 a = make_float4(pr[0] * xv[0].x, pr[0] * xv[0].y, pr[0] * xv[0].z, pr[0] * xv[0].w);
+#pragma unroll
+                for (int k = 1; k < S; ++k) {
+                    a.x = fmaf(pr[k], xv[k].x, a.x);
+                    a.y = fmaf(pr[k], xv[k].y, a.y);
+                    a.z = fmaf(pr[k], xv[k].z, a.z);
+                    a.w = fmaf(pr[k], xv[k].w, a.w);
+                }
+                *reinterpret_cast<float4 *>(yrow + 4 * e) = a;
+            }
+            __syncthreads();   // buffer b is free
+            if (threadIdx.x == 0 && i + kHB < ntok)
+                load_token(i + kHB);
+        }
+        __syncthreads();   // the buffers, pre_s / sink_s / coef_s are free for the next chunk
+    }
+    // ---------------------------------------------------------------- teardown
+    __syncthreads();
+    if (threadIdx.x == 0 && !skip) {   // every load this CTA issued lands before it exits
+        for (int b = 0; b < kHB; ++b) {
+            if (issued[b] > 0)
+                wait_bar<false>(XFULL(b), (issued[b] - 1) & 1, abort_flag, sb, kSiteDrain, false);
+            if (issued[kHB + 1 + b] > 0)
+                wait_bar<false>(TFULL(b), (issued[kHB + 1 + b] - 1) & 1, abort_flag, sb, kSiteDrain, false);
+        }
+        if (issued[kHB] > 0)
+            wait_bar<false>(WFULL, (issued[kHB] - 1) & 1, abort_flag, sb, kSiteDrain, false);
+        if (fused)
+            ptx::bulk_wait_all();
+    }
+    ptx::tmem_fence_before_sync();
+    __syncthreads();
+    ptx::tmem_fence_after_sync();
+    if (warp == 0)
+        ptx::tmem_dealloc(tmem_base, kTmemCols);
+    ptx::griddep_wait();   // the cluster kernel has completed
+}
+
 // ---------------------------------------------------------------------- host side
 
 struct VariantInfo {
@@ -1404,11 +1847,146 @@ bool encode_slab_map(CUtensorMap *m, const float *base, int rows, int s, int d, 
     return tensor_map_f32(m, 4, base, dims, strides, box);
 }
 
+// The helper kernel's partials: [tokens][2 * kCS][RV] floats after the status block (and
+// the stamps of a phase-stamp build).
+size_t helper_part_bytes(int ntok, int s)
+{
+    const int rv = ((2 + s) * s + 1 + 3) / 4 * 4;
+    return (size_t)ntok * 2 * kCS * (size_t)rv * 4;
+}
+
+// How many 8-token tiles the helper takes from the end of a batch of T tokens: the split
+// that evens out the two kernels' times in a model fitted to GB300 timings at d = 4096,
+// s = 4 (a 16-token tile per cluster every pm µs after fm µs; an 8-token tile per helper CTA
+// every ph µs, plus fh µs a chunk of kHMaxTok tokens for its first fn_w slice and its second
+// phase).  The cluster kernel keeps a multiple of 16 tokens and at least one tile per cluster.
+// (Exposed through hc_pre_helper_tokens.)
+struct HelperPlan {
+    int t_main = 0;   // tokens [0, t_main) for the cluster kernel
+    int ntiles = 0;   // helper tiles from t_main (0: no helper)
+    int nh = 0;       // helper CTAs
+};
+
+HelperPlan plan_helper(int T, int nc, int sm_count, bool fused)
+{
+    HelperPlan hp;
+    hp.t_main = T;
+    const int nh = sm_count - kCS * nc;
+    if (nh < 1 || nc < 1)
+        return hp;
+    const double pm = fused ? 4.39 : 3.56, fm = 8.0, ph = fused ? 49.0 : 40.0, fh = fused ? 29.0 : 26.0;
+    auto main_us = [&](int tm) { return std::ceil((double)((tm + kTMT - 1) / kTMT) / nc) * pm + fm; };
+    double best = main_us(T);
+    for (int k = 1;; ++k) {
+        const int tm = (T - k * nh * kHT + kTMT - 1) / kTMT * kTMT;   // helper: at most k tiles a CTA
+        if (tm < kTMT * nc)
+            break;
+        const int htiles = (T - tm + kHT - 1) / kHT;
+        const int per = (htiles + nh - 1) / nh;
+        const double t = std::max(main_us(tm), per * ph + fh * ((per + kHMaxTok / kHT - 1) / (kHMaxTok / kHT)));
+        if (t < best) {
+            best = t;
+            hp.t_main = tm;
+            hp.ntiles = htiles;
+            hp.nh = nh;
+        }
+    }
+    return hp;
+}
+
+struct HelperInfo {
+    unsigned long long ctx = 0;
+    bool ok = false;
+};
+
+template <int S>
+bool helper_ready(int device)
+{
+    static std::mutex mu;
+    static HelperInfo info[64];
+    if (device < 0 || device >= 64)
+        return false;
+    std::lock_guard<std::mutex> lock(mu);
+    HelperInfo &hi = info[device];
+    const unsigned long long ctx = context_id();
+    if (ctx == 0 || hi.ctx != ctx) {
+        hi.ok = cudaFuncSetAttribute(hc_pre_helper_kernel<S>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     make_hlay<S>().total) == cudaSuccess;
+        if (!hi.ok)
+            cudaGetLastError();
+        hi.ctx = hi.ok ? context_id() : 0;
+    }
+    return hi.ok;
+}
+
+// The split for a prefill batch on `device` (no helper if its kernel cannot be set up there
+// or the workspace cannot hold its partials).
+template <int S>
+HelperPlan helper_plan_for(int T, int device, bool fused, size_t ws_bytes, int nc_persist)
+{
+    DeviceInfo di;
+    if (!device_info(di) || !helper_ready<S>(device))
+        return HelperPlan();
+    HelperPlan hp = plan_helper(T, nc_persist, di.sm_count, fused);
+    if (hp.ntiles > 0 && ws_bytes < kStatusBytes + kWorkspaceExtra + helper_part_bytes(T - hp.t_main, S))
+        hp = HelperPlan();
+    return hp;
+}
+
+// Launch the helper kernel behind the cluster kernel just queued on `st` (its parameters
+// p, whose T is already the cluster kernel's share) for the batch's tokens [hp.t_main, T).
+template <int S>
+cudaError_t launch_helper(const Params &p, const HelperPlan &hp, int T, void *workspace, cudaStream_t st)
+{
+    HParams h = {};
+    const bool fused = p.x_new != nullptr;
+    if (!encode_slab_map(&h.tmap_x, p.x, T, S, p.d, p.hs, p.hsc, kHT))
+        return cudaErrorInvalidValue;
+    h.tmap_w = p.tmap_w;
+    if (fused && (!encode_slab_map(&h.tmap_f, p.f, T, 1, p.d, p.hs, p.hsc, kHT) ||
+                  !encode_slab_map(&h.tmap_xnew, p.x_new, T, S, p.d, p.hs, p.hsc, kHT)))
+        return cudaErrorInvalidValue;
+    h.x = p.x;
+    h.scale = p.scale;
+    h.base = p.base;
+    h.post_prev = p.post_prev;
+    h.comb_prev = p.comb_prev;
+    h.pre = p.pre;
+    h.post = p.post;
+    h.comb = p.comb;
+    h.y = p.y;
+    h.x_new = p.x_new;
+    h.part = reinterpret_cast<float *>(static_cast<char *>(workspace) + kStatusBytes + kWorkspaceExtra);
+    h.status = p.status;
+    h.T = T;
+    h.d = p.d;
+    h.hs = p.hs;
+    h.hsc = p.hsc;
+    h.LK = p.LK;
+    h.NJ = p.NJ;
+    h.iters = p.iters;
+    h.t0 = hp.t_main;
+    h.ntiles = hp.ntiles;
+    h.eps = p.eps;
+    h.invK = p.invK;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = dim3((unsigned)hp.nh);
+    cfg.blockDim = dim3(kHThreads);
+    cfg.dynamicSmemBytes = (size_t)make_hlay<S>().total;
+    cfg.stream = st;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, hc_pre_helper_kernel<S>, h);
+}
+
 template <int S, bool HEAD>
 cudaError_t run_s(const float *x, const float *fn_w, const float *scale, const float *base, int T,
                   int d, int iters, float eps, float *pre, float *post, float *comb, float *y,
                   void *workspace, cudaStream_t st, int device, const FusedPost *fp = nullptr,
-                  const NormOut *no = nullptr)
+                  const NormOut *no = nullptr, size_t ws_bytes = 0)
 {
     Params p = {};
     if (no) {
@@ -1472,7 +2050,18 @@ cudaError_t run_s(const float *x, const float *fn_w, const float *scale, const f
             return launch_variant<S, false, 4, HEAD>(p, p.ntiles, st);
         return launch_variant<S, false, 8, HEAD>(p, p.ntiles, st);
     }
-    return launch_variant<S, true, 4, HEAD>(p, min(p.ntiles, nc_persist), st);
+    // Prefill: the persistent clusters, and on the SMs they leave free the helper kernel for
+    // the batch's last tokens (pre-chain and fused modes, when the workspace holds its partials).
+    const HelperPlan hp = (!HEAD && !no) ? helper_plan_for<S>(T, device, p.x_new != nullptr, ws_bytes, nc_persist)
+                                         : HelperPlan();
+    if (hp.ntiles > 0) {
+        p.T = hp.t_main;
+        p.ntiles = hp.t_main / kTMT;
+    }
+    const cudaError_t e = launch_variant<S, true, 4, HEAD>(p, min(p.ntiles, nc_persist), st);
+    if (e != cudaSuccess || hp.ntiles == 0)
+        return e;
+    return launch_helper<S>(p, hp, T, workspace, st);
 }
 
 }  // namespace
@@ -1508,7 +2097,7 @@ bool cluster_fused_supported(int s, int d) { return d / kCS <= kMaxFusedHs && cl
 cudaError_t launch_pre_cluster(const float *x, const float *fn_w, const float *scale,
                                const float *base, int T, int s, int d, int iters, float eps,
                                float *pre, float *post, float *comb, float *y, void *workspace,
-                               cudaStream_t st)
+                               size_t ws_bytes, cudaStream_t st)
 {
     DeviceInfo di;
     if (!device_info(di))
@@ -1517,11 +2106,42 @@ cudaError_t launch_pre_cluster(const float *x, const float *fn_w, const float *s
 #define HC_CASE(S)                                                                                  \
     case S:                                                                                         \
         return run_s<S, false>(x, fn_w, scale, base, T, d, iters, eps, pre, post, comb, y, workspace, st, \
-                               di.device);
+                               di.device, nullptr, nullptr, ws_bytes);
         HC_CASE(1) HC_CASE(2) HC_CASE(3) HC_CASE(4)
 #undef HC_CASE
     default: return cudaErrorInvalidValue;
     }
+}
+
+int cluster_helper_tokens(int T, int s, int d, bool fused, size_t ws_bytes)
+{
+    if (!cluster_supported(s, d, false) || (fused && !cluster_fused_supported(s, d)))
+        return 0;
+    DeviceInfo di;
+    if (!device_info(di))
+        return 0;
+    auto tokens = [&](int nc_decode, int nc_persist, HelperPlan (*plan)(int, int, bool, size_t, int)) {
+        if (nc_decode < 1 || nc_persist < 1 || T <= nc_decode * kTMT)
+            return 0;
+        const HelperPlan hp = plan(T, di.device, fused, ws_bytes, nc_persist);
+        return hp.ntiles > 0 ? T - hp.t_main : 0;
+    };
+    switch (s) {
+#define HC_CASE(S)                                                                                  \
+    case S:                                                                                         \
+        return tokens(max_clusters_for<S, false, 8, false>(di.device), max_clusters_for<S, true, 4, false>(di.device), \
+                      helper_plan_for<S>);
+        HC_CASE(1) HC_CASE(2) HC_CASE(3) HC_CASE(4)
+#undef HC_CASE
+    default: return 0;
+    }
+}
+
+size_t cluster_helper_workspace_bytes(int T, int s, int d)
+{
+    if (T <= 0 || !cluster_shape_ok(s, d))
+        return 0;
+    return kStatusBytes + kWorkspaceExtra + helper_part_bytes(T, s);
 }
 
 bool cluster_norm_supported(int s, int d) { return (d / kCS) % 32 == 0 && cluster_supported(s, d, false); }
@@ -1567,7 +2187,7 @@ cudaError_t launch_post_pre_cluster(const float *x_prev, const float *f, const f
                                     const float *comb_prev, const float *fn_w, const float *scale,
                                     const float *base, int T, int s, int d, int iters, float eps,
                                     float *x_new, float *pre, float *post, float *comb, float *y,
-                                    void *workspace, cudaStream_t st)
+                                    void *workspace, size_t ws_bytes, cudaStream_t st)
 {
     DeviceInfo di;
     if (!device_info(di))
@@ -1577,7 +2197,7 @@ cudaError_t launch_post_pre_cluster(const float *x_prev, const float *f, const f
 #define HC_CASE(S)                                                                                  \
     case S:                                                                                         \
         return run_s<S, false>(x_prev, fn_w, scale, base, T, d, iters, eps, pre, post, comb, y, workspace, \
-                               st, di.device, &fp);
+                               st, di.device, &fp, nullptr, ws_bytes);
         HC_CASE(1) HC_CASE(2) HC_CASE(3) HC_CASE(4)
 #undef HC_CASE
     default: return cudaErrorInvalidValue;

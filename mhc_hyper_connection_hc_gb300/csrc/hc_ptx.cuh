@@ -252,6 +252,26 @@ __device__ __forceinline__ void fence_proxy_async_smem()
 {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
+// Order this thread's completed bulk (async-proxy) writes to global memory before its
+// later generic-proxy accesses.
+__device__ __forceinline__ void fence_proxy_async_global()
+{
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// ---------------------------------------------------------------- programmatic dependent launch
+// The kernel launched after this one on the stream with programmatic stream serialization
+// may start once every CTA of this grid has executed this (or exited).
+__device__ __forceinline__ void griddep_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+// Wait until the grids this one was launched behind have completed and their memory
+// operations are visible (returns at once when there are none).
+__device__ __forceinline__ void griddep_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
 
 // ---------------------------------------------------------------- cluster / DSMEM
 __device__ __forceinline__ uint32_t mapa(uint32_t local_smem, uint32_t rank)

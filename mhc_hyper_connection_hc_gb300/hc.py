@@ -26,7 +26,7 @@ HC_ERR_TOO_LARGE = 9
 HC_PATH_AUTO, HC_PATH_GENERIC, HC_PATH_CLUSTER, HC_PATH_WIDE = 0, 1, 2, 3
 
 EXPORTED = ("hc_status_string", "hc_expand", "hc_pre_workspace_bytes", "hc_workspace_init",
-            "hc_workspace_status", "hc_pre_fused", "hc_pre_fused_path", "hc_pre_auto_path",
+            "hc_workspace_status", "hc_pre_fused", "hc_pre_fused_path", "hc_pre_auto_path", "hc_pre_helper_tokens",
             "hc_post", "hc_mean", "hc_pre_fused_noalloc", "hc_head", "hc_head_path",
             "hc_post_pre_fused", "hc_post_pre_fused_path", "hc_rms_norm_q8", "hc_pre_fused_norm",
             "hc_pre_fused_norm_path")
@@ -58,6 +58,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.hc_workspace_init.argtypes = [vp, sz, vp]
     lib.hc_workspace_status.argtypes = [vp, vp]
     lib.hc_pre_auto_path.argtypes = [i, i, i]
+    lib.hc_pre_helper_tokens.argtypes = [i, i, i, i, sz]
     pre_args = [vp, vp, vp, vp, i, i, i, i, f, vp, vp, vp, vp, vp, sz, vp]
     lib.hc_pre_fused.argtypes = pre_args
     lib.hc_pre_fused_path.argtypes = pre_args + [i]
@@ -186,6 +187,11 @@ def hc_workspace_status(workspace: torch.Tensor, stream=None) -> int:
 
 def hc_pre_auto_path(T: int, s: int, d: int) -> int:
     return int(load().hc_pre_auto_path(T, s, d))
+
+
+def hc_pre_helper_tokens(T: int, s: int, d: int, fused: bool, ws_bytes: int) -> int:
+    """Tokens the cluster path's helper kernel takes from the end of such a batch (0: none)."""
+    return int(load().hc_pre_helper_tokens(T, s, d, int(bool(fused)), int(ws_bytes)))
 
 
 def hc_pre_fused(x, fn_w, scale, base, iters: int, eps: float, pre, post, comb, y, workspace,
