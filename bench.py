@@ -355,6 +355,12 @@ def run_gpu(args):
     path_name = {hc.HC_PATH_CLUSTER: "cluster", hc.HC_PATH_WIDE: "wide"}.get(path, "generic")
     fused = args.pipeline == "fused"
     fused_cluster = path == hc.HC_PATH_CLUSTER and d // 16 <= 256   # else hc_post + generic pre
+    # On the cluster path at prefill sizes a helper kernel runs behind the cluster kernel on
+    # the SMs its clusters leave free, for the batch's last tokens (one more launch per call).
+    help_pre = max(0, hc.hc_pre_helper_tokens(T, s, d, False, ws.numel()))
+    help_fused = max(0, hc.hc_pre_helper_tokens(T, s, d, True, ws.numel())) if fused_cluster else 0
+    pre_launches += 1 if help_pre else 0
+    fused_launches = (1 + (1 if help_fused else 0)) if fused_cluster else 1 + pre_launches
     if fused:
         # The previous site's gates (this trio on this state, computed once) and the
         # new state: a step is site i's hc_post fused with site i+1's pre-chain.
@@ -451,7 +457,7 @@ def run_gpu(args):
                          "TFLOP/s": pre_flops / pre_avg / 1e12,
                          "frac_fp32": pre_flops / pre_avg / 1e12 / fp32_peak,
                          "launches_per_step": pre_launches,
-                         "path": path_name},
+                         "path": path_name, "helper_tokens": help_pre},
         "hc_post": {"us": post_avg * 1e6, "algorithmic_bytes": post_bytes,
                     "GB/s": post_bytes / post_avg / 1e9, "frac_hbm": post_bytes / post_avg / 1e9 / peak,
                     "launches_per_step": 1},
@@ -464,8 +470,9 @@ def run_gpu(args):
             "frac_hbm": fz_bytes / fz_avg / 1e9 / peak,
             "TFLOP/s": (pre_flops + 2 * (s + 1) * s * d * T) / fz_avg / 1e12,
             "frac_fp32": (pre_flops + 2 * (s + 1) * s * d * T) / fz_avg / 1e12 / fp32_peak,
-            "launches_per_step": 1 if fused_cluster else 1 + pre_launches,
-            "path": "cluster" if fused_cluster else f"{path_name} (hc_post, then the {path_name} pre-chain)"}
+            "launches_per_step": fused_launches,
+            "path": "cluster" if fused_cluster else f"{path_name} (hc_post, then the {path_name} pre-chain)",
+            "helper_tokens": help_fused}
         kernels["hc_pre_fused"]["launches_per_step"] = 0
         kernels["hc_post"]["launches_per_step"] = 0
         dom = "hc_post_pre_fused"
@@ -502,10 +509,11 @@ def run_gpu(args):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic", "config": dict(workload_config(w), pipeline=args.pipeline, step=(
                 "site boundary: the previous site's hc_post fused with this site's pre-chain "
-                "(hc_post_pre_fused, one launch; the same work as hc_pre_fused + hc_post)"
+                "(hc_post_pre_fused, one call: the cluster kernel and, on the SMs its clusters leave "
+                "free, the helper kernel for the batch's last tokens; the same work as hc_pre_fused + hc_post)"
                 if fused else "hc_pre_fused then hc_post")), "roofline": roofline,
             "kernels": kernels,
-            "gpu_launches": ((1 if fused_cluster else pre_launches + 1) if fused else pre_launches + 1) * K,
+            "gpu_launches": (fused_launches if fused else pre_launches + 1) * K,
             "clocks": clocks,
             "kernel_sources": src_hash}
 
