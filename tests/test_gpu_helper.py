@@ -130,3 +130,53 @@ def test_helper_not_used_for_small_batches_or_other_modes():
     assert hc.hc_pre_helper_tokens(4096, S, D, False, 256) == 0
     assert hc.hc_pre_helper_tokens(4096, 8, 7168, False, big) == 0   # the wide path's shape
     assert hc.hc_pre_helper_tokens(-1, S, D, False, big) == -1
+
+
+@pytest.mark.parametrize("T,s,d", [(4096, 3, 3072), (3000, 2, 2048), (2600, 1, 1024), (2500, 4, 1024)])
+def test_helper_other_shapes_bit_identical_and_against_oracle(T, s, d):
+    """The helper's other stream counts and slice widths: every token bit for bit against the
+    cluster kernel alone (pre-chain and fused), and sampled tokens from both kernels' ranges
+    against the float64 oracle."""
+    import oracle
+    from hc_testutil import TOL, eps32, rel_err
+    from mhc_hyper_connection_hc_gb300 import hc
+    if hc.hc_pre_auto_path(T, s, d) != hc.HC_PATH_CLUSTER:
+        pytest.skip("cluster path not available")
+    inp = synth.site_inputs(190 + s, T, s, d)
+    dv = {k: _up(v) for k, v in inp.items()}
+    big = hc.new_workspace(T, s, d)
+    small = _small_ws()
+    n_help = hc.hc_pre_helper_tokens(T, s, d, False, big.numel())
+    if n_help == 0:
+        pytest.skip("the split model gives the helper nothing at this shape")
+    outs = []
+    for ws in (big, small):
+        o = hc.new_pre_outputs(T, s, d)
+        hc.hc_pre_fused(dv["x"], dv["fn_w"], dv["scale"], dv["base"], 20, 1e-6, o["pre"], o["post"], o["comb"],
+                        o["y"], ws)
+        torch.cuda.synchronize()
+        assert hc.hc_workspace_status(ws) == hc.HC_OK
+        outs.append(o)
+    for k in ("pre", "post", "comb", "y"):
+        assert torch.equal(_bits(outs[0][k]), _bits(outs[1][k])), k
+    toks = np.unique(np.array([0, 1, T - n_help - 1, T - n_help, T - n_help + 7, T - n_help + 8, T // 2, T - 9, T - 1]))
+    want = oracle.pre(inp["x"][toks], inp["fn_w"], inp["scale"], inp["base"], 20, eps32(1e-6))
+    for k in ("pre", "post", "comb", "y"):
+        got = outs[0][k][torch.from_numpy(toks).cuda()].cpu().numpy()
+        assert rel_err(got, want[k]) <= TOL, k
+    # fused boundary at the same shape, when the cluster kernel takes it
+    if hc.hc_pre_helper_tokens(T, s, d, True, big.numel()) == 0:
+        return
+    post_prev, comb_prev = outs[0]["post"].clone(), outs[0]["comb"].clone()
+    res = []
+    for ws in (big, small):
+        o = hc.new_pre_outputs(T, s, d)
+        x_new = torch.empty_like(dv["x"])
+        hc.hc_post_pre_fused(dv["x"], dv["f"], post_prev, comb_prev, dv["fn_w"], dv["scale"], dv["base"], 20, 1e-6,
+                             x_new, o["pre"], o["post"], o["comb"], o["y"], ws)
+        torch.cuda.synchronize()
+        assert hc.hc_workspace_status(ws) == hc.HC_OK
+        o["x_new"] = x_new
+        res.append(o)
+    for k in ("x_new", "pre", "post", "comb", "y"):
+        assert torch.equal(_bits(res[0][k]), _bits(res[1][k])), "fused " + k
