@@ -49,7 +49,7 @@ def _paths(s, d):
 
 
 @pytest.mark.parametrize("T,s,d", [(37, 4, 4096), (19, 1, 1024), (133, 3, 3072), (17, 3, 4100), (5, 8, 7168),
-                                   (130, 8, 2048), (9, 5, 4096)])
+                                   (130, 8, 2048), (9, 5, 4096), (2050, 4, 1024)])
 def test_outputs_stay_inside_their_buffers(T, s, d):
     from mhc_hyper_connection_hc_gb300 import hc
     inp = synth.site_inputs(970 + T, T, s, d)
@@ -110,9 +110,9 @@ def test_device_error_word_is_reported_and_sticky():
     assert torch.equal(out["y"], y_before)                                   # the context is still usable
 
 
-@pytest.mark.parametrize("T,s,d", [(37, 4, 4096), (1, 4, 4096), (9, 8, 7168)])
+@pytest.mark.parametrize("T,s,d", [(37, 4, 4096), (1, 4, 4096), (9, 8, 7168), (2048, 4, 4096)])
 def test_nonzero_status_word_makes_waiting_kernels_skip(T, s, d):
-    """While the status word is non-zero, the cluster and wide kernels (the ones with
+    """While the status word is non-zero, the cluster, helper and wide kernels (the ones with
     bounded waits) do nothing: the call returns HC_OK, every output keeps its sentinel
     (NaN), the word is unchanged.  After hc_workspace_init the same call writes them."""
     from mhc_hyper_connection_hc_gb300 import hc
