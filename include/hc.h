@@ -67,8 +67,9 @@ enum hc_pre_path {
     HC_PATH_AUTO = 0,     /* what hc_pre_fused runs                                   */
     HC_PATH_GENERIC = 1,  /* any supported shape: split-K mixes kernel + finish kernel */
     HC_PATH_CLUSTER = 2,  /* one fused launch, x read once: thread-block clusters split
-                             the hidden dimension; needs s <= 4 and s*d <= 16384 with
-                             d % 64 == 0                                               */
+                             the hidden dimension (at prefill sizes with the helper
+                             kernel beside it: hc_pre_helper_tokens); needs s <= 4 and
+                             s*d <= 16384 with d % 64 == 0                             */
     HC_PATH_WIDE = 3      /* one fused launch over every SM, x read once from HBM, for
                              5 <= s <= 8: each CTA keeps a fixed hidden range of fn_w
                              resident.  Needs d split over at least 32 CTAs (at most one
