@@ -180,3 +180,44 @@ def test_helper_other_shapes_bit_identical_and_against_oracle(T, s, d):
         res.append(o)
     for k in ("x_new", "pre", "post", "comb", "y"):
         assert torch.equal(_bits(res[0][k]), _bits(res[1][k])), "fused " + k
+
+
+def test_helper_inside_a_cuda_graph():
+    """A prefill call whose helper kernel is launched behind the cluster kernel (programmatic
+    dependent launch) captures into a CUDA graph; the replays give the eager call's bits, and
+    work queued after the graph sees both kernels' outputs (hc_post on the new state)."""
+    from mhc_hyper_connection_hc_gb300 import hc
+    T = 4096
+    if hc.hc_pre_auto_path(T, S, D) != hc.HC_PATH_CLUSTER:
+        pytest.skip("cluster path not available")
+    dv = _inputs(175, T)
+    ws = hc.new_workspace(T, S, D)
+    assert hc.hc_pre_helper_tokens(T, S, D, True, ws.numel()) > 0
+    ref = hc.new_pre_outputs(T, S, D)
+    x_ref = torch.empty(T, S, D, device="cuda")
+    hc.hc_post_pre_fused(dv["x"], dv["f"], dv["post_prev"], dv["comb_prev"], dv["fn_w"], dv["scale"], dv["base"],
+                         20, 1e-6, x_ref, ref["pre"], ref["post"], ref["comb"], ref["y"], ws)
+    torch.cuda.synchronize()
+    got = {k: torch.full_like(v, float("nan")) for k, v in ref.items()}
+    x_new = torch.full_like(x_ref, float("nan"))
+    after = torch.empty_like(x_ref)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(g, stream=side):
+            hc.hc_post_pre_fused(dv["x"], dv["f"], dv["post_prev"], dv["comb_prev"], dv["fn_w"], dv["scale"],
+                                 dv["base"], 20, 1e-6, x_new, got["pre"], got["post"], got["comb"], got["y"], ws)
+            hc.hc_post(x_new, got["y"], got["post"], got["comb"], after)
+    torch.cuda.current_stream().wait_stream(side)
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    assert hc.hc_workspace_status(ws) == hc.HC_OK
+    assert torch.equal(_bits(x_new), _bits(x_ref))
+    for k in ref:
+        assert torch.equal(_bits(got[k]), _bits(ref[k])), k
+    want_after = torch.empty_like(x_ref)
+    hc.hc_post(x_ref, ref["y"], ref["post"], ref["comb"], want_after)
+    torch.cuda.synchronize()
+    assert torch.equal(_bits(after), _bits(want_after))
