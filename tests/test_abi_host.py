@@ -154,6 +154,21 @@ def test_workspace_sizes(lib):
             assert n <= max(generic, wide)
 
 
+def test_workspace_holds_the_helper_partials(lib):
+    """Shapes the cluster path takes have room in hc_pre_workspace_bytes for the helper
+    kernel's partials (after the 256-byte status word: 2 x 16 slices x RV floats a token);
+    the helper query refuses bad dimensions and, without a device, reports no helper."""
+    for T in (1, 37, 4096, 16390):
+        for s, d in ((4, 4096), (3, 3072), (2, 2048), (1, 1024), (4, 1024)):
+            rv = ((2 + s) * s + 1 + 3) // 4 * 4
+            assert hc.hc_pre_workspace_bytes(T, s, d) >= 256 + T * 32 * rv * 4
+    assert hc.hc_pre_helper_tokens(-1, 4, 4096, False, 1 << 30) == -1
+    assert hc.hc_pre_helper_tokens(4096, 9, 4096, False, 1 << 30) == -1
+    assert hc.hc_pre_helper_tokens(0, 4, 4096, True, 1 << 30) == 0
+    if not DEVICE_VISIBLE:
+        assert hc.hc_pre_helper_tokens(4096, 4, 4096, False, 1 << 30) == 0
+
+
 def head_rc(lib, x=A, fn_w=A + 32 * MB, scale=A + 40 * MB, base=A + 40 * MB + 64, gates=A + 41 * MB,
             y=A + 42 * MB, ws=A + 64 * MB, ws_bytes=16 * MB, T=2, s=4, d=4096, eps=1e-6, path=0):
     return lib.hc_head_path(x, fn_w, scale, base, T, s, d, eps, gates, y, ws, ws_bytes, None, path)
