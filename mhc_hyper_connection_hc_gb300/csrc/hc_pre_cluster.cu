@@ -1301,10 +1301,12 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const __gri
 // every token's outputs are the same bits whichever kernel computed them:
 //  * phase 1, slice c = 0..15 (hidden columns [c*hs, (c+1)*hs) of every stream): the fn_w
 //    slice into TMEM (staged through shared memory while the previous slice is in use, then
-//    copied in one pass); then for each of the CTA's tiles the tile's slice by TMA (two
-//    buffers, one tile ahead; fused mode: with the f slice, then the previous site's hc_post
-//    in place and the x' slice stored by TMA), the eight warps' dots, the 16-lane
-//    reduce-scatter, and the two column halves' partials of every token into the workspace;
+//    copied by each thread into its own lane); then for each of the CTA's tiles the tile's
+//    slice by TMA (three buffers, two steps ahead; fused mode: with the f slice, then the
+//    previous site's hc_post in place and the x' slice stored by TMA), the eight warps' dots,
+//    the 16-lane reduce-scatter, and the two column halves' partials of every token into the
+//    workspace.  In the pre-chain mode the warps never wait for one another here: the last
+//    warp done with a buffer refills it;
 //  * phase 2: per token, the 2 x 16 partials in the finisher's order, the gates, pre/post;
 //    the Sinkhorn, one token per thread; then y over all d columns from x (fused: x') read
 //    back from memory.
@@ -1358,8 +1360,8 @@ __host__ __device__ inline HLay make_hlay()
     o += kHMaxTok * 4 * 4;
     L.off_bar = o;    // xfull[kHB], wfull, tfull[kHB]
     o += (2 * kHB + 1) * 8;
-    L.off_misc = o;   // abort flag; loads issued into each x buffer, fn_w, each token buffer; TMEM address
-    o += 48;
+    L.off_misc = o;   // abort flag; loads issued into each x buffer, fn_w, each token buffer; TMEM address;
+    o += 64;          // the warps done with the fn_w staging buffer, with each x buffer
     L.total = o;
     return L;
 }
@@ -1388,6 +1390,8 @@ __global__ void __launch_bounds__(kHThreads, 1) hc_pre_helper_kernel(const __gri
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L.off_misc);
     volatile int *issued = reinterpret_cast<volatile int *>(smem + L.off_misc + 4);   // x [kHB], fn_w, tokens [kHB]
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L.off_misc + 40);
+    int *rel_w = reinterpret_cast<int *>(smem + L.off_misc + 44);   // then rel_x[kHB]
+    int *rel_x = rel_w + 1;
     StatusBlock *sb = p.status;
     const bool fused = p.x_new != nullptr;
     // This CTA's tiles [k0, k1), taken in chunks of at most kHCT tiles (kHMaxTok tokens):
@@ -1408,6 +1412,8 @@ __global__ void __launch_bounds__(kHThreads, 1) hc_pre_helper_kernel(const __gri
         ptx::mbar_init(WFULL, 1);
         for (int i = 0; i < 2 * kHB + 1; ++i)
             issued[i] = 0;
+        for (int i = 0; i < kHB + 1; ++i)
+            rel_w[i] = 0;
         *abort_flag = *reinterpret_cast<volatile unsigned *>(&sb->code) != 0u ? 2 : 0;
         ptx::fence_mbar_init_cluster();
     }
@@ -1461,8 +1467,8 @@ __global__ void __launch_bounds__(kHThreads, 1) hc_pre_helper_kernel(const __gri
         const int tok0 = p.t0 + (k0 + q * kHCT) * kHT;   // the chunk's first token
         const int ntok = min(p.T, tok0 + nq * kHT) - tok0;
         const int g0 = kCS * kHCT * q, g1 = g0 + kCS * nq;   // the chunk's steps
-        if (threadIdx.x == 0) {   // fn_w slice 0 and the first two steps (phase 2 of the last chunk
-            load_w(0);            // is done with the buffers)
+        if (threadIdx.x == 0) {   // fn_w slice 0 and the first kHB steps (phase 2 of the last
+            load_w(0);            // chunk is done with the buffers)
             for (int g = g0; g < g0 + kHB && g < g1; ++g)
                 issue(g);
         }
@@ -1472,41 +1478,56 @@ __global__ void __launch_bounds__(kHThreads, 1) hc_pre_helper_kernel(const __gri
                 coef_s[e] = cc < S ? __ldg(p.post_prev + (size_t)(tok0 + tt) * S + cc)
                                    : __ldg(p.comb_prev + (size_t)(tok0 + tt) * S * S + (cc - S));
             }
+            __syncthreads();
         }
         // ------------------------------------------------------------ phase 1: slices
-        for (int c = 0; ok && c < kCS; ++c) {
+        // Pre-chain mode: no CTA barrier.  Each warp waits for a buffer itself, and the last of
+        // the eight warps to be done with a buffer (a shared counter) issues its next load, which
+        // saves the two CTA-wide barriers a step of the plain scheme.  Fused mode:
+        // the transform makes each step's tokens depend on all eight warps, so one barrier per
+        // step; thread 0 then stores x', loads the next fn_w slice (step 0 of a slice: every
+        // warp has copied the current one) and refills the previous step's buffer.
+        for (int c = 0; c < kCS; ++c) {
             // fn_w slice c: staged in shared memory (loaded during slice c - 1), then copied into
-            // this thread's TMEM lane, which every warp is done reading for slice c - 1: warp
-            // (rg, half) lane kg's values of column group jj at columns half*8*WQ + jj*WQ, row r's
-            // pairs (2kg, 2kg+1) and (32+2kg, 33+2kg) at 4r .. 4r+3 (rows past R zero).
-            ok = __syncthreads_and(threadIdx.x != 0 || wait_bar<false>(WFULL, c & 1, abort_flag, sb, kSiteWFull)) != 0;
-            if (!ok)
+            // this thread's TMEM lane, which only this thread reads: warp (rg, half) lane kg's
+            // values of column group jj at columns half*8*WQ + jj*WQ, row r's pairs (2kg, 2kg+1)
+            // and (32+2kg, 33+2kg) at 4r .. 4r+3 (rows past R zero).
+            if (ok)
+                ok = warp_wait<false>(lane, WFULL, c & 1, abort_flag, sb, kSiteWFull);
+            if (!ok && !fused)
                 break;
-            for (int jj = 0; jj < nj; ++jj) {
-                const int col = 64 * (j0 + jj) + 2 * kg;
+            if (ok) {
+                for (int jj = 0; jj < nj; ++jj) {
+                    const int col = 64 * (j0 + jj) + 2 * kg;
 #pragma unroll
-                for (int r = 0; r < G::B; ++r) {
-                    const int row = rg * G::B + r;
-                    float2 v0 = make_float2(0.f, 0.f), v1 = make_float2(0.f, 0.f);
-                    if (row < G::R) {
-                        v0 = *reinterpret_cast<const float2 *>(wsm + row * p.LK + col);
-                        v1 = *reinterpret_cast<const float2 *>(wsm + row * p.LK + col + 32);
+                    for (int r = 0; r < G::B; ++r) {
+                        const int row = rg * G::B + r;
+                        float2 v0 = make_float2(0.f, 0.f), v1 = make_float2(0.f, 0.f);
+                        if (row < G::R) {
+                            v0 = *reinterpret_cast<const float2 *>(wsm + row * p.LK + col);
+                            v1 = *reinterpret_cast<const float2 *>(wsm + row * p.LK + col + 32);
+                        }
+                        const float a[4] = {v0.x, v0.y, v1.x, v1.y};
+                        ptx::tmem_st4(trow + (uint32_t)(tcol0 + jj * G::WQ + 4 * r), a);
                     }
-                    const float a[4] = {v0.x, v0.y, v1.x, v1.y};
-                    ptx::tmem_st4(trow + (uint32_t)(tcol0 + jj * G::WQ + 4 * r), a);
+                }
+                ptx::tmem_wait_st();
+            }
+            if (!fused) {
+                __syncwarp();
+                if (lane == 0) {   // the last warp out of the staging buffer refills it
+                    __threadfence_block();
+                    if (atomicAdd(rel_w, 1) % 8 == 7 && c + 1 < kCS) {
+                        __threadfence_block();
+                        load_w(c + 1);
+                    }
                 }
             }
-            ptx::tmem_wait_st();
-            ptx::tmem_fence_before_sync();
-            __syncthreads();   // the staging buffer is free, the slice is in TMEM
-            ptx::tmem_fence_after_sync();
-            if (threadIdx.x == 0 && c + 1 < kCS)
-                load_w(c + 1);
-            for (int j = 0; ok && j < nq; ++j) {
+            for (int j = 0; j < nq; ++j) {
                 const int g = kCS * kHCT * q + c * nq + j, b = g % kHB;
-                ok = __syncthreads_and(threadIdx.x != 0 ||
-                                       wait_bar<false>(XFULL(b), (g / kHB) & 1, abort_flag, sb, kSiteXFull)) != 0;
-                if (!ok)
+                if (ok)
+                    ok = warp_wait<false>(lane, XFULL(b), (g / kHB) & 1, abort_flag, sb, kSiteXFull);
+                if (!ok && !fused)
                     break;
                 const int t0 = tok0 + j * kHT;
                 const int tm = min(kHT, p.T - t0);
@@ -1515,7 +1536,7 @@ __global__ void __launch_bounds__(kHThreads, 1) hc_pre_helper_kernel(const __gri
                     // The previous site's hc_post on the slice, in place (hc_post's operations
                     // in hc_post's order): warp t owns token t of the tile, lanes its float4s.
                     const int t = warp;
-                    if (t < tm) {
+                    if (ok && t < tm) {
                         float cf[NC];
 #pragma unroll
                         for (int m = 0; m < NC; ++m)
@@ -1545,10 +1566,18 @@ __global__ void __launch_bounds__(kHThreads, 1) hc_pre_helper_kernel(const __gri
                         }
                     }
                     ptx::fence_proxy_async_smem();   // the TMA store reads the slice
-                    __syncthreads();
+                    ok = __syncthreads_and(ok ? 1 : 0) != 0;
+                    if (!ok)
+                        break;
                     if (threadIdx.x == 0) {
                         ptx::tma_store_4d(&p.tmap_xnew, 0, c * p.hsc, 0, t0, ptx::smem_u32(xs));
                         ptx::bulk_commit();
+                        if (j == 0 && c + 1 < kCS)
+                            load_w(c + 1);
+                        if (g > g0 && g - 1 + kHB < g1) {   // step g - 1's buffer, once its x' is read
+                            ptx::bulk_wait_read<1>();
+                            issue(g - 1 + kHB);
+                        }
                     }
                 }
                 // The decode variant's dots of slice c: warp (row group rg, column half),
@@ -1604,13 +1633,19 @@ __global__ void __launch_bounds__(kHThreads, 1) hc_pre_helper_kernel(const __gri
                         p.part[((size_t)tr * 2 * kCS + 2 * c + half) * G::RV + vid] = v[m];
                     }
                 }
-                __syncthreads();   // buffer b is free (fused: once its x' store has read it)
-                if (threadIdx.x == 0 && g + kHB < g1) {
-                    if (fused)
-                        ptx::bulk_wait_read<0>();
-                    issue(g + kHB);
+                if (!fused) {
+                    __syncwarp();
+                    if (lane == 0) {   // the last warp out of buffer b refills it
+                        __threadfence_block();
+                        if (atomicAdd(rel_x + b, 1) % 8 == 7 && g + kHB < g1) {
+                            __threadfence_block();
+                            issue(g + kHB);
+                        }
+                    }
                 }
             }
+            if (!ok)
+                break;
         }
         // ------------------------------------------------------------ phase 2: the chunk's tokens
         ok = __syncthreads_and(ok ? 1 : 0) != 0;
@@ -1874,7 +1909,7 @@ HelperPlan plan_helper(int T, int nc, int sm_count, bool fused)
     const int nh = sm_count - kCS * nc;
     if (nh < 1 || nc < 1)
         return hp;
-    const double pm = fused ? 4.39 : 3.56, fm = 8.0, ph = fused ? 49.0 : 40.0, fh = fused ? 29.0 : 26.0;
+    const double pm = fused ? 4.39 : 3.56, fm = 8.0, ph = fused ? 46.0 : 37.0, fh = fused ? 29.0 : 26.0;
     auto main_us = [&](int tm) { return std::ceil((double)((tm + kTMT - 1) / kTMT) / nc) * pm + fm; };
     double best = main_us(T);
     for (int k = 1;; ++k) {
