@@ -320,16 +320,18 @@ __device__ __forceinline__ float tree_sum(const float *v)
 }
 
 // Sinkhorn on an S x S matrix held in registers: `iters` rounds of dividing
-// each row by (row sum + eps), then each column by (column sum + eps).  The
-// reciprocal is the hardware approximation (__fdividef, within 2 ulp); the
-// Sinkhorn's error budget against the float64 oracle is 1e-4.
+// each row by (row sum + eps), then each column by (column sum + eps).  Each
+// division is a multiply by the hardware's approximate reciprocal
+// (`rcp.approx.ftz.f32`, within 1 ulp; a sum of positive terms plus eps is never
+// subnormal), one instruction on the Sinkhorn's serial chain; the Sinkhorn's error
+// budget against the float64 oracle is 1e-4.
 template <int S>
 __device__ __forceinline__ void sinkhorn_regs(float *c, int iters, float eps)
 {
     for (int it = 0; it < iters; ++it) {
 #pragma unroll
         for (int j = 0; j < S; ++j) {
-            const float inv = __fdividef(1.0f, tree_sum<S>(c + j * S) + eps);
+            const float inv = ptx::rcp_approx(tree_sum<S>(c + j * S) + eps);
 #pragma unroll
             for (int k = 0; k < S; ++k)
                 c[j * S + k] *= inv;
@@ -340,7 +342,7 @@ __device__ __forceinline__ void sinkhorn_regs(float *c, int iters, float eps)
 #pragma unroll
             for (int j = 0; j < S; ++j)
                 col[j] = c[j * S + k];
-            const float inv = __fdividef(1.0f, tree_sum<S>(col) + eps);
+            const float inv = ptx::rcp_approx(tree_sum<S>(col) + eps);
 #pragma unroll
             for (int j = 0; j < S; ++j)
                 c[j * S + k] *= inv;

@@ -40,6 +40,15 @@ __device__ __forceinline__ uint64_t globaltimer()
     return t;
 }
 
+// The hardware's approximate reciprocal (PTX `rcp.approx.ftz.f32`: within 1 ulp for
+// normal inputs, subnormal inputs and results flushed to zero).
+__device__ __forceinline__ float rcp_approx(float x)
+{
+    float r;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
+
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
 {
