@@ -221,3 +221,38 @@ def test_helper_inside_a_cuda_graph():
     hc.hc_post(x_ref, ref["y"], ref["post"], ref["comb"], want_after)
     torch.cuda.synchronize()
     assert torch.equal(_bits(after), _bits(want_after))
+
+
+@pytest.mark.parametrize("fused", [False, True])
+def test_helper_runs_repeat_bit_for_bit(fused):
+    """In the pre-chain mode the helper's eight warps wait for their tile buffers each on its
+    own and the last warp done with a buffer refills it (no barrier between steps); in the
+    fused mode one barrier a step orders the in-place transform.  Twenty back-to-back calls of
+    each must give the cluster kernel's bits on every token every time."""
+    from mhc_hyper_connection_hc_gb300 import hc
+    T = 4096
+    if hc.hc_pre_auto_path(T, S, D) != hc.HC_PATH_CLUSTER:
+        pytest.skip("cluster path not available")
+    dv = _inputs(7, T)
+    big = hc.new_workspace(T, S, D)
+    small = _small_ws()
+    assert hc.hc_pre_helper_tokens(T, S, D, fused, big.numel()) > 0
+
+    def run(ws):
+        o = hc.new_pre_outputs(T, S, D)
+        if fused:
+            o["x_new"] = torch.empty(T, S, D, device="cuda")
+            hc.hc_post_pre_fused(dv["x"], dv["f"], dv["post_prev"], dv["comb_prev"], dv["fn_w"], dv["scale"],
+                                 dv["base"], 20, 1e-6, o["x_new"], o["pre"], o["post"], o["comb"], o["y"], ws)
+        else:
+            hc.hc_pre_fused(dv["x"], dv["fn_w"], dv["scale"], dv["base"], 20, 1e-6, o["pre"], o["post"],
+                            o["comb"], o["y"], ws)
+        return o
+
+    ref = run(small)
+    runs = [run(big) for _ in range(20)]
+    torch.cuda.synchronize()
+    assert hc.hc_workspace_status(big) == hc.HC_OK
+    for i, o in enumerate(runs):
+        for k in ref:
+            assert torch.equal(_bits(o[k]), _bits(ref[k])), f"call {i}: {k} differs from the cluster kernel's"
