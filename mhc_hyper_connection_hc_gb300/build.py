@@ -6,6 +6,11 @@ target is sm_103a (GB300): -gencode arch=compute_103a,code=sm_103a.
 build(stamps=True) builds the phase-stamp variant instead, with -DHC_STAMPS, as
 _lib/stamps/libmhc_gb300_stamps.so: the same library, whose cluster pre kernel also
 writes %globaltimer stamps at phase boundaries into the workspace (see hc_internal.cuh).
+
+build(bounds=True) builds the bounds-checked variant, with -DHC_DEBUG_BOUNDS, as
+_lib/bounds/libmhc_gb300_bounds.so: the cluster and helper kernels check each global
+store against its buffer's size and report a refused store in the status word instead
+of performing it (see hc_internal.cuh).
 """
 
 from __future__ import annotations
@@ -22,6 +27,8 @@ OUT_DIR = os.path.join(HERE, "_lib")
 LIB = os.path.join(OUT_DIR, "libmhc_gb300.so")
 STAMPS_DIR = os.path.join(OUT_DIR, "stamps")
 STAMPS_LIB = os.path.join(STAMPS_DIR, "libmhc_gb300_stamps.so")
+BOUNDS_DIR = os.path.join(OUT_DIR, "bounds")
+BOUNDS_LIB = os.path.join(BOUNDS_DIR, "libmhc_gb300_bounds.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
@@ -50,10 +57,15 @@ def _stale(lib: str) -> bool:
     return any(os.path.getmtime(p) > t for p in _deps() + [__file__])
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=(), stamps: bool = False) -> str:
-    lib, out_dir = (STAMPS_LIB, STAMPS_DIR) if stamps else (LIB, OUT_DIR)
+def build(force: bool = False, verbose: bool = False, extra_flags=(), stamps: bool = False,
+          bounds: bool = False) -> str:
+    if stamps and bounds:
+        raise ValueError("build one variant at a time: stamps or bounds")
+    lib, out_dir = (STAMPS_LIB, STAMPS_DIR) if stamps else (BOUNDS_LIB, BOUNDS_DIR) if bounds else (LIB, OUT_DIR)
     if stamps:
         extra_flags = list(extra_flags) + ["-DHC_STAMPS"]
+    if bounds:
+        extra_flags = list(extra_flags) + ["-DHC_DEBUG_BOUNDS"]
     if not force and not _stale(lib):
         return lib
     os.makedirs(out_dir, exist_ok=True)

@@ -60,6 +60,7 @@ constexpr size_t kWorkspaceExtra = 0;
 enum DevErr : unsigned int {
     kDevOk = 0,
     kDevWaitTimeout = 1,   // a bounded wait on an mbarrier gave up
+    kDevBounds = 2,        // (bounds-checked build) a store fell outside its buffer and was skipped
 };
 
 __device__ __forceinline__ void report_error(StatusBlock *sb, unsigned int code, unsigned int where)
@@ -68,6 +69,31 @@ __device__ __forceinline__ void report_error(StatusBlock *sb, unsigned int code,
         sb->where = where;
         sb->block = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
     }
+}
+
+// ---------------------------------------------------------------- bounds-checked stores
+// A build with -DHC_DEBUG_BOUNDS (build.build(bounds=True), a separate library) checks the
+// plain global stores of the cluster and helper kernels (y, pre, post, comb and the helper's
+// partials) against the number of elements of the buffer each writes: a store at or past the
+// end is not performed, and the kernel reports kDevBounds with the store's site (below) in
+// the status word.  Any other build stores unconditionally (the same code as a plain store).
+enum StoreSite : unsigned int { kStoreY = 100, kStorePre, kStorePost, kStoreComb, kStorePart };
+
+template <typename T>
+__device__ __forceinline__ void store_checked(T *base, size_t i, size_t n, const T &v, StatusBlock *sb,
+                                              unsigned int site)
+{
+#ifdef HC_DEBUG_BOUNDS
+    if (i >= n) {
+        report_error(sb, kDevBounds, site);
+        return;
+    }
+#else
+    (void)n;
+    (void)sb;
+    (void)site;
+#endif
+    base[i] = v;
 }
 
 // ---------------------------------------------------------------- device properties (host)

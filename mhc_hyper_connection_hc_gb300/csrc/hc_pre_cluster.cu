@@ -74,6 +74,7 @@
 #include "hc_ptx.cuh"
 
 #include <algorithm>
+#include <cstdlib>
 #include <cmath>
 #include <mutex>
 
@@ -217,6 +218,7 @@ struct Params {
     StatusBlock *status;
     unsigned long long *stamps;   // phase stamps (HC_STAMPS builds), else null
     int T, d, hs, hsc, LK, NJ, iters, tm_tile, ntiles;
+    int y_rows;   // rows of y (the call's T): bounds of the bounds-checked build's y stores
     float eps, invK;   // invK = 1 / (s*d)
 };
 
@@ -736,7 +738,8 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const __gri
                     a.z = fmaf(pr[k], xv.z, a.z);
                     a.w = fmaf(pr[k], xv.w, a.w);
                 }
-                *reinterpret_cast<float4 *>(p.y + (size_t)(t0 + t) * p.d + (size_t)rank * p.hs + 4 * h4) = a;
+                store_checked(reinterpret_cast<float4 *>(p.y), ((size_t)(t0 + t) * p.d + (size_t)rank * p.hs + 4 * h4) / 4,
+                              (size_t)p.y_rows * p.d / 4, a, p.status, kStoreY);
             }
             if (threadIdx.x == 0)
                 HC_STAMP(itc, kEvCollapsed);
@@ -1042,9 +1045,9 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const __gri
                     const size_t tok = (size_t)t0 + rank;
                     if (lane < S) {
                         if (p.pre)   // the head's gates are an optional output
-                            p.pre[tok * S + lane] = pre_v;
+                            store_checked(p.pre, tok * S + lane, (size_t)p.T * S, pre_v, p.status, kStorePre);
                     } else if (!HEAD && lane < 2 * S) {
-                        p.post[tok * S + (lane - S)] = 2.f * sg;
+                        store_checked(p.post, tok * S + (lane - S), (size_t)p.T * S, 2.f * sg, p.status, kStorePost);
                     }
                 }
                 __syncwarp();
@@ -1071,10 +1074,10 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const __gri
                     for (int q = 0; q < S * S; ++q)
                         cm[q] = src[q];
                     sinkhorn_regs<S>(cm, p.iters, p.eps);
-                    float *dst = p.comb + (size_t)(t0 + lane) * S * S;
     #pragma unroll
                     for (int q = 0; q < S * S; ++q)
-                        dst[q] = cm[q];
+                        store_checked(p.comb, (size_t)(t0 + lane) * S * S + q, (size_t)p.T * S * S, cm[q], p.status,
+                                      kStoreComb);
                 }
                 __syncwarp();
                 if (lane == 0) {
@@ -1212,7 +1215,7 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const __gri
                     const float4 pv = ptx::lds128(ptx::smem_u32(preb + (q * kTMT + t) * 4));
                     const float pr[4] = {pv.x, pv.y, pv.z, pv.w};
                     const uint32_t xrow = ptx::smem_u32(stages + (it % L.nst) * stage_floats + t * p.LK);
-                    float *yrow = p.y + (size_t)(t0 + t) * p.d + (size_t)rank * p.hs;
+                    const size_t y4 = ((size_t)(t0 + t) * p.d + (size_t)rank * p.hs) / 4;   // y row, float4s
                     for (int h0 = hb; h0 < h4n; h0 += 8 * U) {
                         float4 xv[U][S];
     #pragma unroll
@@ -1236,7 +1239,8 @@ __global__ void __launch_bounds__(kThreads, 1) hc_pre_cluster_kernel(const __gri
                                 a.z = fmaf(pr[k], xv[u][k].z, a.z);
                                 a.w = fmaf(pr[k], xv[u][k].w, a.w);
                             }
-                            *reinterpret_cast<float4 *>(yrow + 4 * h4) = a;
+                            store_checked(reinterpret_cast<float4 *>(p.y), y4 + h4, (size_t)p.y_rows * p.d / 4, a,
+                                          p.status, kStoreY);
                             if (p.z) {
                                 ssy = fmaf(a.x, a.x, ssy);
                                 ssy = fmaf(a.y, a.y, ssy);
@@ -1331,6 +1335,7 @@ struct HParams {
     float *part;             // [tokens from t0][2 * kCS][RV]: the helper tokens' partials
     StatusBlock *status;
     int T, d, hs, hsc, LK, NJ, iters;
+    int y_rows;              // rows of y (the call's T), as in Params
     int t0;                  // first helper token
     int ntiles;              // helper tiles: tile i holds tokens [t0 + kHT*i, t0 + kHT*i + kHT) below T
     float eps, invK;
@@ -1632,7 +1637,8 @@ __global__ void __launch_bounds__(kHThreads, 1) hc_pre_helper_kernel(const __gri
                     }
                     if (vid >= 0 && i < ntok_h) {
                         const int tr = t0 + slot0 + i - p.t0;
-                        p.part[((size_t)tr * 2 * kCS + 2 * c + half) * G::RV + vid] = v[m];
+                        store_checked(p.part, ((size_t)tr * 2 * kCS + 2 * c + half) * G::RV + vid,
+                                      (size_t)(p.T - p.t0) * 2 * kCS * G::RV, v[m], p.status, kStorePart);
                     }
                 }
                 if (!fused) {
@@ -1694,10 +1700,10 @@ __global__ void __launch_bounds__(kHThreads, 1) hc_pre_helper_kernel(const __gri
             const size_t tok = (size_t)tok0 + i;
             if (lane < S) {
                 const float pre_v = sg + p.eps;
-                p.pre[tok * S + lane] = pre_v;
+                store_checked(p.pre, tok * S + lane, (size_t)p.T * S, pre_v, p.status, kStorePre);
                 pre_s[i * 4 + lane] = pre_v;
             } else if (lane < 2 * S) {
-                p.post[tok * S + (lane - S)] = 2.f * sg;
+                store_checked(p.post, tok * S + (lane - S), (size_t)p.T * S, 2.f * sg, p.status, kStorePost);
             } else if (lane < G::R) {
                 sink_s[i * 16 + (lane - 2 * S)] = __expf(logit);
             }
@@ -1709,10 +1715,9 @@ __global__ void __launch_bounds__(kHThreads, 1) hc_pre_helper_kernel(const __gri
             for (int m = 0; m < S * S; ++m)
                 cm[m] = sink_s[i * 16 + m];
             sinkhorn_regs<S>(cm, p.iters, p.eps);
-            float *dst = p.comb + (size_t)(tok0 + i) * S * S;
 #pragma unroll
             for (int m = 0; m < S * S; ++m)
-                dst[m] = cm[m];
+                store_checked(p.comb, (size_t)(tok0 + i) * S * S + m, (size_t)p.T * S * S, cm[m], p.status, kStoreComb);
         }
         for (int i = 0; ok && i < ntok; ++i, ++tl) {   // y, in the collapse's order
             const int b = tl % kHB;
@@ -1723,7 +1728,7 @@ __global__ void __launch_bounds__(kHThreads, 1) hc_pre_helper_kernel(const __gri
             const float4 *xs4 = reinterpret_cast<const float4 *>(tbuf + (size_t)b * (16 * kMaxLK));
             const float4 pv = *reinterpret_cast<const float4 *>(pre_s + i * 4);
             const float pr[4] = {pv.x, pv.y, pv.z, pv.w};
-            float *yrow = p.y + (size_t)(tok0 + i) * p.d;
+            const size_t y4 = (size_t)(tok0 + i) * p.d / 4;   // y row, float4s
             for (int e = threadIdx.x; e < d4; e += kHThreads) {
                 float4 xv[S];
 #pragma unroll
@@ -1737,7 +1742,7 @@ __global__ void __launch_bounds__(kHThreads, 1) hc_pre_helper_kernel(const __gri
                     a.z = fmaf(pr[k], xv[k].z, a.z);
                     a.w = fmaf(pr[k], xv[k].w, a.w);
                 }
-                *reinterpret_cast<float4 *>(yrow + 4 * e) = a;
+                store_checked(reinterpret_cast<float4 *>(p.y), y4 + e, (size_t)p.y_rows * p.d / 4, a, p.status, kStoreY);
             }
             __syncthreads();   // buffer b is free
             if (threadIdx.x == 0 && i + kHB < ntok)
@@ -1996,6 +2001,7 @@ cudaError_t launch_helper(const Params &p, const HelperPlan &hp, int T, void *wo
     h.part = reinterpret_cast<float *>(static_cast<char *>(workspace) + kStatusBytes + kWorkspaceExtra);
     h.status = p.status;
     h.T = T;
+    h.y_rows = p.y_rows;
     h.d = p.d;
     h.hs = p.hs;
     h.hsc = p.hsc;
@@ -2061,6 +2067,13 @@ cudaError_t run_s(const float *x, const float *fn_w, const float *scale, const f
     p.iters = iters;
     p.eps = eps;
     p.invK = 1.0f / (float)(S * d);
+    p.y_rows = T;
+#ifdef HC_DEBUG_BOUNDS
+    // Bounds-checked build only: pretend y has fewer rows, so that the checks' report can be
+    // tested (the stores they refuse are inside the real buffer).
+    if (const char *e = getenv("HC_DEBUG_BOUNDS_Y_ROWS"))
+        p.y_rows = atoi(e);
+#endif
     // Every decode instantiation has the same footprint; NT = 8 bounds the others.
     const int nc_decode = max_clusters_for<S, false, 8, HEAD>(device);
     const int nc_persist = max_clusters_for<S, true, 4, HEAD>(device);
