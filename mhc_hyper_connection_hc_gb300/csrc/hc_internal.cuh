@@ -73,8 +73,8 @@ __device__ __forceinline__ void report_error(StatusBlock *sb, unsigned int code,
 
 // ---------------------------------------------------------------- bounds-checked stores
 // A build with -DHC_DEBUG_BOUNDS (build.build(bounds=True), a separate library) checks the
-// plain global stores of the cluster and helper kernels (y, pre, post, comb and the helper's
-// partials) against the number of elements of the buffer each writes: a store at or past the
+// plain global stores of the cluster, helper and wide kernels (y, pre, post, comb and the
+// helper's partials) against the number of elements of the buffer each writes: a store at or past the
 // end is not performed, and the kernel reports kDevBounds with the store's site (below) in
 // the status word.  Any other build stores unconditionally (the same code as a plain store).
 enum StoreSite : unsigned int { kStoreY = 100, kStorePre, kStorePost, kStoreComb, kStorePart };

@@ -58,6 +58,7 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <cstdlib>
 #include <mutex>
 
 #include "hc_internal.cuh"
@@ -110,6 +111,7 @@ struct WParams {
     float *part;        // [kWNp][ncta][kWM][RV]: each CTA's partials of a tile
     float *red;         // [kWNp][kWM][RV]: the tile's sums over every CTA
     int T, d, ntiles, ncta, iters;
+    int y_rows;            // rows of y (T): bounds of the bounds-checked build's y stores
     int nst, ncs;          // dot-ring and collapse-ring stages
     int nwide, hw0, hw1;   // CTAs [0, nwide) own hw0 columns, the rest hw1
     float eps, invK;       // invK = 1 / (s*d)
@@ -685,9 +687,10 @@ __global__ void __launch_bounds__(kWThreads, 1) hc_pre_wide_kernel(const __grid_
                 if (r < 2 * S) {
                     const float sg = 1.f / (1.f + expf(-logit));
                     if (r < S)
-                        p.pre[(size_t)(t0 + i) * S + r] = sg + p.eps;
+                        store_checked(p.pre, (size_t)(t0 + i) * S + r, (size_t)p.T * S, sg + p.eps, p.status, kStorePre);
                     else
-                        p.post[(size_t)(t0 + i) * S + (r - S)] = 2.f * sg;
+                        store_checked(p.post, (size_t)(t0 + i) * S + (r - S), (size_t)p.T * S, 2.f * sg, p.status,
+                                      kStorePost);
                 } else {
                     ex[i * S * S + (r - 2 * S)] = expf(logit);
                 }
@@ -707,10 +710,10 @@ __global__ void __launch_bounds__(kWThreads, 1) hc_pre_wide_kernel(const __grid_
                 cm[k] = act ? ex[t * S * S + j * S + k] : 0.f;
             w_sinkhorn_rows<S>(cm, p.iters, p.eps, lane);
             if (act) {
-                float *dst = p.comb + (size_t)(t0 + t) * S * S + j * S;
 #pragma unroll
                 for (int k = 0; k < S; ++k)
-                    dst[k] = cm[k];
+                    store_checked(p.comb, (size_t)(t0 + t) * S * S + j * S + k, (size_t)p.T * S * S, cm[k], p.status,
+                                  kStoreComb);
             }
             __syncwarp();
             if (lane == 0)
@@ -764,7 +767,8 @@ __global__ void __launch_bounds__(kWThreads, 1) hc_pre_wide_kernel(const __grid_
                         a.z = fmaf(pr[k], xv.z, a.z);
                         a.w = fmaf(pr[k], xv.w, a.w);
                     }
-                    *reinterpret_cast<float4 *>(p.y + (size_t)(it * kWM + i) * p.d + h0 + 4 * c4) = a;
+                    store_checked(reinterpret_cast<float4 *>(p.y), ((size_t)(it * kWM + i) * p.d + h0 + 4 * c4) / 4,
+                                  (size_t)p.y_rows * p.d / 4, a, p.status, kStoreY);
                 }
                 __syncwarp();
                 if (lane == 0) {
@@ -965,6 +969,13 @@ cudaError_t run_wide(const float *x, const float *fn_w, const float *scale, cons
     p.ncs = sp.ncs;
     p.eps = eps;
     p.invK = 1.0f / (float)(S * d);
+    p.y_rows = T;
+#ifdef HC_DEBUG_BOUNDS
+    // Bounds-checked build only: pretend y has fewer rows, so that the checks' report can be
+    // tested (the stores they refuse are inside the real buffer).
+    if (const char *e = getenv("HC_DEBUG_BOUNDS_Y_ROWS"))
+        p.y_rows = atoi(e);
+#endif
 #ifdef HC_STAMPS
     p.stamps = reinterpret_cast<unsigned long long *>(static_cast<char *>(workspace) + kStatusBytes);
 #endif

@@ -1,5 +1,5 @@
-"""The bounds-checked build (build.build(bounds=True), -DHC_DEBUG_BOUNDS).  Its cluster and
-helper kernels check every plain global store (y, pre, post, comb, the helper's partials)
+"""The bounds-checked build (build.build(bounds=True), -DHC_DEBUG_BOUNDS).  Its cluster, helper
+and wide kernels check every plain global store (y, pre, post, comb, the helper's partials)
 against the size of the buffer it writes, and report a refused store in the workspace status
 word (code 2, the store's site) instead of performing it.  On valid calls the checks never
 fire: the outputs are the plain build's bits.  The report itself is exercised without any
@@ -19,8 +19,9 @@ pytestmark = pytest.mark.gpu
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
-# (T, s, d): decode variant, persistent clusters without a helper, clusters with the helper
-CASES = [(37, 4, 4096), (1000, 2, 2048), (4100, 4, 4096)]
+# (T, s, d): decode variant, persistent clusters without a helper, clusters with the helper,
+# the wide kernel
+CASES = [(37, 4, 4096), (1000, 2, 2048), (4100, 4, 4096), (9, 8, 7168)]
 
 _RUNNER = r"""
 import hashlib, json, sys
@@ -33,7 +34,8 @@ for T, s, d in CASES:
     inp = synth.site_inputs(31 + T, T, s, d)
     dv = {k: torch.from_numpy(v).cuda() for k, v in inp.items()}
     ws = hc.new_workspace(T, s, d)
-    row = {"T": T, "s": s, "d": d}
+    path = hc.hc_pre_auto_path(T, s, d)
+    row = {"T": T, "s": s, "d": d, "path": {hc.HC_PATH_CLUSTER: "cluster", hc.HC_PATH_WIDE: "wide"}.get(path, "other")}
     for mode in ("pre", "fused"):
         out = hc.new_pre_outputs(T, s, d)
         for v in out.values():
@@ -89,6 +91,7 @@ def test_bounds_build_gives_the_plain_build_bits():
             assert a[mode]["hash"] == b[mode]["hash"], f"T={a['T']} s={a['s']} {mode}: outputs differ"
             assert b[mode]["y_rows_written"] == a["T"]
     assert any(r["fused"]["helper_tokens"] > 0 for r in checked), "no case ran the helper kernel"
+    assert [r["path"] for r in checked] == ["cluster", "cluster", "cluster", "wide"], "cases left their paths"
 
 
 def test_bounds_build_reports_a_refused_store_and_skips_it():
