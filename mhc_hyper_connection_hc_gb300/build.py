@@ -8,8 +8,8 @@ _lib/stamps/libmhc_gb300_stamps.so: the same library, whose cluster pre kernel a
 writes %globaltimer stamps at phase boundaries into the workspace (see hc_internal.cuh).
 
 build(bounds=True) builds the bounds-checked variant, with -DHC_DEBUG_BOUNDS, as
-_lib/bounds/libmhc_gb300_bounds.so: the cluster and helper kernels check each global
-store against its buffer's size and report a refused store in the status word instead
+_lib/bounds/libmhc_gb300_bounds.so: the cluster, helper and wide kernels check each
+global output store against its buffer's size and report a refused store in the status word instead
 of performing it (see hc_internal.cuh).
 """
 
