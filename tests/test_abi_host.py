@@ -269,3 +269,13 @@ def test_binding_refuses_bad_tensors_before_any_call():
     with pytest.raises(ValueError, match=r"\[T, s, d\]"):
         hc._shape(torch.zeros(4, 4))
     assert hc._shape(torch.zeros(2, 3, 8)) == (2, 3, 8)
+
+
+def test_build_variants_are_separate_libraries():
+    """The phase-stamp and bounds-checked variants build into their own directories, never over
+    the product library, and one call builds one variant."""
+    from mhc_hyper_connection_hc_gb300 import build
+    libs = {build.LIB, build.STAMPS_LIB, build.BOUNDS_LIB}
+    assert len(libs) == 3 and len({os.path.dirname(p) for p in libs}) == 3
+    with pytest.raises(ValueError):
+        build.build(stamps=True, bounds=True)
