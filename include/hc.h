@@ -114,7 +114,10 @@ int hc_workspace_init(void *workspace, size_t ws_bytes, void *stream);
 /*
  * Read the workspace status word (synchronises `stream`): HC_OK, or
  * HC_ERR_DEVICE if a kernel gave up on a bounded wait.  The word is sticky
- * until hc_workspace_init clears it.
+ * until hc_workspace_init clears it.  Its first 32-bit field is the code (1: a
+ * bounded wait gave up; 2, only in the bounds-checked build of the library: a
+ * store outside its buffer was refused), the second the site, the third the
+ * reporting block.
  *
  * Outputs are valid only while the word reads HC_OK.  While it is non-zero,
  * every later hc_pre_fused, hc_post_pre_fused and hc_head call on that
